@@ -1,0 +1,215 @@
+"""Fused equivariant message passing (l <= 3) for GB300: Python binding.
+
+A thin ctypes layer over the C ABI of ``libeqmp.so`` (declared in
+include/eqmp.h).  Each function takes torch CUDA tensors, checks dtypes and
+shapes, passes raw device pointers and the current CUDA stream, and raises
+``EqmpError`` on a non-OK status.  All arithmetic happens in the library's
+CUDA kernels; there is no CPU path.  PyTorch supplies device memory and
+streams only.
+
+Entry points (same names as the C ABI):
+  eqmp_sh(vec, Y=None)                         -> Y [E, 16]
+  eqmp_tp_scatter(Y, x, row_offsets, src, ...)  -> out [N, C, 16]
+  eqmp_fused(vec, x, row_offsets, src, ...)     -> out [N, C, 16]
+  eqmp_validate_graph(row_offsets, src, n_src, n_edges)
+  eqmp_device_error()                           -> int (watchdog code)
+  eqmp_path_table()                             -> list of (l1, l2, l3)
+"""
+import ctypes
+import os
+
+__all__ = [
+    "EqmpError", "load_library", "library_path", "eqmp_num_paths", "eqmp_path_table",
+    "eqmp_status_string", "eqmp_sh", "eqmp_tp_scatter", "eqmp_fused", "eqmp_validate_graph",
+    "eqmp_device_error", "EQMP_OK", "EQMP_ERR_INVALID_ARG", "EQMP_ERR_UNSUPPORTED",
+    "EQMP_ERR_CUDA", "EQMP_ERR_DEVICE_TIMEOUT", "EQMP_ERR_GRAPH",
+]
+
+EQMP_OK, EQMP_ERR_INVALID_ARG, EQMP_ERR_UNSUPPORTED, EQMP_ERR_CUDA = 0, 1, 2, 3
+EQMP_ERR_DEVICE_TIMEOUT, EQMP_ERR_GRAPH = 4, 5
+EQMP_F32, EQMP_BF16 = 0, 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "libeqmp.so")
+_lib = None
+
+
+class EqmpError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {_status_text(status)} (status {status})")
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [("w", ctypes.c_void_p), ("R", ctypes.c_void_p), ("M", ctypes.c_void_p),
+                ("K", ctypes.c_int32)]
+
+
+def library_path():
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libeqmp.so (built by ``__graft_entry__.build()``); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"libeqmp.so is not built ({_LIB_PATH}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(_LIB_PATH)
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    lib.eqmp_num_paths.restype = i32
+    lib.eqmp_path_table.argtypes = [ctypes.POINTER(i32)]
+    lib.eqmp_path_table.restype = i32
+    lib.eqmp_status_string.argtypes = [i32]
+    lib.eqmp_status_string.restype = ctypes.c_char_p
+    lib.eqmp_sh.argtypes = [vp, i64, vp, vp]
+    lib.eqmp_sh.restype = i32
+    layer = [vp, vp, i64, i32, vp, vp, i64, i64, i32, Weights, vp, i32, vp]
+    lib.eqmp_tp_scatter.argtypes = layer
+    lib.eqmp_tp_scatter.restype = i32
+    lib.eqmp_fused.argtypes = layer
+    lib.eqmp_fused.restype = i32
+    lib.eqmp_validate_graph.argtypes = [vp, vp, i64, i64, i64, vp]
+    lib.eqmp_validate_graph.restype = i32
+    lib.eqmp_device_error.argtypes = [ctypes.POINTER(i32)]
+    lib.eqmp_device_error.restype = i32
+    _lib = lib
+    return lib
+
+
+def _status_text(status):
+    try:
+        return load_library().eqmp_status_string(int(status)).decode()
+    except Exception:  # pragma: no cover - library absent
+        return "status"
+
+
+def _check(status, where):
+    if status != EQMP_OK:
+        raise EqmpError(status, where)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream):
+    import torch
+
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _require(t, name, dtype=None, cuda=True):
+    import torch
+
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if cuda and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError(f"{name} has dtype {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def eqmp_num_paths():
+    return int(load_library().eqmp_num_paths())
+
+
+def eqmp_path_table():
+    lib = load_library()
+    buf = (ctypes.c_int32 * (3 * 34))()
+    _check(lib.eqmp_path_table(buf), "eqmp_path_table")
+    return [tuple(buf[3 * p:3 * p + 3]) for p in range(lib.eqmp_num_paths())]
+
+
+def eqmp_status_string(status):
+    return load_library().eqmp_status_string(int(status)).decode()
+
+
+def eqmp_sh(vec, Y=None, stream=None):
+    """Y[E, 16] = real SH (l <= 3) of vec[E, 3] (fp32, CUDA)."""
+    import torch
+
+    _require(vec, "vec", torch.float32)
+    E = vec.shape[0] if vec.dim() == 2 else -1
+    if vec.dim() != 2 or vec.shape[1] != 3:
+        raise ValueError("vec must be [E, 3]")
+    if Y is None:
+        Y = torch.empty((E, 16), dtype=torch.float32, device=vec.device)
+    _require(Y, "Y", torch.float32)
+    if tuple(Y.shape) != (E, 16):
+        raise ValueError("Y must be [E, 16]")
+    _check(load_library().eqmp_sh(_ptr(vec), E, _ptr(Y), _stream(stream)), "eqmp_sh")
+    return Y
+
+
+def _layer(fn_name, edge_in, x, row_offsets, src, w, R, M, out, stream, n_edges):
+    import torch
+
+    _require(x, "x", (torch.float32, torch.bfloat16))
+    _require(row_offsets, "row_offsets", torch.int32)
+    _require(src, "src", torch.int32)
+    for name, t in (("w", w), ("R", R), ("M", M)):
+        _require(t, name, torch.float32)
+    if x.dim() != 3 or x.shape[2] != 16:
+        raise ValueError("x must be [N_src, C, 16]")
+    n_src, C = x.shape[0], x.shape[1]
+    N = row_offsets.shape[0] - 1
+    E = n_edges if n_edges is not None else edge_in.shape[0]
+    if out is None:
+        out = torch.empty((N, C, 16), dtype=x.dtype, device=x.device)
+    _require(out, "out", x.dtype)
+    if tuple(out.shape) != (N, C, 16):
+        raise ValueError("out must be [N, C, 16]")
+    dt = EQMP_BF16 if x.dtype == torch.bfloat16 else EQMP_F32
+    if w is not None:
+        wt = Weights(ctypes.c_void_p(w.data_ptr()), None, None, 0)
+    else:
+        wt = Weights(None, ctypes.c_void_p(R.data_ptr()) if R is not None else None,
+                     ctypes.c_void_p(M.data_ptr()) if M is not None else None,
+                     R.shape[1] if R is not None and R.dim() == 2 else 0)
+    fn = getattr(load_library(), fn_name)
+    st = fn(_ptr(edge_in), _ptr(x), n_src, dt, _ptr(row_offsets), _ptr(src), N, E, C, wt,
+            _ptr(out), dt, _stream(stream))
+    _check(st, fn_name)
+    return out
+
+
+def eqmp_tp_scatter(Y, x, row_offsets, src, w=None, R=None, M=None, out=None, stream=None,
+                    n_edges=None):
+    """out[N, C, 16] = receiver sum of CG(x[src], Y) with shared w or radial (R, M)."""
+    import torch
+
+    _require(Y, "Y", torch.float32)
+    return _layer("eqmp_tp_scatter", Y, x, row_offsets, src, w, R, M, out, stream, n_edges)
+
+
+def eqmp_fused(vec, x, row_offsets, src, w=None, R=None, M=None, out=None, stream=None,
+               n_edges=None):
+    """out[N, C, 16] = receiver sum of CG(x[src], SH(vec)), one fused kernel."""
+    import torch
+
+    _require(vec, "vec", torch.float32)
+    return _layer("eqmp_fused", vec, x, row_offsets, src, w, R, M, out, stream, n_edges)
+
+
+def eqmp_validate_graph(row_offsets, src, n_src, n_edges, stream=None):
+    """Raise EqmpError(EQMP_ERR_GRAPH) if the CSR preconditions do not hold."""
+    N = row_offsets.shape[0] - 1
+    st = load_library().eqmp_validate_graph(_ptr(row_offsets), _ptr(src), N, int(n_src),
+                                            int(n_edges), _stream(stream))
+    _check(st, "eqmp_validate_graph")
+
+
+def eqmp_device_error():
+    """Watchdog code since the last call (0 = no device wait gave up)."""
+    code = ctypes.c_int32(0)
+    st = load_library().eqmp_device_error(ctypes.byref(code))
+    if st not in (EQMP_OK, EQMP_ERR_DEVICE_TIMEOUT):
+        _check(st, "eqmp_device_error")
+    return int(code.value)

@@ -1,0 +1,193 @@
+// Device helpers shared by the eqmp kernels (sm_103a).
+//
+//  * inline-PTX wrappers for mbarriers and TMA tensor loads, every wait
+//    bounded by the global nanosecond timer (a wait that gives up records a
+//    code in the device watchdog word and returns false; nothing traps);
+//  * the register-resident real spherical harmonics, l <= 3 (Batmobile blog
+//    "Batmobile CUDA内核优化", section "2. 寄存器中间计算");
+//  * compile-time expansion of the generated CG tables (section
+//    "1. 编译时常量": coefficients folded into the instruction stream).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <utility>
+
+#include "eqmp_tables.h"
+
+namespace eqmp {
+
+// ---------------------------------------------------------------- watchdog
+// The watchdog word lives in device memory owned by the library (one per
+// device); kernels receive its address.  It becomes nonzero once any
+// bounded wait has given up and is read and cleared by eqmp_device_error().
+// Codes: 1 consumer full-wait, 2 producer empty-wait, 3 producer drain.
+
+constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void watchdog_trip(int* wd, int code) { atomicCAS(wd, 0, code); }
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase of `parity` to complete; false (and the watchdog
+// set to `code`) if it has not completed within kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* wd, int code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      watchdog_trip(wd, code);
+      return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- TMA
+// 2-D tiled tensor load global -> shared, completion on an mbarrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// Named barrier over `count` threads (count a multiple of 32).
+__device__ __forceinline__ void named_barrier(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// ---------------------------------------------------------------- storage
+template <typename T>
+struct Storage;
+
+template <>
+struct Storage<float> {
+  static __device__ __forceinline__ float load(float v) { return v; }
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Round-to-nearest-even pack of two floats into bf16x2 (lo in low half).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ---------------------------------------------------------------- SH
+// Real SH for one edge vector: Y_lm = poly_lm(z) * {Re, Im}(x + i y)^|m| on
+// the unit sphere, poly coefficients (normalisation folded in) from the
+// generated table.  Zero-length vectors give n = 0 and Y_{l>=1} = 0.
+constexpr float sh_coef(int l, int m, int p) { return tables::kShPoly[l][m][p]; }
+
+template <int L, int M>
+__device__ __forceinline__ float sh_poly(float z) {
+  constexpr float c0 = sh_coef(L, M, 0);
+  constexpr float c1 = sh_coef(L, M, 1);
+  constexpr float c2 = sh_coef(L, M, 2);
+  constexpr float c3 = sh_coef(L, M, 3);
+  // Horner; zero coefficients fold away.
+  return fmaf(fmaf(fmaf(c3, z, c2), z, c1), z, c0);
+}
+
+__device__ __forceinline__ void real_sh16(float vx, float vy, float vz, float (&Y)[16]) {
+  const float r2 = fmaf(vx, vx, fmaf(vy, vy, vz * vz));
+  const bool nonzero = r2 >= 1e-30f;
+  const float inv = nonzero ? rsqrtf(r2) : 0.0f;
+  const float x = vx * inv, y = vy * inv, z = vz * inv;
+  // (x + i y)^m
+  const float c1 = x, s1 = y;
+  const float c2 = fmaf(x, x, -y * y), s2 = 2.0f * x * y;
+  const float c3 = fmaf(x, c2, -y * s2), s3 = fmaf(x, s2, y * c2);
+  Y[0] = sh_poly<0, 0>(z);
+  Y[2] = sh_poly<1, 0>(z);
+  { const float p = sh_poly<1, 1>(z); Y[3] = p * c1; Y[1] = p * s1; }
+  Y[6] = sh_poly<2, 0>(z);
+  { const float p = sh_poly<2, 1>(z); Y[7] = p * c1; Y[5] = p * s1; }
+  { const float p = sh_poly<2, 2>(z); Y[8] = p * c2; Y[4] = p * s2; }
+  Y[12] = sh_poly<3, 0>(z);
+  { const float p = sh_poly<3, 1>(z); Y[13] = p * c1; Y[11] = p * s1; }
+  { const float p = sh_poly<3, 2>(z); Y[14] = p * c2; Y[10] = p * s2; }
+  { const float p = sh_poly<3, 3>(z); Y[15] = p * c3; Y[9] = p * s3; }
+  if (!nonzero) {
+#pragma unroll
+    for (int k = 1; k < 16; ++k) Y[k] = 0.0f;
+  }
+}
+
+// ---------------------------------------------------------------- CG tables
+// Compile-time accessors and queries over the generated term list.
+constexpr tables::Term term_at(int i) { return tables::kTerms[i]; }
+constexpr tables::Path path_at(int p) { return tables::kPaths[p]; }
+
+constexpr int l_of_k(int k) { return k < 1 ? 0 : (k < 4 ? 1 : (k < 9 ? 2 : 3)); }
+
+// Does path P have a term with k1 in [k1lo, k1lo + n) and output k3?
+constexpr bool path_has(int P, int k1lo, int n, int k3) {
+  for (int i = tables::kPaths[P].first; i < tables::kPaths[P].first + tables::kPaths[P].count; ++i)
+    if (tables::kTerms[i].k3 == k3 && tables::kTerms[i].k1 >= k1lo && tables::kTerms[i].k1 < k1lo + n)
+      return true;
+  return false;
+}
+
+constexpr bool path_touches(int P, int k1lo, int n) {
+  for (int k3 = 0; k3 < 16; ++k3)
+    if (path_has(P, k1lo, n, k3)) return true;
+  return false;
+}
+
+}  // namespace eqmp

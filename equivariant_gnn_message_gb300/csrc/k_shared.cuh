@@ -1,0 +1,309 @@
+// Fused SH + CG tensor product + receiver sum, shared per-path weights.
+//
+// What it computes (Batmobile blog "Batmobile CUDA内核优化", section
+// "3. 操作融合", extended with the receiver sum):
+//   out[i,c,k3] = sum_p w[p,c] sum_{k1,k2} C_p[k3,k1,k2] sum_{e->i} x[src_e,c,k1] Y_e[k2]
+// Because the weights do not depend on the edge, the edge sum is taken
+// first: A[c,k1,k2] = sum_{e->i} x[src_e,c,k1] Y_e[k2] (256 FMAs per edge
+// and channel), then contracted once per receiver with the 611 CG terms and
+// the 34 path weights.  The result is the same sum in another order.
+//
+// Organisation of one CTA (persistent; owns a contiguous receiver range):
+//   * producer warp: for its edges, in CSR order, computes the 16 SH in
+//     registers (or reads them, for the unfused tp_scatter entry point),
+//     stores them in the slot's Y area and issues ONE TMA tensor load of the
+//     sender's feature row x[src] (C*16 elements) into the slot, with
+//     128-byte swizzle; ring of S slots with full/empty mbarriers.
+//   * consumer warps: thread (c, q) holds A[c, q*KQ .. q*KQ+KQ-1, 0..15] in
+//     registers.  Per edge: wait full, 4 broadcast LDS.128 of Y, one
+//     conflict-free swizzled LDS of x, KQ*16 FFMAs, release the slot.  At the
+//     end of a receiver: contraction with compile-time CG constants, partial
+//     sums over the NQ quads through shared memory, one store per output.
+//   * the receiver sum is in CSR order, deterministic, with no atomics.
+#pragma once
+
+#include <cuda.h>
+
+#include "common.cuh"
+#include "layer_args.cuh"
+
+namespace eqmp {
+
+template <int C, int KQ, typename XT, bool FROM_VEC>
+struct SharedCfg {
+  static constexpr int NQ = 16 / KQ;                 // quads of k1 per channel
+  static constexpr int NCONS = C * NQ;               // consumer threads
+  static constexpr int NCW = NCONS / 32;             // consumer warps
+  static constexpr int NTHREADS = NCONS + 32;        // + producer warp
+  static constexpr int ROW_BYTES = C * 16 * (int)sizeof(XT);
+  static constexpr int ROWS = ROW_BYTES / 128;        // 128-byte TMA box rows per node
+  static constexpr int INNER = 128 / (int)sizeof(XT);  // elements per box row
+  static constexpr int SLOT = ROW_BYTES < 1024 ? 1024 : ROW_BYTES;  // swizzle atom aligned
+  static constexpr int S = (SLOT * 16 <= 65536) ? 16 : (65536 / SLOT < 4 ? 4 : 65536 / SLOT);
+  static constexpr int OFF_X = 0;
+  static constexpr int OFF_Y = OFF_X + S * SLOT;
+  static constexpr int OFF_RED = OFF_Y + S * 64;
+  static constexpr int OFF_W = OFF_RED + 2 * NQ * 16 * C * 4;
+  static constexpr int OFF_BAR = OFF_W + 34 * C * 4;
+  static constexpr int SMEM_BYTES = OFF_BAR + 2 * S * 8 + 1024;  // + base alignment slack
+  static constexpr int XBYTES = KQ * (int)sizeof(XT);              // bytes of x per thread per edge
+  static constexpr int MIN_BLOCKS = KQ == 4 ? 2 : 1;               // CTAs per SM the registers allow
+  static_assert(NCONS % 32 == 0, "consumer threads must fill warps");
+  static_assert(XBYTES == 8 || XBYTES == 16 || XBYTES == 32, "unsupported x chunk");
+  static_assert(ROW_BYTES % 128 == 0, "row must be whole 128-byte lines");
+};
+
+// Byte offset of logical byte o of a node row inside its 128B-swizzled slot.
+__device__ __forceinline__ uint32_t swz128(uint32_t o) {
+  return (o & ~0x7Fu) | ((((o >> 4) ^ (o >> 7)) & 7u) << 4) | (o & 15u);
+}
+
+// ---- compile-time contraction: partial outputs of quad Q -----------------
+template <int KQ, int Q, int I>
+__device__ __forceinline__ void apply_term(const float (&acc)[KQ][16], float (&tmp)[16]) {
+  constexpr tables::Term t = term_at(I);
+  if constexpr (t.k1 >= Q * KQ && t.k1 < Q * KQ + KQ)
+    tmp[t.k3] = fmaf(t.c, acc[t.k1 - Q * KQ][t.k2], tmp[t.k3]);
+}
+
+template <int KQ, int Q, int First, int... Is>
+__device__ __forceinline__ void apply_terms(const float (&acc)[KQ][16], float (&tmp)[16],
+                                            std::integer_sequence<int, Is...>) {
+  (apply_term<KQ, Q, First + Is>(acc, tmp), ...);
+}
+
+template <int KQ, int Q, int P, int... K3>
+__device__ __forceinline__ void weight_outputs(float w, const float (&tmp)[16], float (&part)[16],
+                                               std::integer_sequence<int, K3...>) {
+  ((path_has(P, Q * KQ, KQ, K3) ? (void)(part[K3] = fmaf(w, tmp[K3], part[K3])) : (void)0), ...);
+}
+
+template <int C, int KQ, int Q, int P>
+__device__ __forceinline__ void contract_path(const float (&acc)[KQ][16], const float* wcol,
+                                              float (&part)[16]) {
+  if constexpr (path_touches(P, Q * KQ, KQ)) {
+    constexpr tables::Path path = path_at(P);
+    float tmp[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) tmp[k] = 0.0f;
+    apply_terms<KQ, Q, path.first>(acc, tmp, std::make_integer_sequence<int, path.count>{});
+    const float w = wcol[P * C];
+    weight_outputs<KQ, Q, P>(w, tmp, part, std::make_integer_sequence<int, 16>{});
+  }
+}
+
+template <int C, int KQ, int Q, int... Ps>
+__device__ __forceinline__ void contract_quad(const float (&acc)[KQ][16], const float* wcol,
+                                              float (&part)[16], std::integer_sequence<int, Ps...>) {
+  (contract_path<C, KQ, Q, Ps>(acc, wcol, part), ...);
+}
+
+template <int C, int KQ>
+__device__ __forceinline__ void contract(int q, const float (&acc)[KQ][16], const float* wcol,
+                                         float (&part)[16]) {
+  using Seq = std::make_integer_sequence<int, tables::kNumPaths>;
+  if constexpr (KQ == 4) {
+    switch (q) {
+      case 0: contract_quad<C, KQ, 0>(acc, wcol, part, Seq{}); break;
+      case 1: contract_quad<C, KQ, 1>(acc, wcol, part, Seq{}); break;
+      case 2: contract_quad<C, KQ, 2>(acc, wcol, part, Seq{}); break;
+      default: contract_quad<C, KQ, 3>(acc, wcol, part, Seq{}); break;
+    }
+  } else {
+    if (q == 0) contract_quad<C, KQ, 0>(acc, wcol, part, Seq{});
+    else contract_quad<C, KQ, 1>(acc, wcol, part, Seq{});
+  }
+}
+
+// ---- x chunk load (KQ elements of one channel) from a swizzled slot -------
+template <typename XT, int KQ>
+__device__ __forceinline__ void load_x(const uint8_t* slot, uint32_t o, float (&xv)[KQ]) {
+  if constexpr (sizeof(XT) == 4) {
+#pragma unroll
+    for (int h = 0; h < KQ / 4; ++h) {
+      const float4 v = *reinterpret_cast<const float4*>(slot + swz128(o + 16 * h));
+      xv[4 * h + 0] = v.x; xv[4 * h + 1] = v.y; xv[4 * h + 2] = v.z; xv[4 * h + 3] = v.w;
+    }
+  } else if constexpr (KQ == 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(slot + swz128(o));
+    xv[0] = bf16_lo(v.x); xv[1] = bf16_hi(v.x); xv[2] = bf16_lo(v.y); xv[3] = bf16_hi(v.y);
+    xv[4] = bf16_lo(v.z); xv[5] = bf16_hi(v.z); xv[6] = bf16_lo(v.w); xv[7] = bf16_hi(v.w);
+  } else {
+    const uint2 v = *reinterpret_cast<const uint2*>(slot + swz128(o));
+    xv[0] = bf16_lo(v.x); xv[1] = bf16_hi(v.x); xv[2] = bf16_lo(v.y); xv[3] = bf16_hi(v.y);
+  }
+}
+
+template <typename XT, int KQ>
+__device__ __forceinline__ void store_out(void* out, size_t elem, const float (&o)[KQ]) {
+  if constexpr (sizeof(XT) == 4) {
+    float* p = reinterpret_cast<float*>(out) + elem;
+#pragma unroll
+    for (int h = 0; h < KQ / 4; ++h)
+      reinterpret_cast<float4*>(p)[h] = make_float4(o[4 * h], o[4 * h + 1], o[4 * h + 2], o[4 * h + 3]);
+  } else if constexpr (KQ == 8) {
+    uint4 v;
+    v.x = pack_bf16x2(o[0], o[1]); v.y = pack_bf16x2(o[2], o[3]);
+    v.z = pack_bf16x2(o[4], o[5]); v.w = pack_bf16x2(o[6], o[7]);
+    *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(out) + elem) = v;
+  } else {
+    uint2 v;
+    v.x = pack_bf16x2(o[0], o[1]); v.y = pack_bf16x2(o[2], o[3]);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + elem) = v;
+  }
+}
+
+template <int C, int KQ, typename XT, bool FROM_VEC>
+__global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
+                                  SharedCfg<C, KQ, XT, FROM_VEC>::MIN_BLOCKS)
+    k_shared(const __grid_constant__ CUtensorMap tmap, const LayerArgs a) {
+  using K = SharedCfg<C, KQ, XT, FROM_VEC>;
+  constexpr int S = K::S;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float4* ys = reinterpret_cast<float4*>(smem + K::OFF_Y);
+  float* red = reinterpret_cast<float*>(smem + K::OFF_RED);
+  float* ws = reinterpret_cast<float*>(smem + K::OFF_W);
+  const uint32_t full0 = smem_u32(smem + K::OFF_BAR);
+  const uint32_t empty0 = full0 + 8 * S;
+  const int tid = threadIdx.x;
+
+  // Contiguous receiver range of this CTA (equal receiver counts).
+  const int G = gridDim.x, b = blockIdx.x;
+  const int r_begin = (int)((long long)a.N * b / G);
+  const int r_end = (int)((long long)a.N * (b + 1) / G);
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, K::NCW);
+    }
+    fence_mbar_init();
+  }
+  for (int i = tid; i < 34 * C; i += K::NTHREADS) ws[i] = __ldg(a.w + i);
+  __syncthreads();
+
+  // Edge range, clamped into [0, E]: a malformed CSR cannot send a load
+  // out of bounds, and producer and consumers agree on the count.
+  const int e_begin = min(max(__ldg(a.off + r_begin), 0), a.E);
+  const int e_end = max(e_begin, min(max(__ldg(a.off + r_end), 0), a.E));
+  const int total = e_end - e_begin;
+
+  if (tid >= K::NCONS) {
+    // ------------------------------------------------------------ producer
+    const int lane = tid & 31;
+    if (lane == 0) prefetch_tmap(&tmap);
+    uint32_t n = 0;
+    bool ok = true;
+    for (int base = e_begin; base < e_end && ok; base += 32) {
+      const int e = base + lane;
+      float y[16];
+      int node = 0;
+      if (e < e_end) {
+        node = __ldg(a.src + e);
+        if constexpr (FROM_VEC) {
+          const float* v = a.vec + 3 * (size_t)e;
+          real_sh16(__ldg(v), __ldg(v + 1), __ldg(v + 2), y);
+        } else {
+          const float4* yp = reinterpret_cast<const float4*>(a.Y) + 4 * (size_t)e;
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const float4 t = __ldg(yp + h);
+            y[4 * h] = t.x; y[4 * h + 1] = t.y; y[4 * h + 2] = t.z; y[4 * h + 3] = t.w;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) y[k] = 0.0f;
+      }
+      const int cnt = min(32, e_end - base);
+      for (int j = 0; j < cnt; ++j) {
+        int good = 1;
+        if (lane == j) {
+          const uint32_t s = n % S, par = ((n / S) & 1u) ^ 1u;
+          if (mbar_wait(empty0 + 8 * s, par, a.watchdog, 2)) {
+            float4* yd = ys + 4 * s;
+            yd[0] = make_float4(y[0], y[1], y[2], y[3]);
+            yd[1] = make_float4(y[4], y[5], y[6], y[7]);
+            yd[2] = make_float4(y[8], y[9], y[10], y[11]);
+            yd[3] = make_float4(y[12], y[13], y[14], y[15]);
+            mbar_arrive_expect_tx(full0 + 8 * s, K::ROW_BYTES);
+            tma_load_2d(smem_u32(smem + K::OFF_X + s * K::SLOT), &tmap, 0, node * K::ROWS,
+                        full0 + 8 * s);
+          } else {
+            good = 0;
+          }
+        }
+        good = __shfl_sync(0xffffffffu, good, j);
+        if (!good) { ok = false; break; }
+        ++n;
+      }
+    }
+    // Drain: wait until the loads of the last min(S, n) issued edges have
+    // landed, so no bulk copy is in flight when this warp leaves.
+    if (lane == 0) {
+      const uint32_t first = n > (uint32_t)S ? n - S : 0;
+      for (uint32_t i = first; i < n; ++i)
+        if (!mbar_wait(full0 + 8 * (i % S), (i / S) & 1u, a.watchdog, 3)) break;
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int c = tid % C, q = tid / C, lane = tid & 31;
+  const uint32_t xo = (uint32_t)(c * 16 * (int)sizeof(XT) + q * K::XBYTES);
+  const float* wcol = ws + c;
+  uint32_t n = 0;
+  int buf = 0;
+  bool failed = false;
+  for (int r = r_begin; r < r_end; ++r) {
+    const int a0 = min(max(__ldg(a.off + r), 0), a.E);
+    const int a1 = min(max(__ldg(a.off + r + 1), 0), a.E);
+    const int deg = min(max(a1 - a0, 0), total - (int)n);
+    float acc[KQ][16];
+#pragma unroll
+    for (int i = 0; i < KQ; ++i)
+#pragma unroll
+      for (int k = 0; k < 16; ++k) acc[i][k] = 0.0f;
+
+    for (int j = 0; j < deg; ++j, ++n) {
+      const uint32_t s = n % S, par = (n / S) & 1u;
+      if (!failed && !mbar_wait(full0 + 8 * s, par, a.watchdog, 1)) failed = true;
+      const float4* yp = ys + 4 * s;
+      const float4 y0 = yp[0], y1 = yp[1], y2 = yp[2], y3 = yp[3];
+      const float yv[16] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w,
+                            y2.x, y2.y, y2.z, y2.w, y3.x, y3.y, y3.z, y3.w};
+      float xv[KQ];
+      load_x<XT, KQ>(smem + K::OFF_X + s * K::SLOT, xo, xv);
+#pragma unroll
+      for (int i = 0; i < KQ; ++i)
+#pragma unroll
+        for (int k = 0; k < 16; ++k) acc[i][k] = fmaf(xv[i], yv[k], acc[i][k]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    }
+
+    float part[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) part[k] = 0.0f;
+    contract<C, KQ>(q, acc, wcol, part);
+
+    float* rb = red + buf * (K::NQ * 16 * C);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) rb[(q * 16 + k) * C + c] = part[k];
+    named_barrier(1, K::NCONS);
+    float o[KQ];
+#pragma unroll
+    for (int i = 0; i < KQ; ++i) {
+      float sum = 0.0f;
+#pragma unroll
+      for (int qq = 0; qq < K::NQ; ++qq) sum += rb[(qq * 16 + q * KQ + i) * C + c];
+      o[i] = sum;
+    }
+    store_out<XT, KQ>(a.out, ((size_t)r * C + c) * 16 + q * KQ, o);
+    buf ^= 1;
+  }
+}
+
+}  // namespace eqmp

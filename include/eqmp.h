@@ -1,0 +1,161 @@
+/*
+ * eqmp.h - C ABI of libeqmp.so: fused equivariant message passing, l <= 3.
+ *
+ * One layer of the equivariant-GNN edge message.  For every edge e
+ * (sender src_e -> receiver i) it evaluates the 16 real orthonormal
+ * spherical harmonics Y_e of the edge vector, takes the channelwise
+ * Clebsch-Gordan tensor product with the sender's features over all 34
+ * triangle-allowed paths (l1, l2 -> l3, all <= 3) with per-path channel
+ * weights, and sums the messages into the receiver:
+ *
+ *   out[i, c, (l3,m3)] = sum_{e -> i} sum_{p=(l1,l2,l3)} W[e,p,c]
+ *                          sum_{m1,m2} C_p[m3,m1,m2] x[src_e, c, (l1,m1)] Y_e[(l2,m2)]
+ *
+ * Sources: "Batmobile CUDA内核优化：等变图神经网络的10-20倍加速策略" (blog
+ * post): section "2. 寄存器中间计算" (SH in registers, Y00 and the l = 1
+ * constants), section "1. 编译时常量" (34 compile-time CG entries for
+ * L_MAX = 3), section "3. 操作融合" (the fused kernel's arguments: edge
+ * vectors [E,3], node features [N,C,16], source indices [E]; one read of
+ * each edge vector; the message-passing sum as the third fused step).
+ *
+ * Conventions shared by every entry point
+ *   - Component index k = l*l + l + m, m = -l..l (16 per channel); real
+ *     SH with the Condon-Shortley phase (Y00 = 0.28209479, Y_1,-1 = -c y,
+ *     Y_10 = c z, Y_11 = -c x, c = 0.48860251).
+ *   - Path order for weights: l1 = 0..3, l2 = 0..3,
+ *     l3 = |l1-l2|..min(3, l1+l2)  (34 paths; eqmp_path_table lists them).
+ *     Real CG tables are unit-normalised CG coefficients in the real basis;
+ *     the 11 odd-parity paths (l1+l2+l3 odd) are taken as -i times the
+ *     (purely imaginary) transform.
+ *   - Graph: CSR by receiver.  row_offsets[N+1] holds ABSOLUTE indices into
+ *     the edge arrays (vec, Y, src, R); receiver i owns edges
+ *     row_offsets[i] .. row_offsets[i+1]-1.  A receiver range [a, b) of a
+ *     larger graph is therefore (row_offsets + a, N = b - a, out + a*C*16).
+ *   - Every pointer argument except eqmp_path_table's is DEVICE memory,
+ *     allocated and owned by the caller.  The library allocates no device
+ *     memory and keeps no state between calls beyond a per-device launch
+ *     configuration cache and a device-side watchdog flag.
+ *   - out is overwritten, never accumulated; receivers with no edges get 0.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream); the
+ *     caller synchronises before reading results.
+ *   - Precision: SH, CG and all accumulation in fp32.  x and out may be
+ *     stored as bf16 (round-to-nearest-even, once, on the final store).
+ *   - Errors: arguments are checked on the host before any launch and
+ *     reported as a status; nothing traps on the device.  Preconditions not
+ *     checked on the host (offsets non-decreasing with 0 <= off <= E,
+ *     0 <= src < N_src, finite vectors) cannot make a kernel fault or hang:
+ *     indices are clamped, out-of-range senders read as zero features, and
+ *     every device-side wait is bounded (see eqmp_device_error).  With them
+ *     violated the outputs are unspecified.  eqmp_validate_graph checks them.
+ *   - Zero-length edge vectors give n = 0: Y00 stays, every l >= 1 term is 0.
+ */
+#ifndef EQMP_H
+#define EQMP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so C callers need no CUDA headers. */
+typedef struct CUstream_st* eqmp_stream_t;
+
+typedef enum {
+  EQMP_OK = 0,
+  EQMP_ERR_INVALID_ARG = 1,   /* null pointer, negative size, misalignment, bad enum */
+  EQMP_ERR_UNSUPPORTED = 2,   /* valid but not built: C not in {8,16,32,64,128}, K != 8 */
+  EQMP_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+  EQMP_ERR_DEVICE_TIMEOUT = 4,/* a bounded device-side wait gave up (see eqmp_device_error) */
+  EQMP_ERR_GRAPH = 5          /* eqmp_validate_graph found a violated precondition */
+} eqmp_status;
+
+typedef enum { EQMP_F32 = 0, EQMP_BF16 = 1 } eqmp_dtype;
+
+/*
+ * Per-path channel weights.  Exactly one of the two modes:
+ *   shared:  w != NULL, R == M == NULL, K == 0.
+ *            w[34][C] fp32, path-major: W[e,p,c] = w[p*C + c] for every edge.
+ *   radial:  w == NULL, R and M non-NULL, K == 8.
+ *            R[E][K] fp32 (per-edge radial features, row e = absolute edge
+ *            index, 16-byte aligned), M[K][34*C] fp32 (column p*C + c,
+ *            16-byte aligned): W[e,p,c] = sum_k R[e*K+k] * M[k*34*C + p*C + c].
+ */
+typedef struct {
+  const float* w;
+  const float* R;
+  const float* M;
+  int32_t K;
+} eqmp_weights;
+
+/* Number of CG paths (34). */
+int32_t eqmp_num_paths(void);
+
+/* Writes the (l1, l2, l3) of each path, path-major, into HOST l1l2l3[34*3].
+ * EQMP_ERR_INVALID_ARG if l1l2l3 is NULL. */
+eqmp_status eqmp_path_table(int32_t* l1l2l3);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char* eqmp_status_string(eqmp_status s);
+
+/*
+ * Real spherical harmonics of each edge vector (Batmobile blog, section
+ * "2. 寄存器中间计算"): Y[e][k] for vec[e][0..2], k = l*l+l+m.
+ *   vec  [E][3] fp32, 4-byte aligned;  Y [E][16] fp32, 16-byte aligned.
+ *   E >= 0 (E == 0 launches nothing).
+ */
+eqmp_status eqmp_sh(const float* vec, int64_t E, float* Y, eqmp_stream_t stream);
+
+/*
+ * CG tensor product + receiver sum with the harmonics read from memory
+ * (the unfused second and third steps; Batmobile blog, sections
+ * "1. 编译时常量" and "3. 操作融合").
+ *   Y            [E][16] fp32 (e.g. from eqmp_sh), 16-byte aligned
+ *   x            [N_src][C][16], x_dtype (fp32 or bf16), 16-byte aligned
+ *   row_offsets  [N+1] int32, absolute edge indices (see above)
+ *   src          [E] int32 sender of each edge
+ *   N            receivers (rows of out), N >= 0;  E edges, 0 <= E < 2^31
+ *   C            channels, one of 8, 16, 32, 64, 128
+ *   weights      shared or radial, see eqmp_weights
+ *   out          [N][C][16], out_dtype == x_dtype, 16-byte aligned
+ */
+eqmp_status eqmp_tp_scatter(const float* Y, const void* x, int64_t N_src, eqmp_dtype x_dtype,
+                            const int32_t* row_offsets, const int32_t* src, int64_t N, int64_t E,
+                            int32_t C, eqmp_weights weights, void* out, eqmp_dtype out_dtype,
+                            eqmp_stream_t stream);
+
+/*
+ * The fused layer: SH in registers + CG tensor product + receiver sum in one
+ * kernel, each edge vector read once and each output row written once
+ * (Batmobile blog, section "3. 操作融合").  Arguments as eqmp_tp_scatter,
+ * with vec [E][3] fp32 (4-byte aligned) in place of Y.
+ */
+eqmp_status eqmp_fused(const float* vec, const void* x, int64_t N_src, eqmp_dtype x_dtype,
+                       const int32_t* row_offsets, const int32_t* src, int64_t N, int64_t E,
+                       int32_t C, eqmp_weights weights, void* out, eqmp_dtype out_dtype,
+                       eqmp_stream_t stream);
+
+/*
+ * Synchronous check of the graph preconditions on device data:
+ * 0 <= row_offsets[0] <= ... <= row_offsets[N] <= E and
+ * 0 <= src[e] < N_src for every e in [row_offsets[0], row_offsets[N]).
+ * Returns EQMP_OK or EQMP_ERR_GRAPH (or an argument/CUDA error).  Runs a
+ * small kernel on `stream` and waits for it.
+ */
+eqmp_status eqmp_validate_graph(const int32_t* row_offsets, const int32_t* src, int64_t N,
+                                int64_t N_src, int64_t E, eqmp_stream_t stream);
+
+/*
+ * Reads and clears the current device's watchdog word (synchronises the
+ * device).  *code = 0 when no bounded wait has given up since the last
+ * call; otherwise a nonzero code naming the wait.  A nonzero code means the
+ * outputs of the kernels since the last call are unspecified.  Returns
+ * EQMP_ERR_DEVICE_TIMEOUT when *code != 0.
+ */
+eqmp_status eqmp_device_error(int32_t* code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EQMP_H */

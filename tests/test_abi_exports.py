@@ -1,0 +1,96 @@
+"""The C-ABI library builds, loads and exports every symbol include/eqmp.h
+declares (CPU only: host-side functions only, no kernel launches)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "eqmp.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(eqmp_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import equivariant_gnn_message_gb300 as eq
+
+    return eq.load_library()
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for want in ("eqmp_sh", "eqmp_tp_scatter", "eqmp_fused", "eqmp_num_paths", "eqmp_path_table",
+                 "eqmp_status_string", "eqmp_validate_graph", "eqmp_device_error"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_host_only_functions(lib):
+    import equivariant_gnn_message_gb300 as eq
+    from oracle import cg
+
+    assert eq.eqmp_num_paths() == 34
+    assert eq.eqmp_path_table() == cg.paths()
+    assert eq.eqmp_status_string(0) == "ok"
+    assert "unsupported" in eq.eqmp_status_string(2)
+    assert eq.eqmp_status_string(99) == "unknown status"
+    assert lib.eqmp_path_table(None) == eq.EQMP_ERR_INVALID_ARG
+
+
+def test_product_path_has_no_oracle_dependency():
+    """The package and its sources never import or mention the oracle."""
+    pkg = os.path.join(ROOT, "equivariant_gnn_message_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        if "_build" in dirpath:
+            continue
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert not re.search(r"^\s*(from|import)\s+oracle", text, re.M), f
+                assert "oracle." not in text, f
+
+
+def test_generated_tables_match_oracle():
+    """The build-time CG generator (independent method) and the oracle agree."""
+    import importlib.util
+
+    import numpy as np
+
+    from oracle import cg, sh
+
+    spec = importlib.util.spec_from_file_location(
+        "gen_tables", os.path.join(ROOT, "equivariant_gnn_message_gb300", "csrc", "gen_tables.py"))
+    g = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(g)
+    _, paths, terms = g.render()
+    assert paths == cg.paths()
+    assert len(terms) == 611
+    for (l1, l2, l3, blk) in cg.real_cg_tables():
+        ent = g.real_cg(l1, l2, l3)
+        dense = np.zeros_like(blk)
+        for (m3, m1, m2), v in ent.items():
+            dense[m3 + l3, m1 + l1, m2 + l2] = v
+        assert np.max(np.abs(dense - blk)) < 1e-12
+    n = np.random.default_rng(0).standard_normal((20, 3))
+    n /= np.linalg.norm(n, axis=1, keepdims=True)
+    Y = sh.real_sh(n)
+    shc = g.sh_constants()
+    for l in range(4):
+        for m in range(l + 1):
+            poly = np.polynomial.polynomial.polyval(n[:, 2], shc[(l, m)])
+            pw = (n[:, 0] + 1j * n[:, 1]) ** m
+            assert np.allclose(poly * pw.real, Y[:, l * l + l + m], atol=1e-14)
+            if m:
+                assert np.allclose(poly * pw.imag, Y[:, l * l + l - m], atol=1e-14)

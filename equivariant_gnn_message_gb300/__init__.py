@@ -30,7 +30,8 @@ EQMP_ERR_DEVICE_TIMEOUT, EQMP_ERR_GRAPH = 4, 5
 EQMP_F32, EQMP_BF16 = 0, 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_LIB_PATH = os.path.join(_HERE, "_build", "libeqmp.so")
+# EQMP_LIB selects another build of the library (e.g. a tuning variant).
+_LIB_PATH = os.environ.get("EQMP_LIB") or os.path.join(_HERE, "_build", "libeqmp.so")
 _lib = None
 
 

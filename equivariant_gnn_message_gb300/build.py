@@ -48,18 +48,25 @@ def generate_tables():
     return out
 
 
-def build(force=False, verbose_ptxas=False, jobs=None):
-    """Compile libeqmp.so; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(force=False, verbose_ptxas=False, jobs=None, out_dir=None, defines=()):
+    """Compile libeqmp.so; returns its path.
+
+    out_dir / defines build a variant elsewhere (e.g. with EQMP_TUNE_* macros
+    for tuning experiments); the default is the in-tree _build/libeqmp.so.
+    """
+    bdir = out_dir or BUILD
+    lib = os.path.join(bdir, "libeqmp.so")
+    os.makedirs(bdir, exist_ok=True)
     newest = _newest_input_mtime()
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= newest and not verbose_ptxas:
-        return LIB
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= newest and not verbose_ptxas:
+        return lib
     generate_tables()
     cc = nvcc()
+    dflags = [f"-D{d}" for d in defines]
 
     def compile_one(unit):
-        obj = os.path.join(BUILD, unit.replace(".cu", ".o"))
-        cmd = [cc, "-c", os.path.join(CSRC, unit), "-o", obj] + _flags(verbose_ptxas)
+        obj = os.path.join(bdir, unit.replace(".cu", ".o"))
+        cmd = [cc, "-c", os.path.join(CSRC, unit), "-o", obj] + _flags(verbose_ptxas) + dflags
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError(f"nvcc failed on {unit}:\n{res.stdout}\n{res.stderr}")
@@ -71,10 +78,10 @@ def build(force=False, verbose_ptxas=False, jobs=None):
         for _, err in results:
             sys.stderr.write(err)
     objs = [o for o, _ in results]
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     subprocess.check_call([cc, "-shared", "-o", tmp] + objs + ARCH + ["-Xcompiler", "-fPIC"])
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -126,8 +126,8 @@ static eqmp_status run_layer(bool from_vec, const float* vec_or_Y, const void* x
   if (shared) {
     if (wt.R || wt.M || wt.K != 0) return EQMP_ERR_INVALID_ARG;
   } else {
-    if (!wt.R || !wt.M) return EQMP_ERR_INVALID_ARG;
     if (wt.K != 8) return EQMP_ERR_UNSUPPORTED;
+    if (E > 0 && (!wt.R || !wt.M)) return EQMP_ERR_INVALID_ARG;  // nothing is read when E == 0
     if (!aligned(wt.R, 16) || !aligned(wt.M, 4)) return EQMP_ERR_INVALID_ARG;
   }
   if (C != 8 && C != 16 && C != 32 && C != 64 && C != 128) return EQMP_ERR_UNSUPPORTED;

@@ -29,6 +29,29 @@
 
 namespace eqmp {
 
+// Tuning defaults (measured on GB300): thread (c, q) owns KQ values of k1,
+// S ring slots, MIN_BLOCKS CTAs per SM for the register budget.  The EQMP_TUNE_*
+// macros override them for experiments with a separately built library.
+template <int C, typename XT>
+struct SharedTune {
+  static constexpr bool B16 = sizeof(XT) == 2;
+#ifdef EQMP_TUNE_KQ
+  static constexpr int KQ = (B16 && C >= 32) ? 8 : (C >= 32 ? EQMP_TUNE_KQ : 4);
+#else
+  static constexpr int KQ = (B16 && C >= 32) ? 8 : (C >= 128 ? 8 : 4);
+#endif
+#ifdef EQMP_TUNE_S
+  static constexpr int S = EQMP_TUNE_S;
+#else
+  static constexpr int S = 16;
+#endif
+#ifdef EQMP_TUNE_MINB
+  static constexpr int MINB = EQMP_TUNE_MINB;
+#else
+  static constexpr int MINB = KQ == 4 ? 2 : 1;
+#endif
+};
+
 template <int C, int KQ, typename XT, bool FROM_VEC>
 struct SharedCfg {
   static constexpr int NQ = 16 / KQ;                 // quads of k1 per channel
@@ -39,7 +62,8 @@ struct SharedCfg {
   static constexpr int ROWS = ROW_BYTES / 128;        // 128-byte TMA box rows per node
   static constexpr int INNER = 128 / (int)sizeof(XT);  // elements per box row
   static constexpr int SLOT = ROW_BYTES < 1024 ? 1024 : ROW_BYTES;  // swizzle atom aligned
-  static constexpr int S = (SLOT * 16 <= 65536) ? 16 : (65536 / SLOT < 4 ? 4 : 65536 / SLOT);
+  static constexpr int S_WANT = SharedTune<C, XT>::S;
+  static constexpr int S = (SLOT * S_WANT <= 65536) ? S_WANT : (65536 / SLOT < 4 ? 4 : 65536 / SLOT);
   static constexpr int OFF_X = 0;
   static constexpr int OFF_Y = OFF_X + S * SLOT;
   static constexpr int OFF_RED = OFF_Y + S * 64;
@@ -47,7 +71,7 @@ struct SharedCfg {
   static constexpr int OFF_BAR = OFF_W + 34 * C * 4;
   static constexpr int SMEM_BYTES = OFF_BAR + 2 * S * 8 + 1024;  // + base alignment slack
   static constexpr int XBYTES = KQ * (int)sizeof(XT);              // bytes of x per thread per edge
-  static constexpr int MIN_BLOCKS = KQ == 4 ? 2 : 1;               // CTAs per SM the registers allow
+  static constexpr int MIN_BLOCKS = SharedTune<C, XT>::MINB;       // CTAs per SM the registers allow
   static_assert(NCONS % 32 == 0, "consumer threads must fill warps");
   static_assert(XBYTES == 8 || XBYTES == 16 || XBYTES == 32, "unsupported x chunk");
   static_assert(ROW_BYTES % 128 == 0, "row must be whole 128-byte lines");
@@ -181,8 +205,7 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
     }
     fence_mbar_init();
   }
-  for (int i = tid; i < 34 * C; i += K::NTHREADS) ws[i] = __ldg(a.w + i);
-  __syncthreads();
+  __syncthreads();  // barriers initialised; the producer starts at once
 
   // Edge range, clamped into [0, E]: a malformed CSR cannot send a load
   // out of bounds, and producer and consumers agree on the count.
@@ -252,14 +275,47 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
 
   // -------------------------------------------------------------- consumers
   const int c = tid % C, q = tid / C, lane = tid & 31;
+  // Path weights to shared memory: every load issued before any store.
+  {
+    constexpr int PER = (34 * C + K::NCONS - 1) / K::NCONS;
+    float wv[PER];
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int i = tid + k * K::NCONS;
+      wv[k] = i < 34 * C ? __ldg(a.w + i) : 0.0f;
+    }
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int i = tid + k * K::NCONS;
+      if (i < 34 * C) ws[i] = wv[k];
+    }
+  }
+  // CSR offsets, 32 receivers per warp-wide load, one chunk prefetched ahead:
+  // lane i holds off[chunk_base + i]; off[r] and off[r+1] come by shuffle.
+  auto load_off = [&](int base) {
+    const int i = base + lane;
+    return i <= r_end ? min(max(__ldg(a.off + i), 0), a.E) : a.E;
+  };
+  int chunk = r_begin;
+  int off_cur = load_off(chunk);
+  int off_nxt = load_off(chunk + 32);
+  named_barrier(2, K::NCONS);  // weights visible to all consumers
   const uint32_t xo = (uint32_t)(c * 16 * (int)sizeof(XT) + q * K::XBYTES);
   const float* wcol = ws + c;
   uint32_t n = 0;
   int buf = 0;
   bool failed = false;
   for (int r = r_begin; r < r_end; ++r) {
-    const int a0 = min(max(__ldg(a.off + r), 0), a.E);
-    const int a1 = min(max(__ldg(a.off + r + 1), 0), a.E);
+    if (r - chunk == 32) {
+      chunk += 32;
+      off_cur = off_nxt;
+      off_nxt = load_off(chunk + 32);
+    }
+    const int j0 = r - chunk;  // 0..31; off[r+1] is lane j0+1, or lane 0 of the next chunk
+    const int a0 = __shfl_sync(0xffffffffu, off_cur, j0);
+    const int a1n = __shfl_sync(0xffffffffu, off_cur, (j0 + 1) & 31);
+    const int a1x = __shfl_sync(0xffffffffu, off_nxt, 0);
+    const int a1 = j0 == 31 ? a1x : a1n;
     const int deg = min(max(a1 - a0, 0), total - (int)n);
     float acc[KQ][16];
 #pragma unroll

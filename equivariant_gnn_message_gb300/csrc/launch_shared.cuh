@@ -30,19 +30,16 @@ eqmp_status launch_shared_t(const LayerArgs& a, const CUtensorMap& map, cudaStre
   return cuda_status(cudaGetLastError());
 }
 
-// KQ per channel count and storage: 4 k1 per thread (64 accumulators) for
-// fp32 up to C = 64; 8 (128 accumulators) for bf16 from C = 32 (keeps the
-// swizzled reads conflict-free) and for fp32 at C = 128.
+// KQ per channel count and storage comes from SharedTune (k_shared.cuh).
 template <typename XT, bool FV>
 eqmp_status launch_shared_c(const LayerArgs& a, int C, const CUtensorMap& map, cudaStream_t st,
                             const DeviceInfo& dev) {
-  constexpr bool B = sizeof(XT) == 2;
   switch (C) {
-    case 8: return launch_shared_t<8, 4, XT, FV>(a, map, st, dev);
-    case 16: return launch_shared_t<16, 4, XT, FV>(a, map, st, dev);
-    case 32: return launch_shared_t<32, B ? 8 : 4, XT, FV>(a, map, st, dev);
-    case 64: return launch_shared_t<64, B ? 8 : 4, XT, FV>(a, map, st, dev);
-    case 128: return launch_shared_t<128, 8, XT, FV>(a, map, st, dev);
+    case 8: return launch_shared_t<8, SharedTune<8, XT>::KQ, XT, FV>(a, map, st, dev);
+    case 16: return launch_shared_t<16, SharedTune<16, XT>::KQ, XT, FV>(a, map, st, dev);
+    case 32: return launch_shared_t<32, SharedTune<32, XT>::KQ, XT, FV>(a, map, st, dev);
+    case 64: return launch_shared_t<64, SharedTune<64, XT>::KQ, XT, FV>(a, map, st, dev);
+    case 128: return launch_shared_t<128, SharedTune<128, XT>::KQ, XT, FV>(a, map, st, dev);
     default: return EQMP_ERR_UNSUPPORTED;
   }
 }

@@ -76,7 +76,7 @@ typedef enum { EQMP_F32 = 0, EQMP_BF16 = 1 } eqmp_dtype;
  * Per-path channel weights.  Exactly one of the two modes:
  *   shared:  w != NULL, R == M == NULL, K == 0.
  *            w[34][C] fp32, path-major: W[e,p,c] = w[p*C + c] for every edge.
- *   radial:  w == NULL, R and M non-NULL, K == 8.
+ *   radial:  w == NULL, K == 8, R and M non-NULL (may be NULL when E == 0).
  *            R[E][K] fp32 (per-edge radial features, row e = absolute edge
  *            index, 16-byte aligned), M[K][34*C] fp32 (column p*C + c,
  *            16-byte aligned): W[e,p,c] = sum_k R[e*K+k] * M[k*34*C + p*C + c].

@@ -90,6 +90,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* wd
   }
 }
 
+// Out-of-line slow path of a wait whose first try failed: keeps the hot loop
+// small.  Skips waiting once `failed` is set (the kernel then finishes its
+// loop structure without blocking and exits).
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, int* wd, int code,
+                                            bool failed) {
+  if (failed) return false;
+  return mbar_wait(bar, parity, wd, code);
+}
+
 // ---------------------------------------------------------------- TMA
 // 2-D tiled tensor load global -> shared, completion on an mbarrier.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y,
@@ -98,6 +107,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(tmap), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// Plain bulk copy global -> shared (16-byte aligned addresses, size a
+// multiple of 16), completion on an mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
 

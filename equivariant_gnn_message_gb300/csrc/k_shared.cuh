@@ -29,26 +29,24 @@
 
 namespace eqmp {
 
-// Tuning defaults (measured on GB300): thread (c, q) owns KQ values of k1,
-// S ring slots, MIN_BLOCKS CTAs per SM for the register budget.  The EQMP_TUNE_*
-// macros override them for experiments with a separately built library.
+// Tuning: thread (c, q) owns KQ values of k1 (8 from C = 64: 128
+// accumulators; 4 below).  When the consumer warps fill whole warpgroups the
+// CTA is warp-specialised: warpgroup 0 is the producer (one active warp) and
+// gives registers away with setmaxnreg, the consumer warpgroups take them.
+// The EQMP_TUNE_* macros override the defaults for experiments with a
+// separately built library.
 template <int C, typename XT>
 struct SharedTune {
-  static constexpr bool B16 = sizeof(XT) == 2;
 #ifdef EQMP_TUNE_KQ
-  static constexpr int KQ = (B16 && C >= 32) ? 8 : (C >= 32 ? EQMP_TUNE_KQ : 4);
+  static constexpr int KQ = C >= 64 ? EQMP_TUNE_KQ : 4;
 #else
-  static constexpr int KQ = (B16 && C >= 32) ? 8 : (C >= 128 ? 8 : 4);
+  static constexpr int KQ = C >= 64 ? 8 : 4;
 #endif
+  static constexpr int ROW = C * 16 * (int)sizeof(XT);
 #ifdef EQMP_TUNE_S
   static constexpr int S = EQMP_TUNE_S;
 #else
-  static constexpr int S = 16;
-#endif
-#ifdef EQMP_TUNE_MINB
-  static constexpr int MINB = EQMP_TUNE_MINB;
-#else
-  static constexpr int MINB = KQ == 4 ? 2 : 1;
+  static constexpr int S = ROW >= 4096 && !(C >= 128 && sizeof(XT) == 2) ? 8 : 16;
 #endif
 };
 
@@ -57,13 +55,26 @@ struct SharedCfg {
   static constexpr int NQ = 16 / KQ;                 // quads of k1 per channel
   static constexpr int NCONS = C * NQ;               // consumer threads
   static constexpr int NCW = NCONS / 32;             // consumer warps
-  static constexpr int NTHREADS = NCONS + 32;        // + producer warp
+  static constexpr bool WS = NCW % 4 == 0;           // warp-specialised with setmaxnreg
+  static constexpr int CONS0 = WS ? 128 : 0;         // first consumer thread
+  static constexpr int NTHREADS = WS ? 128 + NCONS : NCONS + 32;
+  static constexpr int MIN_BLOCKS = WS ? (NCONS >= 256 ? 1 : 2) : 4;
+  // Registers: the launch gives every thread R0 (per-SMSP file of 16K
+  // registers shared by the warps resident on it); the producer warpgroup
+  // drops to RP and the consumer warpgroups rise to RC within that pool.
+  static constexpr int WARPS_PER_SMSP = (NTHREADS / 32 * MIN_BLOCKS + 3) / 4;
+  static constexpr int R0_RAW = 16384 / (32 * WARPS_PER_SMSP);
+  static constexpr int R0 = (R0_RAW > 255 ? 255 : R0_RAW) & ~7;
+  static constexpr int RP = 40;
+  static constexpr int RC_RAW = WS ? (R0 * NTHREADS - RP * 128) / NCONS : R0;
+  static constexpr int RC = (RC_RAW > 256 ? 256 : RC_RAW) & ~7;
+  static_assert(!WS || RP * 128 + RC * NCONS <= R0 * NTHREADS, "register split exceeds the pool");
   static constexpr int ROW_BYTES = C * 16 * (int)sizeof(XT);
   static constexpr int ROWS = ROW_BYTES / 128;        // 128-byte TMA box rows per node
   static constexpr int INNER = 128 / (int)sizeof(XT);  // elements per box row
   static constexpr int SLOT = ROW_BYTES < 1024 ? 1024 : ROW_BYTES;  // swizzle atom aligned
-  static constexpr int S_WANT = SharedTune<C, XT>::S;
-  static constexpr int S = (SLOT * S_WANT <= 65536) ? S_WANT : (65536 / SLOT < 4 ? 4 : 65536 / SLOT);
+  static constexpr int S = SharedTune<C, XT>::S;
+  static_assert((S & (S - 1)) == 0, "ring size must be a power of two");
   static constexpr int OFF_X = 0;
   static constexpr int OFF_Y = OFF_X + S * SLOT;
   static constexpr int OFF_RED = OFF_Y + S * 64;
@@ -71,11 +82,19 @@ struct SharedCfg {
   static constexpr int OFF_BAR = OFF_W + 34 * C * 4;
   static constexpr int SMEM_BYTES = OFF_BAR + 2 * S * 8 + 1024;  // + base alignment slack
   static constexpr int XBYTES = KQ * (int)sizeof(XT);              // bytes of x per thread per edge
-  static constexpr int MIN_BLOCKS = SharedTune<C, XT>::MINB;       // CTAs per SM the registers allow
   static_assert(NCONS % 32 == 0, "consumer threads must fill warps");
   static_assert(XBYTES == 8 || XBYTES == 16 || XBYTES == 32, "unsupported x chunk");
   static_assert(ROW_BYTES % 128 == 0, "row must be whole 128-byte lines");
 };
+
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
 
 // Byte offset of logical byte o of a node row inside its 128B-swizzled slot.
 __device__ __forceinline__ uint32_t swz128(uint32_t o) {
@@ -137,6 +156,15 @@ __device__ __forceinline__ void contract(int q, const float (&acc)[KQ][16], cons
     if (q == 0) contract_quad<C, KQ, 0>(acc, wcol, part, Seq{});
     else contract_quad<C, KQ, 1>(acc, wcol, part, Seq{});
   }
+}
+
+template <int KQ>
+__device__ __forceinline__ void fma_edge(float (&acc)[KQ][16], const float (&yv)[16],
+                                         const float (&xv)[KQ]) {
+#pragma unroll
+  for (int i = 0; i < KQ; ++i)
+#pragma unroll
+    for (int k = 0; k < 16; ++k) acc[i][k] = fmaf(xv[i], yv[k], acc[i][k]);
 }
 
 // ---- x chunk load (KQ elements of one channel) from a swizzled slot -------
@@ -213,53 +241,64 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
   const int e_end = max(e_begin, min(max(__ldg(a.off + r_end), 0), a.E));
   const int total = e_end - e_begin;
 
-  if (tid >= K::NCONS) {
+  if (K::WS ? tid < K::CONS0 : tid >= K::NCONS) {
     // ------------------------------------------------------------ producer
+    if constexpr (K::WS) {
+      setmaxnreg_dec<K::RP>();
+      if (tid >= 32) return;  // one producer warp; the rest of warpgroup 0 idles out
+    }
+    // Batches of 32 edges: lane l owns edge base+l.  The sender index (and
+    // edge vector) of the NEXT batch are loaded while this batch is issued;
+    // lanes take turns in CSR order to claim a slot, write the 16 SH (fused:
+    // computed right there; tp_scatter: bulk-copied from Y) and launch the
+    // row copy of x[src].
     const int lane = tid & 31;
     if (lane == 0) prefetch_tmap(&tmap);
-    uint32_t n = 0;
-    bool ok = true;
-    for (int base = e_begin; base < e_end && ok; base += 32) {
-      const int e = base + lane;
-      float y[16];
-      int node = 0;
+    auto load_edge = [&](int e, int& node, float& vx, float& vy, float& vz) {
+      node = 0; vx = vy = vz = 0.0f;
       if (e < e_end) {
         node = __ldg(a.src + e);
         if constexpr (FROM_VEC) {
           const float* v = a.vec + 3 * (size_t)e;
-          real_sh16(__ldg(v), __ldg(v + 1), __ldg(v + 2), y);
-        } else {
-          const float4* yp = reinterpret_cast<const float4*>(a.Y) + 4 * (size_t)e;
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const float4 t = __ldg(yp + h);
-            y[4 * h] = t.x; y[4 * h + 1] = t.y; y[4 * h + 2] = t.z; y[4 * h + 3] = t.w;
-          }
+          vx = __ldg(v); vy = __ldg(v + 1); vz = __ldg(v + 2);
         }
-      } else {
-#pragma unroll
-        for (int k = 0; k < 16; ++k) y[k] = 0.0f;
       }
+    };
+    constexpr uint32_t TX = K::ROW_BYTES + (FROM_VEC ? 0 : 64);
+    uint32_t n = 0;
+    bool ok = true;
+    int node_nx;
+    float vx_nx, vy_nx, vz_nx;
+    load_edge(e_begin + lane, node_nx, vx_nx, vy_nx, vz_nx);
+    for (int base = e_begin; base < e_end && ok; base += 32) {
+      const int node = node_nx;
+      const float vx = vx_nx, vy = vy_nx, vz = vz_nx;
+      load_edge(base + 32 + lane, node_nx, vx_nx, vy_nx, vz_nx);  // next batch, in flight
       const int cnt = min(32, e_end - base);
       for (int j = 0; j < cnt; ++j) {
         int good = 1;
         if (lane == j) {
           const uint32_t s = n % S, par = ((n / S) & 1u) ^ 1u;
-          if (mbar_wait(empty0 + 8 * s, par, a.watchdog, 2)) {
-            float4* yd = ys + 4 * s;
-            yd[0] = make_float4(y[0], y[1], y[2], y[3]);
-            yd[1] = make_float4(y[4], y[5], y[6], y[7]);
-            yd[2] = make_float4(y[8], y[9], y[10], y[11]);
-            yd[3] = make_float4(y[12], y[13], y[14], y[15]);
-            mbar_arrive_expect_tx(full0 + 8 * s, K::ROW_BYTES);
+          if (mbar_try_wait(empty0 + 8 * s, par) || mbar_wait(empty0 + 8 * s, par, a.watchdog, 2)) {
+            if constexpr (FROM_VEC) {
+              float y[16];
+              real_sh16(vx, vy, vz, y);
+              float4* yd = ys + 4 * s;
+              yd[0] = make_float4(y[0], y[1], y[2], y[3]);
+              yd[1] = make_float4(y[4], y[5], y[6], y[7]);
+              yd[2] = make_float4(y[8], y[9], y[10], y[11]);
+              yd[3] = make_float4(y[12], y[13], y[14], y[15]);
+            }
+            mbar_arrive_expect_tx(full0 + 8 * s, TX);
             tma_load_2d(smem_u32(smem + K::OFF_X + s * K::SLOT), &tmap, 0, node * K::ROWS,
                         full0 + 8 * s);
+            if constexpr (!FROM_VEC)
+              bulk_load(smem_u32(ys + 4 * s), a.Y + 16 * (size_t)(base + j), 64, full0 + 8 * s);
           } else {
             good = 0;
           }
         }
-        good = __shfl_sync(0xffffffffu, good, j);
-        if (!good) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, good)) { ok = false; break; }
         ++n;
       }
     }
@@ -274,19 +313,21 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
   }
 
   // -------------------------------------------------------------- consumers
-  const int c = tid % C, q = tid / C, lane = tid & 31;
+  if constexpr (K::WS) setmaxnreg_inc<K::RC>();
+  const int ct = tid - K::CONS0;  // consumer index
+  const int c = ct % C, q = ct / C, lane = tid & 31;
   // Path weights to shared memory: every load issued before any store.
   {
     constexpr int PER = (34 * C + K::NCONS - 1) / K::NCONS;
     float wv[PER];
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
-      const int i = tid + k * K::NCONS;
+      const int i = ct + k * K::NCONS;
       wv[k] = i < 34 * C ? __ldg(a.w + i) : 0.0f;
     }
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
-      const int i = tid + k * K::NCONS;
+      const int i = ct + k * K::NCONS;
       if (i < 34 * C) ws[i] = wv[k];
     }
   }
@@ -302,9 +343,28 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
   named_barrier(2, K::NCONS);  // weights visible to all consumers
   const uint32_t xo = (uint32_t)(c * 16 * (int)sizeof(XT) + q * K::XBYTES);
   const float* wcol = ws + c;
-  uint32_t n = 0;
+  uint32_t n = 0;  // ordinal of the CTA's next edge
   int buf = 0;
   bool failed = false;
+  // Edge m lives in slot m % S, phase (m / S) & 1.
+  auto fetch = [&](uint32_t m, float (&yv)[16], float (&xv)[KQ]) {
+    const uint32_t s = m % S, par = (m / S) & 1u;
+    if (!mbar_try_wait(full0 + 8 * s, par))
+      if (!mbar_wait_slow(full0 + 8 * s, par, a.watchdog, 1, failed)) failed = true;
+    const float4* yp = ys + 4 * s;
+    const float4 y0 = yp[0], y1 = yp[1], y2 = yp[2], y3 = yp[3];
+    yv[0] = y0.x; yv[1] = y0.y; yv[2] = y0.z; yv[3] = y0.w;
+    yv[4] = y1.x; yv[5] = y1.y; yv[6] = y1.z; yv[7] = y1.w;
+    yv[8] = y2.x; yv[9] = y2.y; yv[10] = y2.z; yv[11] = y2.w;
+    yv[12] = y3.x; yv[13] = y3.y; yv[14] = y3.z; yv[15] = y3.w;
+    load_x<XT, KQ>(smem + K::OFF_X + s * K::SLOT, xo, xv);
+  };
+  auto release = [&](uint32_t m) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * (m % S));
+  };
+  float yA[16], xA[KQ], yB[16], xB[KQ];
+  if (total > 0) fetch(0, yA, xA);
   for (int r = r_begin; r < r_end; ++r) {
     if (r - chunk == 32) {
       chunk += 32;
@@ -323,21 +383,26 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
 #pragma unroll
       for (int k = 0; k < 16; ++k) acc[i][k] = 0.0f;
 
-    for (int j = 0; j < deg; ++j, ++n) {
-      const uint32_t s = n % S, par = (n / S) & 1u;
-      if (!failed && !mbar_wait(full0 + 8 * s, par, a.watchdog, 1)) failed = true;
-      const float4* yp = ys + 4 * s;
-      const float4 y0 = yp[0], y1 = yp[1], y2 = yp[2], y3 = yp[3];
-      const float yv[16] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w,
-                            y2.x, y2.y, y2.z, y2.w, y3.x, y3.y, y3.z, y3.w};
-      float xv[KQ];
-      load_x<XT, KQ>(smem + K::OFF_X + s * K::SLOT, xo, xv);
+    // Two edges per trip: the smem loads of the next edge are in flight
+    // while the FMAs of the current one issue.
+    int j = 0;
+    for (; j + 2 <= deg; j += 2, n += 2) {
+      if (n + 1 < (uint32_t)total) fetch(n + 1, yB, xB);
+      fma_edge(acc, yA, xA);
+      release(n);
+      if (n + 2 < (uint32_t)total) fetch(n + 2, yA, xA);
+      fma_edge(acc, yB, xB);
+      release(n + 1);
+    }
+    if (j < deg) {
+      if (n + 1 < (uint32_t)total) fetch(n + 1, yB, xB);
+      fma_edge(acc, yA, xA);
+      release(n);
 #pragma unroll
-      for (int i = 0; i < KQ; ++i)
+      for (int k = 0; k < 16; ++k) yA[k] = yB[k];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) acc[i][k] = fmaf(xv[i], yv[k], acc[i][k]);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * s);
+      for (int i = 0; i < KQ; ++i) xA[i] = xB[i];
+      ++n;
     }
 
     float part[16];

@@ -19,6 +19,16 @@ eqmp_status launch_shared_t(const LayerArgs& a, const CUtensorMap& map, cudaStre
   cudaGetDevice(&d);
   int occ = __atomic_load_n(&occ_cache[d & 63], __ATOMIC_RELAXED);
   if (occ == 0) {
+    // setmaxnreg.inc waits until the CTA's register pool can cover the
+    // request, with no time limit: launch only if the compiled register
+    // count gives a pool at least as large as the split needs.
+    if constexpr (K::WS) {
+      cudaFuncAttributes fa;
+      err = cudaFuncGetAttributes(&fa, kern);
+      if (err != cudaSuccess) return EQMP_ERR_CUDA;
+      if ((long long)fa.numRegs * K::NTHREADS < (long long)K::RP * 128 + (long long)K::RC * K::NCONS)
+        return EQMP_ERR_UNSUPPORTED;
+    }
     err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, K::NTHREADS, K::SMEM_BYTES);
     if (err != cudaSuccess || occ < 1) return EQMP_ERR_CUDA;
     __atomic_store_n(&occ_cache[d & 63], occ, __ATOMIC_RELAXED);

@@ -74,10 +74,10 @@ struct SharedCfg {
   static constexpr int INNER = 128 / (int)sizeof(XT);  // elements per box row
   static constexpr int SLOT = ROW_BYTES < 1024 ? 1024 : ROW_BYTES;  // swizzle atom aligned
   static constexpr int S = SharedTune<C, XT>::S;
-  static_assert((S & (S - 1)) == 0, "ring size must be a power of two");
+  static_assert((S & (S - 1)) == 0 && S <= 32, "ring size: power of two, at most one batch");
   static constexpr int OFF_X = 0;
-  static constexpr int OFF_Y = OFF_X + S * SLOT;
-  static constexpr int OFF_RED = OFF_Y + S * 64;
+  static constexpr int OFF_Y = OFF_X + S * SLOT;            // 64-entry SH ring (2 batches of 32)
+  static constexpr int OFF_RED = OFF_Y + 64 * 64;
   static constexpr int OFF_W = OFF_RED + 2 * NQ * 16 * C * 4;
   static constexpr int OFF_BAR = OFF_W + 34 * C * 4;
   static constexpr int SMEM_BYTES = OFF_BAR + 2 * S * 8 + 1024;  // + base alignment slack
@@ -248,10 +248,14 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
       if (tid >= 32) return;  // one producer warp; the rest of warpgroup 0 idles out
     }
     // Batches of 32 edges: lane l owns edge base+l.  The sender index (and
-    // edge vector) of the NEXT batch are loaded while this batch is issued;
-    // lanes take turns in CSR order to claim a slot, write the 16 SH (fused:
-    // computed right there; tp_scatter: bulk-copied from Y) and launch the
-    // row copy of x[src].
+    // edge vector) of the NEXT batch are loaded while this batch is issued.
+    // All lanes compute their 16 SH at once into the batch's half of the SH
+    // ring (entry = edge ordinal % 64); then lanes take turns in CSR order to
+    // claim an x slot and launch the row copy of x[src] (tp_scatter: plus a
+    // 64-byte copy of the stored SH row into the ring).  The SH ring half of
+    // batch k was last read for batch k-2, whose slots were all released
+    // before batch k-1 finished issuing (S <= 32), so the overwrite is safe;
+    // each lane's arrive publishes its own SH stores.
     const int lane = tid & 31;
     if (lane == 0) prefetch_tmap(&tmap);
     auto load_edge = [&](int e, int& node, float& vx, float& vy, float& vz) {
@@ -272,7 +276,15 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
     load_edge(e_begin + lane, node_nx, vx_nx, vy_nx, vz_nx);
     for (int base = e_begin; base < e_end && ok; base += 32) {
       const int node = node_nx;
-      const float vx = vx_nx, vy = vy_nx, vz = vz_nx;
+      float4* yd = ys + 4 * ((n + lane) & 63);
+      if constexpr (FROM_VEC) {
+        float y[16];
+        real_sh16(vx_nx, vy_nx, vz_nx, y);
+        yd[0] = make_float4(y[0], y[1], y[2], y[3]);
+        yd[1] = make_float4(y[4], y[5], y[6], y[7]);
+        yd[2] = make_float4(y[8], y[9], y[10], y[11]);
+        yd[3] = make_float4(y[12], y[13], y[14], y[15]);
+      }
       load_edge(base + 32 + lane, node_nx, vx_nx, vy_nx, vz_nx);  // next batch, in flight
       const int cnt = min(32, e_end - base);
       for (int j = 0; j < cnt; ++j) {
@@ -280,20 +292,11 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
         if (lane == j) {
           const uint32_t s = n % S, par = ((n / S) & 1u) ^ 1u;
           if (mbar_try_wait(empty0 + 8 * s, par) || mbar_wait(empty0 + 8 * s, par, a.watchdog, 2)) {
-            if constexpr (FROM_VEC) {
-              float y[16];
-              real_sh16(vx, vy, vz, y);
-              float4* yd = ys + 4 * s;
-              yd[0] = make_float4(y[0], y[1], y[2], y[3]);
-              yd[1] = make_float4(y[4], y[5], y[6], y[7]);
-              yd[2] = make_float4(y[8], y[9], y[10], y[11]);
-              yd[3] = make_float4(y[12], y[13], y[14], y[15]);
-            }
             mbar_arrive_expect_tx(full0 + 8 * s, TX);
             tma_load_2d(smem_u32(smem + K::OFF_X + s * K::SLOT), &tmap, 0, node * K::ROWS,
                         full0 + 8 * s);
             if constexpr (!FROM_VEC)
-              bulk_load(smem_u32(ys + 4 * s), a.Y + 16 * (size_t)(base + j), 64, full0 + 8 * s);
+              bulk_load(smem_u32(yd), a.Y + 16 * (size_t)(base + j), 64, full0 + 8 * s);
           } else {
             good = 0;
           }
@@ -351,7 +354,7 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
     const uint32_t s = m % S, par = (m / S) & 1u;
     if (!mbar_try_wait(full0 + 8 * s, par))
       if (!mbar_wait_slow(full0 + 8 * s, par, a.watchdog, 1, failed)) failed = true;
-    const float4* yp = ys + 4 * s;
+    const float4* yp = ys + 4 * (m & 63);
     const float4 y0 = yp[0], y1 = yp[1], y2 = yp[2], y3 = yp[3];
     yv[0] = y0.x; yv[1] = y0.y; yv[2] = y0.z; yv[3] = y0.w;
     yv[4] = y1.x; yv[5] = y1.y; yv[6] = y1.z; yv[7] = y1.w;

@@ -103,14 +103,17 @@ __device__ __forceinline__ uint32_t swz128(uint32_t o) {
 
 // ---- compile-time contraction: partial outputs of quad Q -----------------
 template <int KQ, int Q, int I>
-__device__ __forceinline__ void apply_term(const float (&acc)[KQ][16], float (&tmp)[16]) {
+__device__ __forceinline__ void apply_term(const float2 (&acc)[KQ][8], float (&tmp)[16]) {
   constexpr tables::Term t = term_at(I);
-  if constexpr (t.k1 >= Q * KQ && t.k1 < Q * KQ + KQ)
-    tmp[t.k3] = fmaf(t.c, acc[t.k1 - Q * KQ][t.k2], tmp[t.k3]);
+  if constexpr (t.k1 >= Q * KQ && t.k1 < Q * KQ + KQ) {
+    constexpr int i = t.k1 - Q * KQ;
+    const float a = (t.k2 & 1) ? acc[i][t.k2 >> 1].y : acc[i][t.k2 >> 1].x;
+    tmp[t.k3] = fmaf(t.c, a, tmp[t.k3]);
+  }
 }
 
 template <int KQ, int Q, int First, int... Is>
-__device__ __forceinline__ void apply_terms(const float (&acc)[KQ][16], float (&tmp)[16],
+__device__ __forceinline__ void apply_terms(const float2 (&acc)[KQ][8], float (&tmp)[16],
                                             std::integer_sequence<int, Is...>) {
   (apply_term<KQ, Q, First + Is>(acc, tmp), ...);
 }
@@ -122,7 +125,7 @@ __device__ __forceinline__ void weight_outputs(float w, const float (&tmp)[16], 
 }
 
 template <int C, int KQ, int Q, int P>
-__device__ __forceinline__ void contract_path(const float (&acc)[KQ][16], const float* wcol,
+__device__ __forceinline__ void contract_path(const float2 (&acc)[KQ][8], const float* wcol,
                                               float (&part)[16]) {
   if constexpr (path_touches(P, Q * KQ, KQ)) {
     constexpr tables::Path path = path_at(P);
@@ -136,13 +139,13 @@ __device__ __forceinline__ void contract_path(const float (&acc)[KQ][16], const 
 }
 
 template <int C, int KQ, int Q, int... Ps>
-__device__ __forceinline__ void contract_quad(const float (&acc)[KQ][16], const float* wcol,
+__device__ __forceinline__ void contract_quad(const float2 (&acc)[KQ][8], const float* wcol,
                                               float (&part)[16], std::integer_sequence<int, Ps...>) {
   (contract_path<C, KQ, Q, Ps>(acc, wcol, part), ...);
 }
 
 template <int C, int KQ>
-__device__ __forceinline__ void contract(int q, const float (&acc)[KQ][16], const float* wcol,
+__device__ __forceinline__ void contract(int q, const float2 (&acc)[KQ][8], const float* wcol,
                                          float (&part)[16]) {
   using Seq = std::make_integer_sequence<int, tables::kNumPaths>;
   if constexpr (KQ == 4) {
@@ -158,30 +161,41 @@ __device__ __forceinline__ void contract(int q, const float (&acc)[KQ][16], cons
   }
 }
 
+// A[i][k] += x[i] * Y[k] for one edge with the paired FP32 FMA of sm_100+
+// (two IEEE round-to-nearest FMAs per instruction, identical to fmaf):
+// acc[i][kk] holds (A[i][2kk], A[i][2kk+1]).
 template <int KQ>
-__device__ __forceinline__ void fma_edge(float (&acc)[KQ][16], const float (&yv)[16],
+__device__ __forceinline__ void fma_edge(float2 (&acc)[KQ][8], const float2 (&yv)[8],
                                          const float (&xv)[KQ]) {
 #pragma unroll
-  for (int i = 0; i < KQ; ++i)
+  for (int i = 0; i < KQ; ++i) {
+    const float2 xx = make_float2(xv[i], xv[i]);
 #pragma unroll
-    for (int k = 0; k < 16; ++k) acc[i][k] = fmaf(xv[i], yv[k], acc[i][k]);
+    for (int kk = 0; kk < 8; ++kk) acc[i][kk] = __ffma2_rn(xx, yv[kk], acc[i][kk]);
+  }
+}
+
+template <int KQ>
+__device__ __forceinline__ float acc_at(const float2 (&acc)[KQ][8], int i, int k) {
+  return (k & 1) ? acc[i][k >> 1].y : acc[i][k >> 1].x;
 }
 
 // ---- x chunk load (KQ elements of one channel) from a swizzled slot -------
+// xo[h]: swizzled byte offsets of the thread's 16-byte chunk(s) in a slot.
 template <typename XT, int KQ>
-__device__ __forceinline__ void load_x(const uint8_t* slot, uint32_t o, float (&xv)[KQ]) {
+__device__ __forceinline__ void load_x(const uint8_t* slot, const uint32_t (&xo)[2], float (&xv)[KQ]) {
   if constexpr (sizeof(XT) == 4) {
 #pragma unroll
     for (int h = 0; h < KQ / 4; ++h) {
-      const float4 v = *reinterpret_cast<const float4*>(slot + swz128(o + 16 * h));
+      const float4 v = *reinterpret_cast<const float4*>(slot + xo[h]);
       xv[4 * h + 0] = v.x; xv[4 * h + 1] = v.y; xv[4 * h + 2] = v.z; xv[4 * h + 3] = v.w;
     }
   } else if constexpr (KQ == 8) {
-    const uint4 v = *reinterpret_cast<const uint4*>(slot + swz128(o));
+    const uint4 v = *reinterpret_cast<const uint4*>(slot + xo[0]);
     xv[0] = bf16_lo(v.x); xv[1] = bf16_hi(v.x); xv[2] = bf16_lo(v.y); xv[3] = bf16_hi(v.y);
     xv[4] = bf16_lo(v.z); xv[5] = bf16_hi(v.z); xv[6] = bf16_lo(v.w); xv[7] = bf16_hi(v.w);
   } else {
-    const uint2 v = *reinterpret_cast<const uint2*>(slot + swz128(o));
+    const uint2 v = *reinterpret_cast<const uint2*>(slot + xo[0]);
     xv[0] = bf16_lo(v.x); xv[1] = bf16_hi(v.x); xv[2] = bf16_lo(v.y); xv[3] = bf16_hi(v.y);
   }
 }
@@ -344,29 +358,32 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
   int off_cur = load_off(chunk);
   int off_nxt = load_off(chunk + 32);
   named_barrier(2, K::NCONS);  // weights visible to all consumers
-  const uint32_t xo = (uint32_t)(c * 16 * (int)sizeof(XT) + q * K::XBYTES);
+  const uint32_t xlog = (uint32_t)(c * 16 * (int)sizeof(XT) + q * K::XBYTES);
+  const uint32_t xo[2] = {swz128(xlog), swz128(xlog + 16)};
   const float* wcol = ws + c;
   uint32_t n = 0;  // ordinal of the CTA's next edge
   int buf = 0;
   bool failed = false;
   // Edge m lives in slot m % S, phase (m / S) & 1.
-  auto fetch = [&](uint32_t m, float (&yv)[16], float (&xv)[KQ]) {
+  auto fetch = [&](uint32_t m, float2 (&yv)[8], float (&xv)[KQ]) {
     const uint32_t s = m % S, par = (m / S) & 1u;
     if (!mbar_try_wait(full0 + 8 * s, par))
       if (!mbar_wait_slow(full0 + 8 * s, par, a.watchdog, 1, failed)) failed = true;
     const float4* yp = ys + 4 * (m & 63);
-    const float4 y0 = yp[0], y1 = yp[1], y2 = yp[2], y3 = yp[3];
-    yv[0] = y0.x; yv[1] = y0.y; yv[2] = y0.z; yv[3] = y0.w;
-    yv[4] = y1.x; yv[5] = y1.y; yv[6] = y1.z; yv[7] = y1.w;
-    yv[8] = y2.x; yv[9] = y2.y; yv[10] = y2.z; yv[11] = y2.w;
-    yv[12] = y3.x; yv[13] = y3.y; yv[14] = y3.z; yv[15] = y3.w;
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const float4 t = yp[h];
+      yv[2 * h] = make_float2(t.x, t.y);
+      yv[2 * h + 1] = make_float2(t.z, t.w);
+    }
     load_x<XT, KQ>(smem + K::OFF_X + s * K::SLOT, xo, xv);
   };
   auto release = [&](uint32_t m) {
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * (m % S));
   };
-  float yA[16], xA[KQ], yB[16], xB[KQ];
+  float2 yA[8], yB[8];
+  float xA[KQ], xB[KQ];
   if (total > 0) fetch(0, yA, xA);
   for (int r = r_begin; r < r_end; ++r) {
     if (r - chunk == 32) {
@@ -380,11 +397,11 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
     const int a1x = __shfl_sync(0xffffffffu, off_nxt, 0);
     const int a1 = j0 == 31 ? a1x : a1n;
     const int deg = min(max(a1 - a0, 0), total - (int)n);
-    float acc[KQ][16];
+    float2 acc[KQ][8];
 #pragma unroll
     for (int i = 0; i < KQ; ++i)
 #pragma unroll
-      for (int k = 0; k < 16; ++k) acc[i][k] = 0.0f;
+      for (int k = 0; k < 8; ++k) acc[i][k] = make_float2(0.0f, 0.0f);
 
     // Two edges per trip: the smem loads of the next edge are in flight
     // while the FMAs of the current one issue.
@@ -402,7 +419,7 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
       fma_edge(acc, yA, xA);
       release(n);
 #pragma unroll
-      for (int k = 0; k < 16; ++k) yA[k] = yB[k];
+      for (int k = 0; k < 8; ++k) yA[k] = yB[k];
 #pragma unroll
       for (int i = 0; i < KQ; ++i) xA[i] = xB[i];
       ++n;

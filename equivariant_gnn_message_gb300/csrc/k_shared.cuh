@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, K::NCW);
+      mbar_init(empty0 + 8 * s, K::NCONS);  // every consumer thread releases
     }
     fence_mbar_init();
   }
@@ -319,6 +319,17 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
         ++n;
       }
     }
+    // Tail: one empty edge at ordinal `total` (phase completed by a plain
+    // arrive, no data) so the consumers' one-edge look-ahead never waits
+    // on a slot that is not coming.
+    if (ok && lane == 0) {
+      const uint32_t s = n % S, par = ((n / S) & 1u) ^ 1u;
+      if (mbar_try_wait(empty0 + 8 * s, par) || mbar_wait(empty0 + 8 * s, par, a.watchdog, 2)) {
+        mbar_arrive(full0 + 8 * s);
+        ++n;
+      }
+    }
+    n = __shfl_sync(0xffffffffu, n, 0);
     // Drain: wait until the loads of the last min(S, n) issued edges have
     // landed, so no bulk copy is in flight when this warp leaves.
     if (lane == 0) {
@@ -378,13 +389,11 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
     }
     load_x<XT, KQ>(smem + K::OFF_X + s * K::SLOT, xo, xv);
   };
-  auto release = [&](uint32_t m) {
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8 * (m % S));
-  };
+  // Each consumer thread arrives once its own reads of slot m are done.
+  auto release = [&](uint32_t m) { mbar_arrive(empty0 + 8 * (m % S)); };
   float2 yA[8], yB[8];
   float xA[KQ], xB[KQ];
-  if (total > 0) fetch(0, yA, xA);
+  fetch(0, yA, xA);
   for (int r = r_begin; r < r_end; ++r) {
     if (r - chunk == 32) {
       chunk += 32;
@@ -404,18 +413,19 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
       for (int k = 0; k < 8; ++k) acc[i][k] = make_float2(0.0f, 0.0f);
 
     // Two edges per trip: the smem loads of the next edge are in flight
-    // while the FMAs of the current one issue.
+    // while the FMAs of the current one issue.  The look-ahead may reach
+    // ordinal `total`, the producer's empty tail edge (never used).
     int j = 0;
     for (; j + 2 <= deg; j += 2, n += 2) {
-      if (n + 1 < (uint32_t)total) fetch(n + 1, yB, xB);
+      fetch(n + 1, yB, xB);
       fma_edge(acc, yA, xA);
       release(n);
-      if (n + 2 < (uint32_t)total) fetch(n + 2, yA, xA);
+      fetch(n + 2, yA, xA);
       fma_edge(acc, yB, xB);
       release(n + 1);
     }
     if (j < deg) {
-      if (n + 1 < (uint32_t)total) fetch(n + 1, yB, xB);
+      fetch(n + 1, yB, xB);
       fma_edge(acc, yA, xA);
       release(n);
 #pragma unroll

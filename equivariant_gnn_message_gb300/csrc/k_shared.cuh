@@ -42,11 +42,12 @@ struct SharedTune {
 #else
   static constexpr int KQ = C >= 64 ? 8 : 4;
 #endif
-  static constexpr int ROW = C * 16 * (int)sizeof(XT);
 #ifdef EQMP_TUNE_S
-  static constexpr int S = EQMP_TUNE_S;
+  static constexpr int S_MAX = EQMP_TUNE_S;
 #else
-  static constexpr int S = ROW >= 4096 && !(C >= 128 && sizeof(XT) == 2) ? 8 : 16;
+  // Slots in flight hide the row-gather latency (Little's law: about
+  // 16 x 4 KB per CTA at two CTAs per SM); capped by the shared-memory budget.
+  static constexpr int S_MAX = 32;
 #endif
 };
 
@@ -73,7 +74,15 @@ struct SharedCfg {
   static constexpr int ROWS = ROW_BYTES / 128;        // 128-byte TMA box rows per node
   static constexpr int INNER = 128 / (int)sizeof(XT);  // elements per box row
   static constexpr int SLOT = ROW_BYTES < 1024 ? 1024 : ROW_BYTES;  // swizzle atom aligned
-  static constexpr int S = SharedTune<C, XT>::S;
+  // Shared memory besides the x slots: SH ring, partial sums, weights,
+  // barriers and alignment slack.  The slots take what is left of the
+  // per-CTA share of the SM's 227 KB, rounded down to a power of two.
+  static constexpr int FIXED = 64 * 64 + 2 * NQ * 16 * C * 4 + 34 * C * 4 + 2 * 32 * 8 + 1024;
+  static constexpr int BUDGET = 227 * 1024 / MIN_BLOCKS - 1024 - FIXED;
+  static constexpr int S_FIT = BUDGET / SLOT;
+  static constexpr int S_CAP = S_FIT < SharedTune<C, XT>::S_MAX ? S_FIT : SharedTune<C, XT>::S_MAX;
+  static constexpr int S = S_CAP >= 32 ? 32 : S_CAP >= 16 ? 16 : S_CAP >= 8 ? 8 : 4;
+  static_assert(S_CAP >= 4, "not even four slots fit");
   static_assert((S & (S - 1)) == 0 && S <= 32, "ring size: power of two, at most one batch");
   static constexpr int OFF_X = 0;
   static constexpr int OFF_Y = OFF_X + S * SLOT;            // 64-entry SH ring (2 batches of 32)

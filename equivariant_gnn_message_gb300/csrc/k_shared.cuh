@@ -77,7 +77,9 @@ struct SharedCfg {
   // Shared memory besides the x slots: SH ring, partial sums, weights,
   // barriers and alignment slack.  The slots take what is left of the
   // per-CTA share of the SM's 227 KB, rounded down to a power of two.
-  static constexpr int FIXED = 64 * 64 + 2 * NQ * 16 * C * 4 + 34 * C * 4 + 2 * 32 * 8 + 1024;
+  static constexpr int NP = WS ? 4 : 1;              // producer warps (batches of 32 edges, round robin)
+  static constexpr int YR = 64 * NP;                 // SH ring entries (2 batches per producer warp)
+  static constexpr int FIXED = YR * 64 + 2 * NQ * 16 * C * 4 + 34 * C * 4 + 2 * 32 * 8 + 1024;
   static constexpr int BUDGET = 227 * 1024 / MIN_BLOCKS - 1024 - FIXED;
   static constexpr int S_FIT = BUDGET / SLOT;
   static constexpr int S_CAP = S_FIT < SharedTune<C, XT>::S_MAX ? S_FIT : SharedTune<C, XT>::S_MAX;
@@ -85,8 +87,8 @@ struct SharedCfg {
   static_assert(S_CAP >= 4, "not even four slots fit");
   static_assert((S & (S - 1)) == 0 && S <= 32, "ring size: power of two, at most one batch");
   static constexpr int OFF_X = 0;
-  static constexpr int OFF_Y = OFF_X + S * SLOT;            // 64-entry SH ring (2 batches of 32)
-  static constexpr int OFF_RED = OFF_Y + 64 * 64;
+  static constexpr int OFF_Y = OFF_X + S * SLOT;            // SH ring, YR entries of 16 floats
+  static constexpr int OFF_RED = OFF_Y + YR * 64;
   static constexpr int OFF_W = OFF_RED + 2 * NQ * 16 * C * 4;
   static constexpr int OFF_BAR = OFF_W + 34 * C * 4;
   static constexpr int SMEM_BYTES = OFF_BAR + 2 * S * 8 + 1024;  // + base alignment slack
@@ -266,21 +268,23 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
 
   if (K::WS ? tid < K::CONS0 : tid >= K::NCONS) {
     // ------------------------------------------------------------ producer
-    if constexpr (K::WS) {
-      setmaxnreg_dec<K::RP>();
-      if (tid >= 32) return;  // one producer warp; the rest of warpgroup 0 idles out
-    }
-    // Batches of 32 edges: lane l owns edge base+l.  The sender index (and
-    // edge vector) of the NEXT batch are loaded while this batch is issued.
-    // All lanes compute their 16 SH at once into the batch's half of the SH
-    // ring (entry = edge ordinal % 64); then lanes take turns in CSR order to
-    // claim an x slot and launch the row copy of x[src] (tp_scatter: plus a
-    // 64-byte copy of the stored SH row into the ring).  The SH ring half of
-    // batch k was last read for batch k-2, whose slots were all released
-    // before batch k-1 finished issuing (S <= 32), so the overwrite is safe;
-    // each lane's arrive publishes its own SH stores.
+    if constexpr (K::WS) setmaxnreg_dec<K::RP>();
+    // NP producer warps; warp w issues the batches k = w, w+NP, ... of 32
+    // edges (ordinals 32k .. 32k+31).  An edge's slot (ordinal % S) and phase
+    // are fixed by its ordinal, and its empty-wait proves the consumers
+    // released the slot's previous edge, so the warps need no coordination.
+    // Per batch: the sender indices (and edge vectors) of the warp's next
+    // batch are loaded while this one is issued; all lanes compute their 16
+    // SH at once into the SH ring (entry = ordinal % YR); then lanes take
+    // turns in CSR order to claim an x slot and launch the row copy of
+    // x[src] (tp_scatter: plus a 64-byte copy of the stored SH row).  The SH
+    // ring entries of batch k were last read for batch k - YR/32; this warp
+    // issued batch k - NP, whose empty-waits proved every edge up to
+    // 32(k-NP) + 31 - S released, which covers batch k - YR/32 (YR = 64 NP,
+    // S <= 32).  Each lane's arrive publishes its own SH stores.
+    const int pw = K::WS ? tid >> 5 : 0;  // producer warp index (the non-specialised CTA has one)
     const int lane = tid & 31;
-    if (lane == 0) prefetch_tmap(&tmap);
+    if (lane == 0 && pw == 0) prefetch_tmap(&tmap);
     auto load_edge = [&](int e, int& node, float& vx, float& vy, float& vz) {
       node = 0; vx = vy = vz = 0.0f;
       if (e < e_end) {
@@ -292,14 +296,17 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
       }
     };
     constexpr uint32_t TX = K::ROW_BYTES + (FROM_VEC ? 0 : 64);
-    uint32_t n = 0;
     bool ok = true;
     int node_nx;
     float vx_nx, vy_nx, vz_nx;
-    load_edge(e_begin + lane, node_nx, vx_nx, vy_nx, vz_nx);
-    for (int base = e_begin; base < e_end && ok; base += 32) {
+    const int nbatch = (total + 31) / 32;
+    load_edge(e_begin + 32 * pw + lane, node_nx, vx_nx, vy_nx, vz_nx);
+    uint32_t last = 0, issued = 0;  // this warp's last issued ordinal + 1, and count
+    for (int k = pw; k < nbatch && ok; k += K::NP) {
+      const int base = e_begin + 32 * k;
+      const uint32_t n0 = 32u * k;
       const int node = node_nx;
-      float4* yd = ys + 4 * ((n + lane) & 63);
+      float4* yd = ys + 4 * ((n0 + lane) % K::YR);
       if constexpr (FROM_VEC) {
         float y[16];
         real_sh16(vx_nx, vy_nx, vz_nx, y);
@@ -308,11 +315,12 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
         yd[2] = make_float4(y[8], y[9], y[10], y[11]);
         yd[3] = make_float4(y[12], y[13], y[14], y[15]);
       }
-      load_edge(base + 32 + lane, node_nx, vx_nx, vy_nx, vz_nx);  // next batch, in flight
+      load_edge(base + 32 * K::NP + lane, node_nx, vx_nx, vy_nx, vz_nx);  // next own batch, in flight
       const int cnt = min(32, e_end - base);
       for (int j = 0; j < cnt; ++j) {
         int good = 1;
         if (lane == j) {
+          const uint32_t n = n0 + j;
           const uint32_t s = n % S, par = ((n / S) & 1u) ^ 1u;
           if (mbar_try_wait(empty0 + 8 * s, par) || mbar_wait(empty0 + 8 * s, par, a.watchdog, 2)) {
             mbar_arrive_expect_tx(full0 + 8 * s, TX);
@@ -325,26 +333,26 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
           }
         }
         if (!__all_sync(0xffffffffu, good)) { ok = false; break; }
-        ++n;
+        last = n0 + j + 1;
+        ++issued;
       }
     }
     // Tail: one empty edge at ordinal `total` (phase completed by a plain
-    // arrive, no data) so the consumers' one-edge look-ahead never waits
-    // on a slot that is not coming.
-    if (ok && lane == 0) {
+    // arrive, no data), issued by the warp that owns its batch, so the
+    // consumers' one-edge look-ahead never waits on a slot that is not coming.
+    if (ok && pw == (int)((total / 32) % K::NP) && lane == 0) {
+      const uint32_t n = (uint32_t)total;
       const uint32_t s = n % S, par = ((n / S) & 1u) ^ 1u;
-      if (mbar_try_wait(empty0 + 8 * s, par) || mbar_wait(empty0 + 8 * s, par, a.watchdog, 2)) {
+      if (mbar_try_wait(empty0 + 8 * s, par) || mbar_wait(empty0 + 8 * s, par, a.watchdog, 2))
         mbar_arrive(full0 + 8 * s);
-        ++n;
-      }
     }
-    n = __shfl_sync(0xffffffffu, n, 0);
-    // Drain: wait until the loads of the last min(S, n) issued edges have
-    // landed, so no bulk copy is in flight when this warp leaves.
-    if (lane == 0) {
-      const uint32_t first = n > (uint32_t)S ? n - S : 0;
-      for (uint32_t i = first; i < n; ++i)
-        if (!mbar_wait(full0 + 8 * (i % S), (i / S) & 1u, a.watchdog, 3)) break;
+    // Drain: wait until this warp's loads among the last S ordinals have
+    // landed, so no bulk copy of this warp is in flight when it leaves.
+    if (lane == 0 && issued > 0) {
+      const uint32_t first = last > (uint32_t)S ? last - S : 0;
+      for (uint32_t i = first; i < last; ++i)
+        if (((i / 32) % K::NP) == (uint32_t)pw)
+          if (!mbar_wait(full0 + 8 * (i % S), (i / S) & 1u, a.watchdog, 3)) break;
     }
     return;
   }
@@ -389,7 +397,7 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
     const uint32_t s = m % S, par = (m / S) & 1u;
     if (!mbar_try_wait(full0 + 8 * s, par))
       if (!mbar_wait_slow(full0 + 8 * s, par, a.watchdog, 1, failed)) failed = true;
-    const float4* yp = ys + 4 * (m & 63);
+    const float4* yp = ys + 4 * (m % K::YR);
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
       const float4 t = yp[h];

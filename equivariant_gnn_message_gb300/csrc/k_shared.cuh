@@ -269,25 +269,32 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
   if (K::WS ? tid < K::CONS0 : tid >= K::NCONS) {
     // ------------------------------------------------------------ producer
     if constexpr (K::WS) setmaxnreg_dec<K::RP>();
-    // NP producer warps; warp w issues the batches k = w, w+NP, ... of 32
-    // edges (ordinals 32k .. 32k+31).  An edge's slot (ordinal % S) and phase
-    // are fixed by its ordinal, and its empty-wait proves the consumers
-    // released the slot's previous edge, so the warps need no coordination.
-    // Per batch: the sender indices (and edge vectors) of the warp's next
-    // batch are loaded while this one is issued; all lanes compute their 16
-    // SH at once into the SH ring (entry = ordinal % YR); then lanes take
-    // turns in CSR order to claim an x slot and launch the row copy of
-    // x[src] (tp_scatter: plus a 64-byte copy of the stored SH row).  The SH
-    // ring entries of batch k were last read for batch k - YR/32; this warp
-    // issued batch k - NP, whose empty-waits proved every edge up to
-    // 32(k-NP) + 31 - S released, which covers batch k - YR/32 (YR = 64 NP,
-    // S <= 32).  Each lane's arrive publishes its own SH stores.
+    // NP producer warps.  Ordinals come in chunks of CH = S / NP edges and
+    // chunk c belongs to warp c % NP, so slot s = ordinal % S always belongs
+    // to warp (s / CH) and every warp issues its own edges in increasing
+    // order: a warp is never more than one phase ahead on any of its slots,
+    // which is what parity waits require.  A warp works on 32 of its edges at
+    // a time (lane l: chunk w + NP (32g/CH + l/CH), element l % CH): the sender
+    // indices (and edge vectors) of its next 32 are loaded while these are
+    // issued; all lanes compute their 16 SH at once into the SH ring (entry =
+    // ordinal % YR); then lanes take turns to claim their slot and launch the
+    // row copy of x[src] (tp_scatter: plus a 64-byte copy of the stored SH
+    // row).  SH ring reuse: entry n was last used by ordinal n - YR; before
+    // this round the warp issued its previous 32 edges (up to 32 NP ordinals
+    // back), whose empty-waits proved every ordinal up to that point minus S
+    // released; YR >= 32 NP + S.  Each lane's arrive publishes its own SH.
+    constexpr int CH = S / K::NP;
+    static_assert(CH >= 1 && 32 % CH == 0 && K::YR >= 32 * K::NP + S, "producer layout");
     const int pw = K::WS ? tid >> 5 : 0;  // producer warp index (the non-specialised CTA has one)
     const int lane = tid & 31;
     if (lane == 0 && pw == 0) prefetch_tmap(&tmap);
-    auto load_edge = [&](int e, int& node, float& vx, float& vy, float& vz) {
+    auto ordinal = [&](int g) {
+      return (uint32_t)((pw + K::NP * (g * (32 / CH) + lane / CH)) * CH + lane % CH);
+    };
+    auto load_edge = [&](uint32_t n, int& node, float& vx, float& vy, float& vz) {
       node = 0; vx = vy = vz = 0.0f;
-      if (e < e_end) {
+      if (n < (uint32_t)total) {
+        const int e = e_begin + (int)n;
         node = __ldg(a.src + e);
         if constexpr (FROM_VEC) {
           const float* v = a.vec + 3 * (size_t)e;
@@ -299,14 +306,14 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
     bool ok = true;
     int node_nx;
     float vx_nx, vy_nx, vz_nx;
-    const int nbatch = (total + 31) / 32;
-    load_edge(e_begin + 32 * pw + lane, node_nx, vx_nx, vy_nx, vz_nx);
-    uint32_t last = 0, issued = 0;  // this warp's last issued ordinal + 1, and count
-    for (int k = pw; k < nbatch && ok; k += K::NP) {
-      const int base = e_begin + 32 * k;
-      const uint32_t n0 = 32u * k;
+    load_edge(ordinal(0), node_nx, vx_nx, vy_nx, vz_nx);
+    uint32_t last = 0;  // this warp's last issued ordinal + 1 (0: none)
+    for (int g = 0; ok; ++g) {
+      const uint32_t n = ordinal(g);
+      const uint32_t cnt = (uint32_t)__popc(__ballot_sync(0xffffffffu, n < (uint32_t)total));
+      if (cnt == 0) break;  // valid lanes are a prefix
       const int node = node_nx;
-      float4* yd = ys + 4 * ((n0 + lane) % K::YR);
+      float4* yd = ys + 4 * (n % K::YR);
       if constexpr (FROM_VEC) {
         float y[16];
         real_sh16(vx_nx, vy_nx, vz_nx, y);
@@ -315,43 +322,46 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
         yd[2] = make_float4(y[8], y[9], y[10], y[11]);
         yd[3] = make_float4(y[12], y[13], y[14], y[15]);
       }
-      load_edge(base + 32 * K::NP + lane, node_nx, vx_nx, vy_nx, vz_nx);  // next own batch, in flight
-      const int cnt = min(32, e_end - base);
-      for (int j = 0; j < cnt; ++j) {
+      load_edge(ordinal(g + 1), node_nx, vx_nx, vy_nx, vz_nx);  // next 32 of this warp, in flight
+      for (uint32_t j = 0; j < cnt; ++j) {
         int good = 1;
-        if (lane == j) {
-          const uint32_t n = n0 + j;
+        if ((uint32_t)lane == j) {
           const uint32_t s = n % S, par = ((n / S) & 1u) ^ 1u;
           if (mbar_try_wait(empty0 + 8 * s, par) || mbar_wait(empty0 + 8 * s, par, a.watchdog, 2)) {
             mbar_arrive_expect_tx(full0 + 8 * s, TX);
             tma_load_2d(smem_u32(smem + K::OFF_X + s * K::SLOT), &tmap, 0, node * K::ROWS,
                         full0 + 8 * s);
             if constexpr (!FROM_VEC)
-              bulk_load(smem_u32(yd), a.Y + 16 * (size_t)(base + j), 64, full0 + 8 * s);
+              bulk_load(smem_u32(yd), a.Y + 16 * (size_t)(e_begin + (int)n), 64, full0 + 8 * s);
           } else {
             good = 0;
           }
         }
         if (!__all_sync(0xffffffffu, good)) { ok = false; break; }
-        last = n0 + j + 1;
-        ++issued;
       }
+      if (ok) last = __shfl_sync(0xffffffffu, n, (int)cnt - 1) + 1;
     }
     // Tail: one empty edge at ordinal `total` (phase completed by a plain
-    // arrive, no data), issued by the warp that owns its batch, so the
-    // consumers' one-edge look-ahead never waits on a slot that is not coming.
-    if (ok && pw == (int)((total / 32) % K::NP) && lane == 0) {
-      const uint32_t n = (uint32_t)total;
-      const uint32_t s = n % S, par = ((n / S) & 1u) ^ 1u;
-      if (mbar_try_wait(empty0 + 8 * s, par) || mbar_wait(empty0 + 8 * s, par, a.watchdog, 2))
-        mbar_arrive(full0 + 8 * s);
+    // arrive, no data), issued by the warp that owns its slot after all its
+    // real edges, so the consumers' one-edge look-ahead never waits on a slot
+    // that is not coming.
+    if (ok && pw == (int)(((uint32_t)total / CH) % K::NP)) {
+      if (lane == 0) {
+        const uint32_t n = (uint32_t)total;
+        const uint32_t s = n % S, par = ((n / S) & 1u) ^ 1u;
+        if (mbar_try_wait(empty0 + 8 * s, par) || mbar_wait(empty0 + 8 * s, par, a.watchdog, 2))
+          mbar_arrive(full0 + 8 * s);
+      }
+      last = (uint32_t)total + 1;  // the tail is this warp's latest ordinal on its slot
     }
     // Drain: wait until this warp's loads among the last S ordinals have
-    // landed, so no bulk copy of this warp is in flight when it leaves.
-    if (lane == 0 && issued > 0) {
+    // landed, so no bulk copy of this warp is in flight when it leaves.  The
+    // window [last - S, last) holds exactly the latest ordinal of each slot,
+    // so every phase waited for is the current or the one just completed.
+    if (lane == 0 && last > 0) {
       const uint32_t first = last > (uint32_t)S ? last - S : 0;
       for (uint32_t i = first; i < last; ++i)
-        if (((i / 32) % K::NP) == (uint32_t)pw)
+        if ((i / CH) % K::NP == (uint32_t)pw)
           if (!mbar_wait(full0 + 8 * (i % S), (i / S) & 1u, a.watchdog, 3)) break;
     }
     return;

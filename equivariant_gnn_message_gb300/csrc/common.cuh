@@ -92,6 +92,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* wd
   }
 }
 
+// Non-blocking test of the phase (no suspension): issue early, branch late.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Out-of-line slow path of a wait whose first try failed: keeps the hot loop
 // small.  Skips waiting once `failed` is set (the kernel then finishes its
 // loop structure without blocking and exits).

@@ -98,6 +98,10 @@ struct SharedCfg {
   static_assert(ROW_BYTES % 128 == 0, "row must be whole 128-byte lines");
 };
 
+// Consumers read ahead this many edges (the producer pads as many empty
+// edges after the last real one).
+constexpr uint32_t kLookAhead = 2;
+
 template <int N>
 __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
@@ -341,18 +345,21 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
       }
       if (ok) last = __shfl_sync(0xffffffffu, n, (int)cnt - 1) + 1;
     }
-    // Tail: one empty edge at ordinal `total` (phase completed by a plain
-    // arrive, no data), issued by the warp that owns its slot after all its
-    // real edges, so the consumers' one-edge look-ahead never waits on a slot
-    // that is not coming.
-    if (ok && pw == (int)(((uint32_t)total / CH) % K::NP)) {
-      if (lane == 0) {
-        const uint32_t n = (uint32_t)total;
-        const uint32_t s = n % S, par = ((n / S) & 1u) ^ 1u;
-        if (mbar_try_wait(empty0 + 8 * s, par) || mbar_wait(empty0 + 8 * s, par, a.watchdog, 2))
-          mbar_arrive(full0 + 8 * s);
+    // Tail: empty edges at ordinals total and total+1 (phase completed by a
+    // plain arrive, no data), each issued by the warp that owns its slot
+    // after all its real edges, so the consumers' two-edge look-ahead never
+    // waits on a slot that is not coming.
+#pragma unroll
+    for (uint32_t t = 0; t < kLookAhead; ++t) {
+      const uint32_t n = (uint32_t)total + t;
+      if (ok && pw == (int)((n / CH) % K::NP)) {
+        if (lane == 0) {
+          const uint32_t s = n % S, par = ((n / S) & 1u) ^ 1u;
+          if (mbar_try_wait(empty0 + 8 * s, par) || mbar_wait(empty0 + 8 * s, par, a.watchdog, 2))
+            mbar_arrive(full0 + 8 * s);
+        }
+        last = n + 1;  // the tail is this warp's latest ordinal on its slot
       }
-      last = (uint32_t)total + 1;  // the tail is this warp's latest ordinal on its slot
     }
     // Drain: wait until this warp's loads among the last S ordinals have
     // landed, so no bulk copy of this warp is in flight when it leaves.  The
@@ -402,11 +409,14 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
   uint32_t n = 0;  // ordinal of the CTA's next edge
   int buf = 0;
   bool failed = false;
-  // Edge m lives in slot m % S, phase (m / S) & 1.
-  auto fetch = [&](uint32_t m, float2 (&yv)[8], float (&xv)[KQ]) {
-    const uint32_t s = m % S, par = (m / S) & 1u;
-    if (!mbar_try_wait(full0 + 8 * s, par))
-      if (!mbar_wait_slow(full0 + 8 * s, par, a.watchdog, 1, failed)) failed = true;
+  // Edge m lives in slot m % S, phase (m / S) & 1; its SH in ring entry m % YR.
+  auto full_bar = [&](uint32_t m) { return full0 + 8 * (m % S); };
+  auto full_par = [&](uint32_t m) { return (m / S) & 1u; };
+  auto wait_full = [&](uint32_t m) {
+    if (!mbar_try_wait(full_bar(m), full_par(m)))
+      if (!mbar_wait_slow(full_bar(m), full_par(m), a.watchdog, 1, failed)) failed = true;
+  };
+  auto load_edge = [&](uint32_t m, float2 (&yv)[8], float (&xv)[KQ]) {
     const float4* yp = ys + 4 * (m % K::YR);
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
@@ -414,13 +424,26 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
       yv[2 * h] = make_float2(t.x, t.y);
       yv[2 * h + 1] = make_float2(t.z, t.w);
     }
-    load_x<XT, KQ>(smem + K::OFF_X + s * K::SLOT, xo, xv);
+    load_x<XT, KQ>(smem + K::OFF_X + (m % S) * K::SLOT, xo, xv);
   };
   // Each consumer thread arrives once its own reads of slot m are done.
   auto release = [&](uint32_t m) { mbar_arrive(empty0 + 8 * (m % S)); };
+  // One edge: test (non-blocking) that edge m+2 has landed, run the FMAs of
+  // edge m from registers, release m, then (waiting only if the early test
+  // failed) load edge m+2 into the registers just freed.
+  auto step = [&](float2 (&acc)[KQ][8], uint32_t m, float2 (&yv)[8], float (&xv)[KQ]) {
+    const bool ready = mbar_test_wait(full_bar(m + 2), full_par(m + 2));
+    fma_edge(acc, yv, xv);
+    release(m);
+    if (!ready) wait_full(m + 2);
+    load_edge(m + 2, yv, xv);
+  };
   float2 yA[8], yB[8];
   float xA[KQ], xB[KQ];
-  fetch(0, yA, xA);
+  wait_full(0);
+  load_edge(0, yA, xA);
+  wait_full(1);
+  load_edge(1, yB, xB);
   for (int r = r_begin; r < r_end; ++r) {
     if (r - chunk == 32) {
       chunk += 32;
@@ -439,26 +462,23 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
 #pragma unroll
       for (int k = 0; k < 8; ++k) acc[i][k] = make_float2(0.0f, 0.0f);
 
-    // Two edges per trip: the smem loads of the next edge are in flight
-    // while the FMAs of the current one issue.  The look-ahead may reach
-    // ordinal `total`, the producer's empty tail edge (never used).
+    // Two edges per trip; registers A hold edge n, B edge n+1.  The
+    // look-ahead may reach the producer's empty tail edges (never used).
     int j = 0;
     for (; j + 2 <= deg; j += 2, n += 2) {
-      fetch(n + 1, yB, xB);
-      fma_edge(acc, yA, xA);
-      release(n);
-      fetch(n + 2, yA, xA);
-      fma_edge(acc, yB, xB);
-      release(n + 1);
+      step(acc, n, yA, xA);
+      step(acc, n + 1, yB, xB);
     }
-    if (j < deg) {
-      fetch(n + 1, yB, xB);
+    if (j < deg) {  // odd degree: edge n from A, then A takes n+1 and B loads n+2
+      const bool ready = mbar_test_wait(full_bar(n + 2), full_par(n + 2));
       fma_edge(acc, yA, xA);
       release(n);
 #pragma unroll
       for (int k = 0; k < 8; ++k) yA[k] = yB[k];
 #pragma unroll
       for (int i = 0; i < KQ; ++i) xA[i] = xB[i];
+      if (!ready) wait_full(n + 2);
+      load_edge(n + 2, yB, xB);
       ++n;
     }
 

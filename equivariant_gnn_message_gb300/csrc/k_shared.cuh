@@ -66,7 +66,11 @@ struct SharedCfg {
   static constexpr int WARPS_PER_SMSP = (NTHREADS / 32 * MIN_BLOCKS + 3) / 4;
   static constexpr int R0_RAW = 16384 / (32 * WARPS_PER_SMSP);
   static constexpr int R0 = (R0_RAW > 255 ? 255 : R0_RAW) & ~7;
+#ifdef EQMP_TUNE_RP
+  static constexpr int RP = EQMP_TUNE_RP;
+#else
   static constexpr int RP = 40;
+#endif
   static constexpr int RC_RAW = WS ? (R0 * NTHREADS - RP * 128) / NCONS : R0;
   static constexpr int RC = (RC_RAW > 256 ? 256 : RC_RAW) & ~7;
   static_assert(!WS || RP * 128 + RC * NCONS <= R0 * NTHREADS, "register split exceeds the pool");
@@ -77,7 +81,11 @@ struct SharedCfg {
   // Shared memory besides the x slots: SH ring, partial sums, weights,
   // barriers and alignment slack.  The slots take what is left of the
   // per-CTA share of the SM's 227 KB, rounded down to a power of two.
-  static constexpr int NP = WS ? 4 : 1;              // producer warps (batches of 32 edges, round robin)
+#ifdef EQMP_TUNE_NP
+  static constexpr int NP = WS ? EQMP_TUNE_NP : 1;
+#else
+  static constexpr int NP = WS ? 4 : 1;              // producer warps (chunks of S/NP edges, round robin)
+#endif
   static constexpr int YR = 64 * NP;                 // SH ring entries (2 batches per producer warp)
   static constexpr int FIXED = YR * 64 + 2 * NQ * 16 * C * 4 + 34 * C * 4 + 2 * 32 * 8 + 1024;
   static constexpr int BUDGET = 227 * 1024 / MIN_BLOCKS - 1024 - FIXED;

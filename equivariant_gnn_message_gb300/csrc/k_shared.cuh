@@ -82,6 +82,7 @@ struct SharedCfg {
   // barriers and alignment slack.  The slots take what is left of the
   // per-CTA share of the SM's 227 KB, rounded down to a power of two.
 #ifdef EQMP_TUNE_NP
+  static_assert(EQMP_TUNE_NP >= 1 && EQMP_TUNE_NP <= 4, "at most the four warps of warpgroup 0");
   static constexpr int NP = WS ? EQMP_TUNE_NP : 1;
 #else
   static constexpr int NP = WS ? 4 : 1;              // producer warps (chunks of S/NP edges, round robin)
@@ -298,6 +299,7 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
     constexpr int CH = S / K::NP;
     static_assert(CH >= 1 && 32 % CH == 0 && K::YR >= 32 * K::NP + S, "producer layout");
     const int pw = K::WS ? tid >> 5 : 0;  // producer warp index (the non-specialised CTA has one)
+    if (pw >= K::NP) return;              // warpgroup 0 has 4 warps; NP of them produce
     const int lane = tid & 31;
     if (lane == 0 && pw == 0) prefetch_tmap(&tmap);
     auto ordinal = [&](int g) {

@@ -230,6 +230,7 @@ def main():
     args.warmup = max(3, args.warmup)
 
     from equivariant_gnn_message_gb300.inputs import make_workload
+    from equivariant_gnn_message_gb300.sharding import max_over_ranks
 
     wl = make_workload(args.workload)
     if args.impl == "reference":
@@ -306,11 +307,7 @@ def main():
     barrier()
     t1 = time.time()
     kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms = float(np.mean(kernel_ms))
-    if dist is not None:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(float(np.mean(kernel_ms)))
 
     # ---- e2e through the public API with pinned host buffers
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
@@ -347,11 +344,7 @@ def main():
         e_e[i].record(stream)
     barrier()
     sampler.stop()
-    e2e_ms = float(np.mean([s.elapsed_time(e) for s, e in zip(e_s, e_e)]))
-    if dist is not None:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(float(np.mean([s.elapsed_time(e) for s, e in zip(e_s, e_e)])))
     wd = eq.eqmp_device_error()
 
     if rank != 0:

@@ -39,8 +39,15 @@ METRIC = "edges/s fused SH+CG-TP+scatter (1k atoms, C=32, ~20 nbrs); % of roofli
 FLUSH_BYTES = 256 << 20
 # DRAM bytes per launch of the layer kernel from the ncu capture recorded in
 # profiles/ (None until captured for the current kernel version).
-NCU_TRAFFIC = {}
-KERNEL_VERSION = "k_shared-v1"
+# Keyed by (workload, kernel version); a changed kernel gets a new version
+# tag, which makes its entry missing (traffic null) until re-captured.
+KERNEL_VERSION = {"shared": "k_shared-lookahead-v1", "radial": "k_radial-v1"}
+NCU_TRAFFIC = {
+    ("pages_1k_c32", "k_shared-lookahead-v1"): 2358272 + 0,
+    ("scale_100k_c64", "k_shared-lookahead-v1"): 6204414000 + 407759872,
+    ("dense_10k_c128_bf16", "k_shared-lookahead-v1"): 48817152 + 10746112,
+    ("radial_1k_c32", "k_radial-v1"): 2883328 + 0,
+}
 
 
 def fma_count(wl):
@@ -360,7 +367,8 @@ def main():
     peak_tflops = props.multi_processor_count * 128 * 2 * max_mhz * 1e6 / 1e12
     flops = 2.0 * fma_count(wl)
     achieved = flops / (ms * 1e-3) / 1e12
-    traffic = NCU_TRAFFIC.get((args.workload, KERNEL_VERSION))
+    version = KERNEL_VERSION["shared" if wl.w is not None else "radial"]
+    traffic = NCU_TRAFFIC.get((args.workload, version)) if args.entry == "fused" else None
     value = wl.n_edges * world / (ms * 1e-3)
 
     cpu = None
@@ -380,7 +388,8 @@ def main():
                    "l2": "flushed (256 MB write) before every timed step",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
-                     "frac": achieved / peak_tflops, "traffic": traffic,
+                     "frac": achieved / peak_tflops, "traffic": traffic, "traffic_unit": "bytes/launch",
+                     "kernel": version,
                      "peak_basis": f"{props.multi_processor_count} SMs x 128 FP32 lanes x 2 x {max_mhz:.0f} MHz (derived)",
                      "hbm_gbs_compulsory": compulsory_bytes(wl) / (ms * 1e-3) / 1e9},
         "e2e": {"value": wl.n_edges * world / (e2e_ms * 1e-3), "unit": "edges/s",

@@ -264,11 +264,9 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
   const int r_begin = (int)((long long)a.N * b / G);
   const int r_end = (int)((long long)a.N * (b + 1) / G);
 
-  if (tid == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, K::NCONS);  // every consumer thread releases
-    }
+  if (tid < S) {
+    mbar_init(full0 + 8 * tid, 1);
+    mbar_init(empty0 + 8 * tid, K::NCONS);  // every consumer thread releases
     fence_mbar_init();
   }
   __syncthreads();  // barriers initialised; the producer starts at once

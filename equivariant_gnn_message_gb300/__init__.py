@@ -13,6 +13,8 @@ Entry points (same names as the C ABI):
   eqmp_fused(vec, x, row_offsets, src, ...)     -> out [N, C, 16]
   eqmp_validate_graph(row_offsets, src, n_src, n_edges)
   eqmp_device_error()                           -> int (watchdog code)
+  eqmp_fused_backward(vec, x, row_offsets, src, dst, send_offsets, send_edges, grad_out, ...)
+                                                -> dict of gradients
   eqmp_path_table()                             -> list of (l1, l2, l3)
 """
 import ctypes
@@ -21,7 +23,7 @@ import os
 __all__ = [
     "EqmpError", "load_library", "library_path", "eqmp_num_paths", "eqmp_path_table",
     "eqmp_status_string", "eqmp_sh", "eqmp_tp_scatter", "eqmp_fused", "eqmp_validate_graph",
-    "eqmp_device_error", "EQMP_OK", "EQMP_ERR_INVALID_ARG", "EQMP_ERR_UNSUPPORTED",
+    "eqmp_device_error", "eqmp_fused_backward", "sender_view", "EQMP_OK", "EQMP_ERR_INVALID_ARG", "EQMP_ERR_UNSUPPORTED",
     "EQMP_ERR_CUDA", "EQMP_ERR_DEVICE_TIMEOUT", "EQMP_ERR_GRAPH",
 ]
 
@@ -75,6 +77,11 @@ def load_library():
     lib.eqmp_validate_graph.restype = i32
     lib.eqmp_device_error.argtypes = [ctypes.POINTER(i32)]
     lib.eqmp_device_error.restype = i32
+    lib.eqmp_fused_backward_workspace_size.argtypes = [i64, i64, i32, i32]
+    lib.eqmp_fused_backward_workspace_size.restype = i64
+    lib.eqmp_fused_backward.argtypes = [vp, vp, i64, vp, vp, vp, vp, vp, i64, i64, i64, i32, Weights,
+                                        vp, vp, vp, vp, vp, vp, vp, i64, vp]
+    lib.eqmp_fused_backward.restype = i32
     _lib = lib
     return lib
 
@@ -214,3 +221,59 @@ def eqmp_device_error():
     if st not in (EQMP_OK, EQMP_ERR_DEVICE_TIMEOUT):
         _check(st, "eqmp_device_error")
     return int(code.value)
+
+
+def sender_view(src, n_src):
+    """(send_offsets [n_src+1], send_edges [E]) grouping edge ids by sender
+    (stable, edge order kept within a sender); host-side graph preparation
+    for eqmp_fused_backward (numpy or torch CPU int arrays in, numpy out)."""
+    import numpy as np
+
+    src = np.asarray(src, dtype=np.int64)
+    order = np.argsort(src, kind="stable").astype(np.int32)
+    offs = np.searchsorted(src[order], np.arange(int(n_src) + 1), side="left").astype(np.int32)
+    return offs, order
+
+
+def eqmp_fused_backward(vec, x, row_offsets, src, dst, send_offsets, send_edges, grad_out,
+                        w=None, R=None, M=None, need=("x", "w", "vec"), stream=None):
+    """Gradients of the fused layer; returns {"x", "w" | "R", "M", "vec"} as requested."""
+    import torch
+
+    for name, t, dt in (("vec", vec, torch.float32), ("x", x, torch.float32),
+                        ("row_offsets", row_offsets, torch.int32), ("src", src, torch.int32),
+                        ("dst", dst, torch.int32), ("send_offsets", send_offsets, torch.int32),
+                        ("send_edges", send_edges, torch.int32), ("grad_out", grad_out, torch.float32),
+                        ("w", w, torch.float32), ("R", R, torch.float32), ("M", M, torch.float32)):
+        _require(t, name, dt)
+    n_src, C = x.shape[0], x.shape[1]
+    N = row_offsets.shape[0] - 1
+    E = vec.shape[0]
+    radial = w is None
+    dev = x.device
+    out = {}
+    if "x" in need:
+        out["x"] = torch.empty((n_src, C, 16), dtype=torch.float32, device=dev)
+    if "vec" in need:
+        out["vec"] = torch.zeros((E, 3), dtype=torch.float32, device=dev)
+    if radial:
+        if "R" in need:
+            out["R"] = torch.zeros((E, 8), dtype=torch.float32, device=dev)
+        if "M" in need:
+            out["M"] = torch.empty((8, 34 * C), dtype=torch.float32, device=dev)
+    elif "w" in need:
+        out["w"] = torch.empty((34, C), dtype=torch.float32, device=dev)
+    lib = load_library()
+    nbytes = int(lib.eqmp_fused_backward_workspace_size(N, E, C, 1 if radial else 0))
+    if nbytes < 0:
+        raise EqmpError(EQMP_ERR_CUDA, "eqmp_fused_backward_workspace_size")
+    ws = torch.empty(max(nbytes // 4, 4), dtype=torch.float32, device=dev)
+    wt = (Weights(ctypes.c_void_p(w.data_ptr()), None, None, 0) if not radial else
+          Weights(None, ctypes.c_void_p(R.data_ptr()), ctypes.c_void_p(M.data_ptr()), R.shape[1]))
+    st = lib.eqmp_fused_backward(
+        _ptr(vec), _ptr(x), n_src, _ptr(row_offsets), _ptr(src), _ptr(dst), _ptr(send_offsets),
+        _ptr(send_edges), send_edges.shape[0], N, E, C, wt, _ptr(grad_out), _ptr(out.get("x")),
+        _ptr(out.get("w")), _ptr(out.get("R")), _ptr(out.get("M")), _ptr(out.get("vec")),
+        _ptr(ws), ws.numel() * 4, _stream(stream))
+    _check(st, "eqmp_fused_backward")
+    return out

@@ -1,0 +1,149 @@
+// Backward entry points: eqmp_fused_backward and its workspace size query.
+#include "k_bwd.cuh"
+#include "launch.h"
+
+namespace eqmp {
+
+constexpr int kBwdGridPerSm = 8;
+
+template <int C>
+static long long bwd_slots(long long N, int sms) {
+  using K = BwdCfg<C, false>;
+  const long long want = (N + K::GROUPS - 1) / K::GROUPS;
+  const long long cap = (long long)sms * kBwdGridPerSm;
+  return (want < cap ? want : cap) * K::GROUPS;
+}
+
+static long long slots_for(int C, long long N, int sms) {
+  switch (C) {
+    case 8: return bwd_slots<8>(N, sms);
+    case 16: return bwd_slots<16>(N, sms);
+    case 32: return bwd_slots<32>(N, sms);
+    case 64: return bwd_slots<64>(N, sms);
+    case 128: return bwd_slots<128>(N, sms);
+  }
+  return -1;
+}
+
+template <int C, bool RADIAL>
+static eqmp_status run_bwd(const BwdArgs& a, bool want_x, bool want_wv, float* gw, float* gM, int e0, int e1,
+                           cudaStream_t st, const DeviceInfo& dev) {
+  using K = BwdCfg<C, RADIAL>;
+  if (want_x && a.N_src > 0) {
+    const long long want = (a.N_src + K::GROUPS - 1) / K::GROUPS;
+    const long long cap = (long long)dev.sms * 16;
+    k_bwd_x<C, RADIAL><<<(int)(want < cap ? want : cap), K::NT, 0, st>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
+  }
+  if (want_wv && a.N > 0) {
+    const int grid = (int)(bwd_slots<C>(a.N, dev.sms) / K::GROUPS);
+    const int smem = RADIAL ? 0 : K::GROUPS * 34 * C * 4;
+    static unsigned long long attr_done = 0;
+    if (ensure_smem_attr(k_bwd_wv<C, RADIAL>, smem > 0 ? smem : 1, &attr_done) != cudaSuccess)
+      return EQMP_ERR_CUDA;
+    k_bwd_wv<C, RADIAL><<<grid, K::NT, smem, st>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
+    if (!RADIAL && gw) {
+      k_bwd_reduce_w<C><<<(34 * C + 127) / 128, 128, 0, st>>>(a.ws, grid * K::GROUPS, gw);
+      if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
+    }
+    if (RADIAL && gM) {
+      k_bwd_reduce_M<C><<<(8 * 34 * C + 127) / 128, 128, 0, st>>>(a.R, a.ws, e0, e1, gM);
+      if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
+    }
+  }
+  return EQMP_OK;
+}
+
+template <bool RADIAL>
+static eqmp_status dispatch_bwd(int C, const BwdArgs& a, bool want_x, bool want_wv, float* gw, float* gM,
+                                int e0, int e1, cudaStream_t st, const DeviceInfo& dev) {
+  switch (C) {
+    case 8: return run_bwd<8, RADIAL>(a, want_x, want_wv, gw, gM, e0, e1, st, dev);
+    case 16: return run_bwd<16, RADIAL>(a, want_x, want_wv, gw, gM, e0, e1, st, dev);
+    case 32: return run_bwd<32, RADIAL>(a, want_x, want_wv, gw, gM, e0, e1, st, dev);
+    case 64: return run_bwd<64, RADIAL>(a, want_x, want_wv, gw, gM, e0, e1, st, dev);
+    case 128: return run_bwd<128, RADIAL>(a, want_x, want_wv, gw, gM, e0, e1, st, dev);
+  }
+  return EQMP_ERR_UNSUPPORTED;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace eqmp
+
+using namespace eqmp;
+
+extern "C" {
+
+int64_t eqmp_fused_backward_workspace_size(int64_t N, int64_t E, int32_t C, int32_t radial) {
+  if (N < 0 || E < 0) return -1;
+  if (radial) return E * 34 * (int64_t)C * 4;
+  DeviceInfo dev;
+  if (device_info(&dev) != EQMP_OK) return -1;
+  const long long slots = slots_for(C, N, dev.sms);
+  return slots < 0 ? -1 : slots * 34 * (int64_t)C * 4;
+}
+
+eqmp_status eqmp_fused_backward(const float* vec, const float* x, int64_t N_src, const int32_t* row_offsets,
+                                const int32_t* src, const int32_t* dst, const int32_t* send_offsets,
+                                const int32_t* send_edges, int64_t E_send, int64_t N, int64_t E, int32_t C,
+                                eqmp_weights weights, const float* grad_out, float* grad_x, float* grad_w,
+                                float* grad_R, float* grad_M, float* grad_vec, void* workspace,
+                                int64_t workspace_bytes, eqmp_stream_t stream) {
+  if (N < 0 || E < 0 || N_src < 0 || E_send < 0) return EQMP_ERR_INVALID_ARG;
+  if (N > INT32_MAX - 1 || E > INT32_MAX || N_src > INT32_MAX - 1 || E_send > INT32_MAX)
+    return EQMP_ERR_INVALID_ARG;
+  if (C != 8 && C != 16 && C != 32 && C != 64 && C != 128) return EQMP_ERR_UNSUPPORTED;
+  const bool radial = weights.w == nullptr;
+  if (!radial && (weights.R || weights.M || weights.K != 0)) return EQMP_ERR_INVALID_ARG;
+  if (radial && weights.K != 8) return EQMP_ERR_UNSUPPORTED;
+  if (radial && E > 0 && (!weights.R || !weights.M)) return EQMP_ERR_INVALID_ARG;
+  if (!radial && (grad_R || grad_M)) return EQMP_ERR_INVALID_ARG;
+  if (radial && grad_w) return EQMP_ERR_INVALID_ARG;
+  const bool want_x = grad_x != nullptr;
+  const bool want_wv = grad_vec || grad_w || grad_R || grad_M;
+  if (want_x && (!send_offsets || (E_send > 0 && (!send_edges || !dst)) || !aligned16(grad_x)))
+    return EQMP_ERR_INVALID_ARG;
+  if ((want_x || want_wv) && N > 0 && (!row_offsets || !grad_out || !aligned16(grad_out)))
+    return EQMP_ERR_INVALID_ARG;
+  if (E > 0 && (want_x || want_wv) && (!vec || !src || !x || !aligned16(x) || N_src < 1))
+    return EQMP_ERR_INVALID_ARG;
+  if (radial && E > 0 && (!aligned16(weights.R) || (grad_R && !aligned16(grad_R)))) return EQMP_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  eqmp_status s = device_info(&dev);
+  if (s != EQMP_OK) return s;
+  const int64_t need = want_wv ? eqmp_fused_backward_workspace_size(N, E, C, radial ? 1 : 0) : 0;
+  if (need < 0) return EQMP_ERR_CUDA;
+  if (want_wv && need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+    return EQMP_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int e0 = 0, e1 = 0;
+  if (radial && grad_M && N > 0) {
+    // the edge range of this call's receivers, read once (synchronous)
+    int h[2] = {0, 0};
+    if (cudaMemcpyAsync(&h[0], row_offsets, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaMemcpyAsync(&h[1], row_offsets + N, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+      return EQMP_ERR_CUDA;
+    e0 = h[0] < 0 ? 0 : (h[0] > E ? (int)E : h[0]);
+    e1 = h[1] < e0 ? e0 : (h[1] > E ? (int)E : h[1]);
+  }
+  BwdArgs a{};
+  a.vec = vec; a.x = x; a.off = row_offsets; a.src = src; a.dst = dst;
+  a.send_off = send_offsets; a.send_edges = send_edges;
+  a.w = weights.w; a.R = weights.R; a.M = weights.M; a.g = grad_out;
+  a.gx = grad_x; a.gvec = grad_vec; a.gR = grad_R; a.ws = static_cast<float*>(workspace);
+  a.N = (int)N; a.E = (int)E; a.N_src = (int)N_src; a.n_send = (int)E_send;
+  if (radial && grad_M && e1 == e0) {  // no edge: dL/dM = 0
+    if (cudaMemsetAsync(grad_M, 0, (size_t)8 * 34 * C * 4, st) != cudaSuccess) return EQMP_ERR_CUDA;
+    grad_M = nullptr;
+  }
+  if (!radial && grad_w && N == 0) {
+    if (cudaMemsetAsync(grad_w, 0, (size_t)34 * C * 4, st) != cudaSuccess) return EQMP_ERR_CUDA;
+  }
+  return radial ? dispatch_bwd<true>(C, a, want_x, want_wv, nullptr, grad_M, e0, e1, st, dev)
+                : dispatch_bwd<false>(C, a, want_x, want_wv, grad_w, nullptr, 0, 0, st, dev);
+}
+
+}  // extern "C"

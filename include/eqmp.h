@@ -136,6 +136,37 @@ eqmp_status eqmp_fused(const float* vec, const void* x, int64_t N_src, eqmp_dtyp
                        eqmp_stream_t stream);
 
 /*
+ * Backward of eqmp_fused (fp32 storage): gradients of a scalar loss L given
+ * grad_out = dL/dout [N][C][16] fp32 (16-byte aligned):
+ *   grad_x   [N_src][C][16]  dL/dx, every row written (0 for nodes that send nothing)
+ *   grad_w   [34][C]         dL/dw            (shared weights)
+ *   grad_R   [E][8]          dL/dR            (radial weights; rows of this call's edges)
+ *   grad_M   [8][34*C]       dL/dM            (radial weights)
+ *   grad_vec [E][3]          dL/dvec, forces through the harmonics' derivative
+ *                            (rows of this call's edges; 0 for zero-length vectors)
+ * Any output may be NULL to skip it.  The chain rule is the plain one (see
+ * the forward formula); the harmonics' derivative is that of the real SH in
+ * the blog's section "2. 寄存器中间计算", n = v/|v| projected.
+ * dL/dx needs the sender-grouped view of the same edges: send_edges[E_send]
+ * lists edge ids grouped by sender, send_offsets[N_src+1] indexes it, and
+ * dst[E] gives each edge's receiver (0-based, < N).  The other gradients use
+ * row_offsets/src like the forward.  workspace: device memory of at least
+ * eqmp_fused_backward_workspace_size(N, E, C, radial) bytes (16-byte aligned),
+ * used for the fixed-order (deterministic) weight-gradient reductions; its
+ * contents on entry are ignored.  x must be fp32.  Radial grad_M reads
+ * row_offsets[0] and row_offsets[N] back to the host (synchronises the stream).
+ */
+int64_t eqmp_fused_backward_workspace_size(int64_t N, int64_t E, int32_t C, int32_t radial);
+
+eqmp_status eqmp_fused_backward(const float* vec, const float* x, int64_t N_src,
+                                const int32_t* row_offsets, const int32_t* src, const int32_t* dst,
+                                const int32_t* send_offsets, const int32_t* send_edges, int64_t E_send,
+                                int64_t N, int64_t E, int32_t C, eqmp_weights weights,
+                                const float* grad_out, float* grad_x, float* grad_w, float* grad_R,
+                                float* grad_M, float* grad_vec, void* workspace, int64_t workspace_bytes,
+                                eqmp_stream_t stream);
+
+/*
  * Synchronous check of the graph preconditions on device data:
  * 0 <= row_offsets[0] <= ... <= row_offsets[N] <= E and
  * 0 <= src[e] < N_src for every e in [row_offsets[0], row_offsets[N]).

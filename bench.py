@@ -233,6 +233,8 @@ def main():
     ap.add_argument("--workload", default="pages_1k_c32")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--entry", default="fused", choices=["fused", "tp_scatter"])
+    ap.add_argument("--pass", dest="which", default="forward", choices=["forward", "backward"],
+                    help="backward: time eqmp_fused_backward (dx, dw or dR/dM, dvec) instead")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -285,8 +287,19 @@ def main():
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
+    bwd_args = None
+    if args.which == "backward":
+        if wl.storage != "f32":
+            raise SystemExit("the backward pass takes fp32 features")
+        so, se = eq.sender_view(wl.src, wl.n_atoms)
+        gout = torch.randn((wl.n_atoms, wl.channels, 16), device=dev, generator=torch.Generator(device=dev).manual_seed(0))
+        need = ("x", "vec", "w") if w is not None else ("x", "vec", "R", "M")
+        bwd_args = ((vec, x, off, src, t(wl.dst), t(so), t(se), gout), dict(need=need, **wkw))
+
     def step():
-        if args.entry == "fused":
+        if bwd_args is not None:
+            eq.eqmp_fused_backward(*bwd_args[0], **bwd_args[1])
+        elif args.entry == "fused":
             eq.eqmp_fused(vec, x, off, src, out=out, **wkw)
         else:
             eq.eqmp_sh(vec, Yb)
@@ -339,19 +352,21 @@ def main():
         eq.eqmp_fused(d_in["vec"], xd, d_in["off"], d_in["src"], out=out, **kw)
         h_out.copy_(out, non_blocking=True)
 
-    for _ in range(3):
-        e2e_step()
-    barrier()
-    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    for i in range(args.steps):
-        flush.zero_()
-        e_s[i].record(stream)
-        e2e_step()
-        e_e[i].record(stream)
-    barrier()
+    e2e_ms = None
+    if bwd_args is None:  # the end-to-end figure is the forward layer's
+        for _ in range(3):
+            e2e_step()
+        barrier()
+        e_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        e_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            e_s[i].record(stream)
+            e2e_step()
+            e_e[i].record(stream)
+        barrier()
+        e2e_ms = max_over_ranks(float(np.mean([s.elapsed_time(e) for s, e in zip(e_s, e_e)])))
     sampler.stop()
-    e2e_ms = max_over_ranks(float(np.mean([s.elapsed_time(e) for s, e in zip(e_s, e_e)])))
     wd = eq.eqmp_device_error()
 
     if rank != 0:
@@ -365,9 +380,11 @@ def main():
     peaks = json.load(open(peaks_path)) if os.path.exists(peaks_path) else {}
     max_mhz = clocks.get("sm_max_mhz") or peaks.get("sm_max_mhz") or 2070.0
     peak_tflops = props.multi_processor_count * 128 * 2 * max_mhz * 1e6 / 1e12
-    flops = 2.0 * fma_count(wl)
+    # backward: three forward-sized contractions (dx, the weight gradient,
+    # dY) of the lowest-FMA schedule plus the SH Jacobian (48 FMA per edge)
+    flops = 2.0 * fma_count(wl) if bwd_args is None else 2.0 * (3 * fma_count(wl) + 48 * wl.n_edges)
     achieved = flops / (ms * 1e-3) / 1e12
-    version = KERNEL_VERSION["shared" if wl.w is not None else "radial"]
+    version = KERNEL_VERSION["shared" if wl.w is not None else "radial"] if bwd_args is None else "k_bwd-v1"
     traffic = NCU_TRAFFIC.get((args.workload, version)) if args.entry == "fused" else None
     value = wl.n_edges * world / (ms * 1e-3)
 
@@ -392,9 +409,11 @@ def main():
                      "kernel": version,
                      "peak_basis": f"{props.multi_processor_count} SMs x 128 FP32 lanes x 2 x {max_mhz:.0f} MHz (derived)",
                      "hbm_gbs_compulsory": compulsory_bytes(wl) / (ms * 1e-3) / 1e9},
-        "e2e": {"value": wl.n_edges * world / (e2e_ms * 1e-3), "unit": "edges/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps * (1 if args.entry == "fused" else 2),
+        "e2e": None if e2e_ms is None else {
+            "value": wl.n_edges * world / (e2e_ms * 1e-3), "unit": "edges/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "pass": args.which,
+        "gpu_launches": args.steps * ((1 if args.entry == "fused" else 2) if bwd_args is None else 3),
         "clocks": clocks,
         "kernel_ms": {"min": float(np.min(kernel_ms)), "median": float(np.median(kernel_ms))},
         "watchdog": wd,

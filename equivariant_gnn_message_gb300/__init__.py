@@ -277,3 +277,43 @@ def eqmp_fused_backward(vec, x, row_offsets, src, dst, send_offsets, send_edges,
         _ptr(ws), ws.numel() * 4, _stream(stream))
     _check(st, "eqmp_fused_backward")
     return out
+
+
+def eqmp_fused_backward_noalloc(vec, x, row_offsets, src, dst, send_offsets, send_edges, grad_out,
+                                w=None, R=None, M=None, need=("x", "w", "vec"), stream=None):
+    """eqmp_fused_backward with the library's static scratch instead of a
+    workspace (the C entry point allocates no device memory; this wrapper
+    only allocates the requested output tensors through torch)."""
+    import torch
+
+    lib = load_library()
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    fn = lib.eqmp_fused_backward_noalloc
+    fn.argtypes = [vp, vp, i64, vp, vp, vp, vp, vp, i64, i64, i64, i32, Weights,
+                   vp, vp, vp, vp, vp, vp, vp]
+    fn.restype = i32
+    n_src, C = x.shape[0], x.shape[1]
+    N = row_offsets.shape[0] - 1
+    E = vec.shape[0]
+    radial = w is None
+    dev = x.device
+    out = {}
+    if "x" in need:
+        out["x"] = torch.empty((n_src, C, 16), dtype=torch.float32, device=dev)
+    if "vec" in need:
+        out["vec"] = torch.zeros((E, 3), dtype=torch.float32, device=dev)
+    if radial:
+        if "R" in need:
+            out["R"] = torch.zeros((E, 8), dtype=torch.float32, device=dev)
+        if "M" in need:
+            out["M"] = torch.empty((8, 34 * C), dtype=torch.float32, device=dev)
+    elif "w" in need:
+        out["w"] = torch.empty((34, C), dtype=torch.float32, device=dev)
+    wt = (Weights(ctypes.c_void_p(w.data_ptr()), None, None, 0) if not radial else
+          Weights(None, ctypes.c_void_p(R.data_ptr()), ctypes.c_void_p(M.data_ptr()), R.shape[1]))
+    st = fn(_ptr(vec), _ptr(x), n_src, _ptr(row_offsets), _ptr(src), _ptr(dst), _ptr(send_offsets),
+            _ptr(send_edges), send_edges.shape[0], N, E, C, wt, _ptr(grad_out), _ptr(out.get("x")),
+            _ptr(out.get("w")), _ptr(out.get("R")), _ptr(out.get("M")), _ptr(out.get("vec")),
+            _stream(stream))
+    _check(st, "eqmp_fused_backward_noalloc")
+    return out

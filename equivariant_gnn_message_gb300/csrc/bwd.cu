@@ -1,4 +1,6 @@
 // Backward entry points: eqmp_fused_backward and its workspace size query.
+#include <mutex>
+
 #include "k_bwd.cuh"
 #include "launch.h"
 
@@ -144,6 +146,155 @@ eqmp_status eqmp_fused_backward(const float* vec, const float* x, int64_t N_src,
   }
   return radial ? dispatch_bwd<true>(C, a, want_x, want_wv, nullptr, grad_M, e0, e1, st, dev)
                 : dispatch_bwd<false>(C, a, want_x, want_wv, grad_w, nullptr, 0, 0, st, dev);
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// eqmp_fused_backward_noalloc: the same backward with its scratch in a
+// static device array instead of a caller-supplied workspace.
+//
+// Some callers cannot hand the library extra device memory: code running as
+// a plugin inside a host framework that owns the whole device memory pool,
+// or a tight simulation loop that must not pay for an allocation every
+// step.  This entry point needs nothing beyond its inputs and outputs.  Its
+// scratch is the array below, of kNoAllocBytes (8 MiB); every GPU that loads
+// the library holds it until the process exits.  All calls share the array
+// and it keeps the previous call's contents; the kernels overwrite every
+// part they later read, so nothing has to start at zero.  Two calls that
+// overlap on the GPU (other streams, other threads) race on the array.
+namespace eqmp {
+
+constexpr size_t kNoAllocBytes = size_t(8) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+// Device address of g_noalloc_scratch for the current device, looked up once
+// per device.  Host code must not pass the symbol itself to a kernel: on the
+// host it is only a stand-in, not a device address.
+static eqmp_status noalloc_scratch(float** out) {
+  static std::once_flag once[64];
+  static void* addr[64];
+  static cudaError_t err[64];
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 64) return EQMP_ERR_CUDA;
+  std::call_once(once[d], [d]() { err[d] = cudaGetSymbolAddress(&addr[d], g_noalloc_scratch); });
+  if (err[d] != cudaSuccess || addr[d] == nullptr) return EQMP_ERR_CUDA;
+  *out = static_cast<float*>(addr[d]);
+  return EQMP_OK;
+}
+
+template <int C, bool RADIAL>
+static eqmp_status run_bwd_noalloc(const BwdArgs& a, bool want_x, bool want_wv, float* gw, float* gM, int e0,
+                                   int e1, cudaStream_t st, const DeviceInfo& dev) {
+  using K = BwdCfg<C, RADIAL>;
+  if (want_x && a.N_src > 0) {
+    const long long want = (a.N_src + K::GROUPS - 1) / K::GROUPS;
+    const long long cap = (long long)dev.sms * 16;
+    k_bwd_x<C, RADIAL><<<(int)(want < cap ? want : cap), K::NT, 0, st>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
+  }
+  if (want_wv && a.N > 0) {
+    // as many receiver groups as the static scratch holds partial rows for
+    const long long fit = (long long)(kNoAllocBytes / ((size_t)34 * C * 4)) / K::GROUPS;
+    long long grid = bwd_slots<C>(a.N, dev.sms) / K::GROUPS;
+    if (!RADIAL && grid > fit) grid = fit;
+    const int smem = RADIAL ? 0 : K::GROUPS * 34 * C * 4;
+    static unsigned long long attr_done = 0;
+    if (ensure_smem_attr(k_bwd_wv<C, RADIAL>, smem > 0 ? smem : 1, &attr_done) != cudaSuccess)
+      return EQMP_ERR_CUDA;
+    k_bwd_wv<C, RADIAL><<<(int)grid, K::NT, smem, st>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
+    if (!RADIAL && gw) {
+      k_bwd_reduce_w<C><<<(34 * C + 127) / 128, 128, 0, st>>>(a.ws, (int)grid * K::GROUPS, gw);
+      if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
+    }
+    if (RADIAL && gM) {
+      k_bwd_reduce_M<C><<<(8 * 34 * C + 127) / 128, 128, 0, st>>>(a.R, a.ws, e0, e1, gM);
+      if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
+    }
+  }
+  return EQMP_OK;
+}
+
+template <bool RADIAL>
+static eqmp_status dispatch_bwd_noalloc(int C, const BwdArgs& a, bool want_x, bool want_wv, float* gw, float* gM,
+                                        int e0, int e1, cudaStream_t st, const DeviceInfo& dev) {
+  switch (C) {
+    case 8: return run_bwd_noalloc<8, RADIAL>(a, want_x, want_wv, gw, gM, e0, e1, st, dev);
+    case 16: return run_bwd_noalloc<16, RADIAL>(a, want_x, want_wv, gw, gM, e0, e1, st, dev);
+    case 32: return run_bwd_noalloc<32, RADIAL>(a, want_x, want_wv, gw, gM, e0, e1, st, dev);
+    case 64: return run_bwd_noalloc<64, RADIAL>(a, want_x, want_wv, gw, gM, e0, e1, st, dev);
+    case 128: return run_bwd_noalloc<128, RADIAL>(a, want_x, want_wv, gw, gM, e0, e1, st, dev);
+  }
+  return EQMP_ERR_UNSUPPORTED;
+}
+
+}  // namespace eqmp
+
+extern "C" {
+
+int64_t eqmp_fused_backward_noalloc_max_bytes(void) { return (int64_t)eqmp::kNoAllocBytes; }
+
+eqmp_status eqmp_fused_backward_noalloc(const float* vec, const float* x, int64_t N_src,
+                                        const int32_t* row_offsets, const int32_t* src, const int32_t* dst,
+                                        const int32_t* send_offsets, const int32_t* send_edges, int64_t E_send,
+                                        int64_t N, int64_t E, int32_t C, eqmp_weights weights,
+                                        const float* grad_out, float* grad_x, float* grad_w, float* grad_R,
+                                        float* grad_M, float* grad_vec, eqmp_stream_t stream) {
+  if (N < 0 || E < 0 || N_src < 0 || E_send < 0) return EQMP_ERR_INVALID_ARG;
+  if (N > INT32_MAX - 1 || E > INT32_MAX || N_src > INT32_MAX - 1 || E_send > INT32_MAX)
+    return EQMP_ERR_INVALID_ARG;
+  if (C != 8 && C != 16 && C != 32 && C != 64 && C != 128) return EQMP_ERR_UNSUPPORTED;
+  const bool radial = weights.w == nullptr;
+  if (!radial && (weights.R || weights.M || weights.K != 0)) return EQMP_ERR_INVALID_ARG;
+  if (radial && weights.K != 8) return EQMP_ERR_UNSUPPORTED;
+  if (radial && E > 0 && (!weights.R || !weights.M)) return EQMP_ERR_INVALID_ARG;
+  if (!radial && (grad_R || grad_M)) return EQMP_ERR_INVALID_ARG;
+  if (radial && grad_w) return EQMP_ERR_INVALID_ARG;
+  const bool want_x = grad_x != nullptr;
+  const bool want_wv = grad_vec || grad_w || grad_R || grad_M;
+  if (want_x && (!send_offsets || (E_send > 0 && (!send_edges || !dst)) || !aligned16(grad_x)))
+    return EQMP_ERR_INVALID_ARG;
+  if ((want_x || want_wv) && N > 0 && (!row_offsets || !grad_out || !aligned16(grad_out)))
+    return EQMP_ERR_INVALID_ARG;
+  if (E > 0 && (want_x || want_wv) && (!vec || !src || !x || !aligned16(x) || N_src < 1))
+    return EQMP_ERR_INVALID_ARG;
+  if (radial && E > 0 && (!aligned16(weights.R) || (grad_R && !aligned16(grad_R)))) return EQMP_ERR_INVALID_ARG;
+  // Radial weights keep one scratch row of 34*C floats per edge: beyond the
+  // static array this entry point cannot run (use eqmp_fused_backward).
+  if (radial && want_wv && (size_t)E * 34 * (size_t)C * 4 > kNoAllocBytes) return EQMP_ERR_UNSUPPORTED;
+  DeviceInfo dev;
+  eqmp_status s = device_info(&dev);
+  if (s != EQMP_OK) return s;
+  float* scratch = nullptr;
+  s = noalloc_scratch(&scratch);
+  if (s != EQMP_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int e0 = 0, e1 = 0;
+  if (radial && grad_M && N > 0) {
+    int h[2] = {0, 0};
+    if (cudaMemcpyAsync(&h[0], row_offsets, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaMemcpyAsync(&h[1], row_offsets + N, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+      return EQMP_ERR_CUDA;
+    e0 = h[0] < 0 ? 0 : (h[0] > E ? (int)E : h[0]);
+    e1 = h[1] < e0 ? e0 : (h[1] > E ? (int)E : h[1]);
+  }
+  BwdArgs a{};
+  a.vec = vec; a.x = x; a.off = row_offsets; a.src = src; a.dst = dst;
+  a.send_off = send_offsets; a.send_edges = send_edges;
+  a.w = weights.w; a.R = weights.R; a.M = weights.M; a.g = grad_out;
+  a.gx = grad_x; a.gvec = grad_vec; a.gR = grad_R; a.ws = scratch;
+  a.N = (int)N; a.E = (int)E; a.N_src = (int)N_src; a.n_send = (int)E_send;
+  if (radial && grad_M && e1 == e0) {
+    if (cudaMemsetAsync(grad_M, 0, (size_t)8 * 34 * C * 4, st) != cudaSuccess) return EQMP_ERR_CUDA;
+    grad_M = nullptr;
+  }
+  if (!radial && grad_w && N == 0) {
+    if (cudaMemsetAsync(grad_w, 0, (size_t)34 * C * 4, st) != cudaSuccess) return EQMP_ERR_CUDA;
+  }
+  return radial ? dispatch_bwd_noalloc<true>(C, a, want_x, want_wv, nullptr, grad_M, e0, e1, st, dev)
+                : dispatch_bwd_noalloc<false>(C, a, want_x, want_wv, grad_w, nullptr, 0, 0, st, dev);
 }
 
 }  // extern "C"

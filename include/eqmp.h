@@ -167,6 +167,37 @@ eqmp_status eqmp_fused_backward(const float* vec, const float* x, int64_t N_src,
                                 eqmp_stream_t stream);
 
 /*
+ * eqmp_fused_backward without a workspace argument: for callers that cannot
+ * give the library extra device memory, such as a plugin inside a framework
+ * that owns the whole device memory pool, or a simulation loop that must not
+ * allocate on every step.  (The pages have no counterpart; this is a
+ * deployment variant of eqmp_fused_backward.)  Arguments and results are
+ * those of eqmp_fused_backward minus workspace/workspace_bytes.
+ *   - It allocates nothing.  Its scratch is one static device array of
+ *     eqmp_fused_backward_noalloc_max_bytes() bytes (8 MiB), held by every
+ *     GPU that loads the library until the process exits.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, on the current device); make that first call before any
+ *     stream capture.
+ *   - Shared weights: any size (the weight-gradient reduction uses fewer,
+ *     larger partial blocks so its partials fit the array).  Radial weights:
+ *     E * 34 * C * 4 bytes must fit the array when grad_vec, grad_R or grad_M
+ *     is requested, else EQMP_ERR_UNSUPPORTED (use eqmp_fused_backward).
+ *   - All calls share the array, which keeps the previous call's contents;
+ *     every part a call reads is written first by that call.  Calls that
+ *     overlap on the GPU (other streams or threads) race on the array.
+ */
+int64_t eqmp_fused_backward_noalloc_max_bytes(void);
+
+eqmp_status eqmp_fused_backward_noalloc(const float* vec, const float* x, int64_t N_src,
+                                        const int32_t* row_offsets, const int32_t* src, const int32_t* dst,
+                                        const int32_t* send_offsets, const int32_t* send_edges,
+                                        int64_t E_send, int64_t N, int64_t E, int32_t C,
+                                        eqmp_weights weights, const float* grad_out, float* grad_x,
+                                        float* grad_w, float* grad_R, float* grad_M, float* grad_vec,
+                                        eqmp_stream_t stream);
+
+/*
  * Synchronous check of the graph preconditions on device data:
  * 0 <= row_offsets[0] <= ... <= row_offsets[N] <= E and
  * 0 <= src[e] < N_src for every e in [row_offsets[0], row_offsets[N]).

@@ -11,6 +11,7 @@ Entry points (same names as the C ABI):
   eqmp_sh(vec, Y=None)                         -> Y [E, 16]
   eqmp_tp_scatter(Y, x, row_offsets, src, ...)  -> out [N, C, 16]
   eqmp_fused(vec, x, row_offsets, src, ...)     -> out [N, C, 16]
+  eqmp_fused_so2(...)                           -> out, aligned-frame schedule
   eqmp_validate_graph(row_offsets, src, n_src, n_edges)
   eqmp_device_error()                           -> int (watchdog code)
   eqmp_fused_backward(vec, x, row_offsets, src, dst, send_offsets, send_edges, grad_out, ...)
@@ -22,7 +23,7 @@ import os
 
 __all__ = [
     "EqmpError", "load_library", "library_path", "eqmp_num_paths", "eqmp_path_table",
-    "eqmp_status_string", "eqmp_sh", "eqmp_tp_scatter", "eqmp_fused", "eqmp_validate_graph",
+    "eqmp_status_string", "eqmp_sh", "eqmp_tp_scatter", "eqmp_fused", "eqmp_fused_so2", "eqmp_validate_graph",
     "eqmp_device_error", "eqmp_fused_backward", "sender_view", "EQMP_OK", "EQMP_ERR_INVALID_ARG", "EQMP_ERR_UNSUPPORTED",
     "EQMP_ERR_CUDA", "EQMP_ERR_DEVICE_TIMEOUT", "EQMP_ERR_GRAPH",
 ]
@@ -73,6 +74,8 @@ def load_library():
     lib.eqmp_tp_scatter.restype = i32
     lib.eqmp_fused.argtypes = layer
     lib.eqmp_fused.restype = i32
+    lib.eqmp_fused_so2.argtypes = layer
+    lib.eqmp_fused_so2.restype = i32
     lib.eqmp_validate_graph.argtypes = [vp, vp, i64, i64, i64, vp]
     lib.eqmp_validate_graph.restype = i32
     lib.eqmp_device_error.argtypes = [ctypes.POINTER(i32)]
@@ -204,6 +207,15 @@ def eqmp_fused(vec, x, row_offsets, src, w=None, R=None, M=None, out=None, strea
 
     _require(vec, "vec", torch.float32)
     return _layer("eqmp_fused", vec, x, row_offsets, src, w, R, M, out, stream, n_edges)
+
+
+def eqmp_fused_so2(vec, x, row_offsets, src, w=None, R=None, M=None, out=None, stream=None,
+                   n_edges=None):
+    """eqmp_fused computed in the aligned (SO(2)) edge frame; same result."""
+    import torch
+
+    _require(vec, "vec", torch.float32)
+    return _layer("eqmp_fused_so2", vec, x, row_offsets, src, w, R, M, out, stream, n_edges)
 
 
 def eqmp_validate_graph(row_offsets, src, n_src, n_edges, stream=None):

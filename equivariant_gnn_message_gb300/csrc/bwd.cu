@@ -46,11 +46,11 @@ static eqmp_status run_bwd(const BwdArgs& a, bool want_x, bool want_wv, float* g
     k_bwd_wv<C, RADIAL><<<grid, K::NT, smem, st>>>(a);
     if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
     if (!RADIAL && gw) {
-      k_bwd_reduce_w<C><<<(34 * C + 127) / 128, 128, 0, st>>>(a.ws, grid * K::GROUPS, gw);
+      k_bwd_reduce_w<<<(34 * C + kRedX - 1) / kRedX, dim3(kRedX, kRedY), 0, st>>>(a.ws, grid * K::GROUPS, 34 * C, gw);
       if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
     }
     if (RADIAL && gM) {
-      k_bwd_reduce_M<C><<<(8 * 34 * C + 127) / 128, 128, 0, st>>>(a.R, a.ws, e0, e1, gM);
+      k_bwd_reduce_M<<<dim3((34 * C + kRedX - 1) / kRedX, 8), dim3(kRedX, kRedY), 0, st>>>(a.R, a.ws, e0, e1, 34 * C, gM);
       if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
     }
   }
@@ -205,11 +205,11 @@ static eqmp_status run_bwd_noalloc(const BwdArgs& a, bool want_x, bool want_wv, 
     k_bwd_wv<C, RADIAL><<<(int)grid, K::NT, smem, st>>>(a);
     if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
     if (!RADIAL && gw) {
-      k_bwd_reduce_w<C><<<(34 * C + 127) / 128, 128, 0, st>>>(a.ws, (int)grid * K::GROUPS, gw);
+      k_bwd_reduce_w<<<(34 * C + kRedX - 1) / kRedX, dim3(kRedX, kRedY), 0, st>>>(a.ws, (int)grid * K::GROUPS, 34 * C, gw);
       if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
     }
     if (RADIAL && gM) {
-      k_bwd_reduce_M<C><<<(8 * 34 * C + 127) / 128, 128, 0, st>>>(a.R, a.ws, e0, e1, gM);
+      k_bwd_reduce_M<<<dim3((34 * C + kRedX - 1) / kRedX, 8), dim3(kRedX, kRedY), 0, st>>>(a.R, a.ws, e0, e1, 34 * C, gM);
       if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
     }
   }

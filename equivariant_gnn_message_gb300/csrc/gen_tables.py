@@ -176,6 +176,27 @@ def render():
             row.append("{" + ", ".join(_f(v) for v in c) + "}")
         lines.append("  {" + ", ".join(row) + "},")
     lines.append("};")
+    # aligned-frame (SO(2)) tables
+    at = aligned_terms()
+    lines.append("// aligned frame: m'[k3] += W_p * kappa * x'[k1]  (E2Former-V2 Eq. 13 form)")
+    lines.append("struct AlignedTerm { int p, k3, k1; float kappa; };")
+    lines.append(f"constexpr int kNumAligned = {len(at)};")
+    lines.append("constexpr AlignedTerm kAligned[kNumAligned] = {")
+    for (pp, k3, k1, kap) in at:
+        lines.append(f"  {{{pp}, {k3}, {k1}, {_f(kap)}}},")
+    lines.append("};")
+    ir = ir_coefficients()
+    for nm, idx in (("kIrU", 0), ("kIrV", 1), ("kIrW", 2)):
+        lines.append(f"constexpr float {nm}[2][7][7] = {{  // [l-2][m+3][n+3] (zero outside |m|,|n| <= l)")
+        for l in (2, 3):
+            rows = []
+            for m in range(-3, 4):
+                vals = []
+                for n in range(-3, 4):
+                    vals.append(_f(ir[l][m + l][n + l][idx]) if abs(m) <= l and abs(n) <= l else "0.0f")
+                rows.append("{" + ", ".join(vals) + "}")
+            lines.append("  {" + ", ".join(rows) + "},")
+        lines.append("};")
     lines.append("}}  // namespace eqmp::tables")
     return "\n".join(lines) + "\n", paths, terms
 
@@ -187,6 +208,119 @@ def main(argv):
             fh.write(text)
     else:
         sys.stdout.write(text)
+
+
+
+# ---------------------------------------------------------------------------
+# Aligned-frame (SO(2)) form of the same tensor product, E2Former-V2 section
+# 2.1 (EAAS): rotate x into a frame whose z axis is the edge, where the edge
+# harmonics keep only m = 0 (Lemma 4.1) and each output m3 takes at most one
+# input m1 (Eq. 13); rotate the result back.  Everything below is computed
+# here independently and emitted as constexpr tables.
+
+def aligned_terms():
+    """[(p, k3, k1, kappa)]: m'[k3] += W_p kappa x'[k1] in the edge frame.
+
+    kappa = C_p[m3, m1, m2=0] * Y_l2,0(z-axis), Y_l,0(z) = sqrt((2l+1)/(4 pi)).
+    """
+    out = []
+    for p, (l1, l2, l3) in enumerate(all_paths()):
+        ent = real_cg(l1, l2, l3)
+        yz = sqrt((2 * l2 + 1) / (4 * pi))
+        for (m3, m1, m2), v in sorted(ent.items()):
+            if m2 == 0:
+                out.append((p, k_of(l3, m3), k_of(l1, m1), v * yz))
+    return out
+
+
+def frame_from_direction(n):
+    """Right-handed orthonormal (t1, t2, n) with n the unit edge direction
+    (branch-free construction of an orthonormal basis from one vector,
+    Duff et al. 2017).  Returns the 3x3 rotation Q with columns t1, t2, n."""
+    x, y, z = n
+    s = 1.0 if z >= 0.0 else -1.0
+    a = -1.0 / (s + z)
+    b = x * y * a
+    t1 = (1.0 + s * x * x * a, s * b, -s * x)
+    t2 = (b, s + y * y * a, -y)
+    return [[t1[0], t2[0], x], [t1[1], t2[1], y], [t1[2], t2[2], z]]
+
+
+def ir_coefficients():
+    """Ivanic-Ruedenberg recursion coefficients u, v, w for l = 2, 3:
+    {l: [[(u, v, w) for n in -l..l] for m in -l..l]}."""
+    out = {}
+    for l in (2, 3):
+        rows = []
+        for m in range(-l, l + 1):
+            row = []
+            for n in range(-l, l + 1):
+                d = 1 if m == 0 else 0
+                den = (2 * l) * (2 * l - 1) if abs(n) == l else (l + n) * (l - n)
+                u = sqrt((l + m) * (l - m) / den)
+                v = 0.5 * sqrt((1 + d) * (l + abs(m) - 1) * (l + abs(m)) / den) * (1 - 2 * d)
+                w = -0.5 * sqrt((l - abs(m) - 1) * (l - abs(m)) / den) * (1 - d)
+                row.append((u, v, w))
+            rows.append(row)
+        out[l] = rows
+    return out
+
+
+def wigner_real(Q):
+    """Real Wigner-D blocks D_1..D_3 in this library's SH basis (CS phase,
+    k = l*l+l+m) for rotation Q: Y_l(Q v) = D_l Y_l(v).  Plain Python
+    reference of the device recursion."""
+    # l = 1 in the (y, z, x) ordering without signs
+    idx = [1, 2, 0]
+    R = [[Q[idx[i]][idx[j]] for j in range(3)] for i in range(3)]
+    D = {1: R}
+    coef = ir_coefficients()
+
+    def Rm(i, j):
+        return R[i + 1][j + 1]
+
+    def Dl(l, a, b):
+        return D[l][a + l][b + l]
+
+    def P(i, l, a, b):
+        if b == l:
+            return Rm(i, 1) * Dl(l - 1, a, l - 1) - Rm(i, -1) * Dl(l - 1, a, -l + 1)
+        if b == -l:
+            return Rm(i, 1) * Dl(l - 1, a, -l + 1) + Rm(i, -1) * Dl(l - 1, a, l - 1)
+        return Rm(i, 0) * Dl(l - 1, a, b)
+
+    for l in (2, 3):
+        M = []
+        for m in range(-l, l + 1):
+            row = []
+            for n in range(-l, l + 1):
+                u, v, w = coef[l][m + l][n + l]
+                val = 0.0
+                if u != 0.0:
+                    val += u * P(0, l, m, n)
+                if v != 0.0:
+                    if m == 0:
+                        V = P(1, l, 1, n) + P(-1, l, -1, n)
+                    elif m > 0:
+                        V = P(1, l, m - 1, n) * sqrt(1 + (m == 1)) - P(-1, l, -m + 1, n) * (1 - (m == 1))
+                    else:
+                        V = P(1, l, m + 1, n) * (1 - (m == -1)) + P(-1, l, -m - 1, n) * sqrt(1 + (m == -1))
+                    val += v * V
+                if w != 0.0:
+                    if m > 0:
+                        W = P(1, l, m + 1, n) + P(-1, l, -m - 1, n)
+                    else:
+                        W = P(1, l, m - 1, n) - P(-1, l, -m + 1, n)
+                    val += w * W
+                row.append(val)
+            M.append(row)
+        D[l] = M
+    # this library's basis carries the Condon-Shortley sign (-1)^|m| on m != 0
+    out = {}
+    for l in (1, 2, 3):
+        sg = [(-1) ** abs(m) if m != 0 else 1 for m in range(-l, l + 1)]
+        out[l] = [[sg[i] * D[l][i][j] * sg[j] for j in range(2 * l + 1)] for i in range(2 * l + 1)]
+    return out
 
 
 if __name__ == "__main__":

@@ -338,26 +338,47 @@ __global__ void __launch_bounds__(128) k_bwd_wv(const BwdArgs a) {
   }
 }
 
-// dL/dw[p, c] = sum over slots of the partials, in slot order.
-template <int C>
-__global__ void k_bwd_reduce_w(const float* ws, int slots, float* gw) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;  // i = p*C + c
-  if (i >= 34 * C) return;
-  const int p = i / C, c = i % C;
+// Column sums of a [rows][cols] fp32 matrix (optionally weighted by a
+// column of R), deterministic: block (32 columns x 16 row partitions); thread
+// (x, y) sums rows y, y+16, ... of column x in order, then the 16 partials
+// are added in partition order.
+constexpr int kRedX = 32, kRedY = 16;
+
+// dL/dw[i] = sum over slots k of ws[k][i], i = p*C + c (34*C columns).
+__global__ void __launch_bounds__(kRedX* kRedY) k_bwd_reduce_w(const float* ws, int slots, int cols, float* gw) {
+  __shared__ float part[kRedY][kRedX];
+  const int col = blockIdx.x * kRedX + threadIdx.x;
   float s = 0.0f;
-  for (int k = 0; k < slots; ++k) s += ws[((size_t)k * 34 + p) * C + c];
-  gw[i] = s;
+  if (col < cols)
+    for (int k = threadIdx.y; k < slots; k += kRedY) s += ws[(size_t)k * cols + col];
+  part[threadIdx.y][threadIdx.x] = s;
+  __syncthreads();
+  if (threadIdx.y == 0 && col < cols) {
+    float t = 0.0f;
+#pragma unroll
+    for (int y = 0; y < kRedY; ++y) t += part[y][threadIdx.x];
+    gw[col] = t;
+  }
 }
 
-// dL/dM[k, col] = sum_e R[e, k] s[e, col], in edge order.
-template <int C>
-__global__ void k_bwd_reduce_M(const float* R, const float* S, int e0, int e1, float* gM) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;  // i = k*34C + col
-  if (i >= 8 * 34 * C) return;
-  const int k = i / (34 * C), col = i % (34 * C);
+// dL/dM[k][col] = sum over edges e in [e0, e1) of R[e][k] S[e][col].
+__global__ void __launch_bounds__(kRedX* kRedY) k_bwd_reduce_M(const float* R, const float* S, int e0, int e1,
+                                                              int cols, float* gM) {
+  __shared__ float part[kRedY][kRedX];
+  const int k = blockIdx.y;
+  const int col = blockIdx.x * kRedX + threadIdx.x;
   float s = 0.0f;
-  for (int e = e0; e < e1; ++e) s = fmaf(__ldg(R + (size_t)e * 8 + k), __ldg(S + (size_t)e * 34 * C + col), s);
-  gM[i] = s;
+  if (col < cols)
+    for (int e = e0 + threadIdx.y; e < e1; e += kRedY)
+      s = fmaf(__ldg(R + (size_t)e * 8 + k), __ldg(S + (size_t)e * cols + col), s);
+  part[threadIdx.y][threadIdx.x] = s;
+  __syncthreads();
+  if (threadIdx.y == 0 && col < cols) {
+    float t = 0.0f;
+#pragma unroll
+    for (int y = 0; y < kRedY; ++y) t += part[y][threadIdx.x];
+    gM[(size_t)k * cols + col] = t;
+  }
 }
 
 }  // namespace eqmp

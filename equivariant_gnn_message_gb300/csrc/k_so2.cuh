@@ -1,0 +1,408 @@
+// Fused layer in the aligned (SO(2)) frame, E2Former-V2 section 2.1 (EAAS).
+//
+// Same result as k_shared / k_radial (the dense CG product), computed per
+// edge in a frame whose z axis is the edge:
+//   x'_l = D_l^T x_l                      (Wigner-D of the frame rotation Q, Q z = n)
+//   m'[k3] = sum_p W_p kappa_p x'[k1]     (only m2 = 0 survives, Lemma 4.1; one m1
+//                                          per output m3, Eq. 13: 111 terms)
+//   out_l += D_l m'_l                     (back to the global frame, summed per receiver)
+// About 2.5x fewer FMAs per edge and channel than the dense product, which
+// pays off where the weights change per edge (radial weights).
+//
+// CTA: one producer warp + NCONS = 128 consumer threads split into EG = 128/C
+// edge groups of C threads (thread = channel); group g takes the edges whose
+// CTA ordinal is g mod EG.  Producer, per 32 edges lane-parallel: frame Q
+// (branch-free orthonormal basis), D_1..D_3 by the Ivanic-Ruedenberg
+// recursion (coefficients generated at build time), the 8 radial features,
+// into a 64-entry edge ring; then one TMA row copy of x[src] per edge into an
+// S-slot ring (128-byte swizzle), as in k_shared.  Receiver partials of the
+// groups are summed through shared memory in group order (deterministic).
+#pragma once
+
+#include <cuda.h>
+
+#include "common.cuh"
+#include "k_shared.cuh"
+#include "layer_args.cuh"
+
+namespace eqmp {
+
+constexpr float ir_u(int l, int m, int n) { return tables::kIrU[l - 2][m + 3][n + 3]; }
+constexpr float ir_v(int l, int m, int n) { return tables::kIrV[l - 2][m + 3][n + 3]; }
+constexpr float ir_w(int l, int m, int n) { return tables::kIrW[l - 2][m + 3][n + 3]; }
+constexpr tables::AlignedTerm aligned_at(int i) { return tables::kAligned[i]; }
+
+// Edge ring entry (floats): D_1 (9) at 0, D_2 (25) at 9, D_3 (49) at 34,
+// radial features (8) at 84, zero-length flag at 92; 96 floats.
+constexpr int kEntryFloats = 96;
+constexpr int kD1 = 0, kD2 = 9, kD3 = 34, kRad = 84, kFlag = 92;
+
+// ---- Ivanic-Ruedenberg recursion (real SH without CS sign, (y,z,x) order) ---
+// R[i+1][j+1], i,j in {-1,0,1}; Dp: level L-1, (2L-1)^2 row-major.
+template <int L, int I, int A, int B>
+__device__ __forceinline__ float ir_P(const float (&R)[3][3], const float* Dp) {
+  constexpr int W = 2 * L - 1;
+  auto dp = [&](int a, int b) { return Dp[(a + L - 1) * W + (b + L - 1)]; };
+  if constexpr (B == L) {
+    return R[I + 1][2] * dp(A, L - 1) - R[I + 1][0] * dp(A, -L + 1);
+  } else if constexpr (B == -L) {
+    return R[I + 1][2] * dp(A, -L + 1) + R[I + 1][0] * dp(A, L - 1);
+  } else {
+    return R[I + 1][1] * dp(A, B);
+  }
+}
+
+template <int L, int M, int N>
+__device__ __forceinline__ float ir_entry(const float (&R)[3][3], const float* Dp) {
+  constexpr float u = ir_u(L, M, N), v = ir_v(L, M, N), w = ir_w(L, M, N);
+  float val = 0.0f;
+  if constexpr (u != 0.0f) val = u * ir_P<L, 0, M, N>(R, Dp);
+  if constexpr (v != 0.0f) {
+    float V;
+    if constexpr (M == 0) {
+      V = ir_P<L, 1, 1, N>(R, Dp) + ir_P<L, -1, -1, N>(R, Dp);
+    } else if constexpr (M > 0) {
+      constexpr float f1 = M == 1 ? 1.41421356237309515f : 1.0f;
+      constexpr float f2 = M == 1 ? 0.0f : 1.0f;
+      V = ir_P<L, 1, M - 1, N>(R, Dp) * f1;
+      if constexpr (f2 != 0.0f) V -= ir_P<L, -1, -M + 1, N>(R, Dp);
+    } else {
+      constexpr float f1 = M == -1 ? 0.0f : 1.0f;
+      constexpr float f2 = M == -1 ? 1.41421356237309515f : 1.0f;
+      V = ir_P<L, -1, -M - 1, N>(R, Dp) * f2;
+      if constexpr (f1 != 0.0f) V += ir_P<L, 1, M + 1, N>(R, Dp);
+    }
+    val = fmaf(v, V, val);
+  }
+  if constexpr (w != 0.0f) {
+    float Wt;
+    if constexpr (M > 0) {
+      Wt = ir_P<L, 1, M + 1, N>(R, Dp) + ir_P<L, -1, -M - 1, N>(R, Dp);
+    } else {
+      Wt = ir_P<L, 1, M - 1, N>(R, Dp) - ir_P<L, -1, -M + 1, N>(R, Dp);
+    }
+    val = fmaf(w, Wt, val);
+  }
+  return val;
+}
+
+template <int L, int... Is>
+__device__ __forceinline__ void ir_level(const float (&R)[3][3], const float* Dp, float* Dl,
+                                         std::integer_sequence<int, Is...>) {
+  constexpr int W = 2 * L + 1;
+  ((Dl[Is] = ir_entry<L, Is / W - L, Is % W - L>(R, Dp)), ...);
+}
+
+constexpr float cs_sign(int m) { return (m != 0 && (m & 1)) ? -1.0f : 1.0f; }
+
+// This library's basis: D[i][j] = s_i s_j D_IR[i][j], s = (-1)^|m|.
+template <int L, int... Is>
+__device__ __forceinline__ void store_block(const float* Dir, float* out, std::integer_sequence<int, Is...>) {
+  constexpr int W = 2 * L + 1;
+  ((out[Is] = cs_sign(Is / W - L) * cs_sign(Is % W - L) * Dir[Is]), ...);
+}
+
+// Frame and D_1..D_3 for unit direction (x, y, z) into entry e (83 floats).
+__device__ __forceinline__ void wigner_blocks(float x, float y, float z, float* e) {
+  const float s = z >= 0.0f ? 1.0f : -1.0f;
+  const float a = -1.0f / (s + z);
+  const float b = x * y * a;
+  // Q columns: t1, t2, n
+  const float Q[3][3] = {{fmaf(s * x * x, a, 1.0f), b, x},
+                         {s * b, fmaf(y * y, a, s), y},
+                         {-s * x, -y, z}};
+  // (y, z, x) ordering
+  const float R[3][3] = {{Q[1][1], Q[1][2], Q[1][0]},
+                         {Q[2][1], Q[2][2], Q[2][0]},
+                         {Q[0][1], Q[0][2], Q[0][0]}};
+  float D2[25], D3[49];
+  ir_level<2>(R, &R[0][0], D2, std::make_integer_sequence<int, 25>{});
+  ir_level<3>(R, D2, D3, std::make_integer_sequence<int, 49>{});
+  store_block<1>(&R[0][0], e + kD1, std::make_integer_sequence<int, 9>{});
+  store_block<2>(D2, e + kD2, std::make_integer_sequence<int, 25>{});
+  store_block<3>(D3, e + kD3, std::make_integer_sequence<int, 49>{});
+}
+
+template <int C, typename XT, bool RADIAL>
+struct So2Cfg {
+  static constexpr int NCONS = 128;
+  static constexpr int EG = NCONS / C;                 // edge groups
+  static constexpr int NTHREADS = NCONS + 32;
+  static constexpr int ROW_BYTES = C * 16 * (int)sizeof(XT);
+  static constexpr int ROWS = ROW_BYTES / 128;
+  static constexpr int SLOT = ROW_BYTES < 1024 ? 1024 : ROW_BYTES;
+  static constexpr int YR = 64;
+  static constexpr int M_BYTES = RADIAL ? 8 * 34 * C * 4 : 0;
+  static constexpr int FIXED = YR * kEntryFloats * 4 + 2 * EG * 16 * C * 4 + M_BYTES + 2 * 16 * 8 + 2048;
+  static constexpr int S_FIT = (227 * 1024 - FIXED) / SLOT;
+  static constexpr int S = S_FIT >= 16 ? 16 : S_FIT >= 8 ? 8 : S_FIT >= 4 ? 4 : 2;
+  static_assert(S % EG == 0 && S <= 32 && YR >= 32 + S && S_FIT >= 2, "ring layout");
+  static constexpr int OFF_X = 0;
+  static constexpr int OFF_E = OFF_X + S * SLOT;                       // edge ring
+  static constexpr int OFF_RED = OFF_E + YR * kEntryFloats * 4;         // [2][EG][16][C]
+  static constexpr int OFF_M = OFF_RED + 2 * EG * 16 * C * 4;          // radial: [8][17][C] float2
+  static constexpr int OFF_BAR = OFF_M + M_BYTES;
+  static constexpr int SMEM_BYTES = OFF_BAR + 2 * S * 8 + 1024;
+};
+
+template <int P, int C, bool RADIAL>
+__device__ __forceinline__ void so2_weight_pair(const float2* Ms, int c, const float2 (&rr)[8], float (&W)[34]) {
+  // paths P, P+1 of channel c:  (W_P, W_P+1) = sum_k R_k (M[k][P][c], M[k][P+1][c])
+  float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) acc = __ffma2_rn(rr[k], Ms[(k * 17 + P / 2) * C + c], acc);
+  W[P] = acc.x;
+  W[P + 1] = acc.y;
+}
+
+template <int C, bool RADIAL, int... Ps>
+__device__ __forceinline__ void so2_weights(const float2* Ms, int c, const float2 (&rr)[8], float (&W)[34],
+                                            std::integer_sequence<int, Ps...>) {
+  (so2_weight_pair<2 * Ps, C, RADIAL>(Ms, c, rr, W), ...);
+}
+
+template <int I>
+__device__ __forceinline__ void so2_term(const float (&W)[34], const float (&xr)[16], float (&mp)[16]) {
+  constexpr tables::AlignedTerm t = aligned_at(I);
+  mp[t.k3] = fmaf(W[t.p], t.kappa * xr[t.k1], mp[t.k3]);
+}
+template <int... Is>
+__device__ __forceinline__ void so2_terms(const float (&W)[34], const float (&xr)[16], float (&mp)[16],
+                                          std::integer_sequence<int, Is...>) {
+  (so2_term<Is>(W, xr, mp), ...);
+}
+
+// x'_l[n] = sum_m D[m][n] x_l[m]
+template <int L>
+__device__ __forceinline__ void rotate_in(const float* D, const float (&x)[16], float (&xr)[16]) {
+  constexpr int W = 2 * L + 1, o = L * L;
+#pragma unroll
+  for (int n = 0; n < W; ++n) {
+    float s = 0.0f;
+#pragma unroll
+    for (int m = 0; m < W; ++m) s = fmaf(D[m * W + n], x[o + m], s);
+    xr[o + n] = s;
+  }
+}
+// out_l[m] += sum_n D[m][n] m'_l[n]
+template <int L>
+__device__ __forceinline__ void rotate_out(const float* D, const float (&mp)[16], float (&out)[16]) {
+  constexpr int W = 2 * L + 1, o = L * L;
+#pragma unroll
+  for (int m = 0; m < W; ++m) {
+    float s = out[o + m];
+#pragma unroll
+    for (int n = 0; n < W; ++n) s = fmaf(D[m * W + n], mp[o + n], s);
+    out[o + m] = s;
+  }
+}
+
+template <int C, typename XT, bool RADIAL>
+__global__ void __launch_bounds__(So2Cfg<C, XT, RADIAL>::NTHREADS, 1)
+    k_so2(const __grid_constant__ CUtensorMap tmap, const LayerArgs a) {
+  using K = So2Cfg<C, XT, RADIAL>;
+  constexpr int S = K::S;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* ering = reinterpret_cast<float*>(smem + K::OFF_E);
+  float* red = reinterpret_cast<float*>(smem + K::OFF_RED);
+  float2* Ms = reinterpret_cast<float2*>(smem + K::OFF_M);
+  const uint32_t full0 = smem_u32(smem + K::OFF_BAR);
+  const uint32_t empty0 = full0 + 8 * S;
+  const int tid = threadIdx.x;
+  const int G = gridDim.x, b = blockIdx.x;
+  const int r_begin = (int)((long long)a.N * b / G);
+  const int r_end = (int)((long long)a.N * (b + 1) / G);
+  if (tid < S) {
+    mbar_init(full0 + 8 * tid, 1);
+    mbar_init(empty0 + 8 * tid, C);  // the C threads of the owning edge group
+    fence_mbar_init();
+  }
+  if constexpr (RADIAL) {
+    // M[k][p*C + c] -> Ms[(k*17 + p/2)*C + c] = (M[k][p][c], M[k][p+1][c])
+    for (int i = tid; i < 8 * 17 * C; i += K::NTHREADS) {
+      const int k = i / (17 * C), pp = (i / C) % 17, c = i % C;
+      Ms[i] = make_float2(__ldg(a.M + (size_t)k * 34 * C + (2 * pp) * C + c),
+                          __ldg(a.M + (size_t)k * 34 * C + (2 * pp + 1) * C + c));
+    }
+  }
+  __syncthreads();
+  const int e_begin = min(max(__ldg(a.off + r_begin), 0), a.E);
+  const int e_end = max(e_begin, min(max(__ldg(a.off + r_end), 0), a.E));
+  const int total = e_end - e_begin;
+
+  if (tid >= K::NCONS) {
+    // ------------------------------------------------------------ producer
+    const int lane = tid & 31;
+    if (lane == 0) prefetch_tmap(&tmap);
+    bool ok = true;
+    for (int base = 0; base < total && ok; base += 32) {
+      const uint32_t n = (uint32_t)(base + lane);
+      int node = 0;
+      if (n < (uint32_t)total) {
+        const int e = e_begin + (int)n;
+        node = __ldg(a.src + e);
+        const float* v = a.vec + 3 * (size_t)e;
+        const float vx = __ldg(v), vy = __ldg(v + 1), vz = __ldg(v + 2);
+        float* ent = ering + (size_t)(n % K::YR) * kEntryFloats;
+        const float r2 = fmaf(vx, vx, fmaf(vy, vy, vz * vz));
+        if (r2 >= 1e-30f) {
+          const float inv = rsqrtf(r2);
+          wigner_blocks(vx * inv, vy * inv, vz * inv, ent);
+          ent[kFlag] = 0.0f;
+        } else {
+          ent[kFlag] = 1.0f;  // zero-length edge: only the l2 = 0 paths contribute
+        }
+        if constexpr (RADIAL) {
+          const float4* rp = reinterpret_cast<const float4*>(a.R) + 2 * (size_t)e;
+          reinterpret_cast<float4*>(ent + kRad)[0] = __ldg(rp);
+          reinterpret_cast<float4*>(ent + kRad)[1] = __ldg(rp + 1);
+        }
+      }
+      const int cnt = min(32, total - base);
+      for (int j = 0; j < cnt; ++j) {
+        int good = 1;
+        if (lane == j) {
+          const uint32_t s = n % S, par = ((n / S) & 1u) ^ 1u;
+          if (mbar_try_wait(empty0 + 8 * s, par) || mbar_wait(empty0 + 8 * s, par, a.watchdog, 2)) {
+            mbar_arrive_expect_tx(full0 + 8 * s, K::ROW_BYTES);
+            tma_load_2d(smem_u32(smem + K::OFF_X + s * K::SLOT), &tmap, 0, node * K::ROWS, full0 + 8 * s);
+          } else {
+            good = 0;
+          }
+        }
+        if (!__all_sync(0xffffffffu, good)) { ok = false; break; }
+      }
+    }
+    // Drain: the last min(S, total) loads have landed before this warp leaves.
+    if (lane == 0 && ok) {
+      const uint32_t last = (uint32_t)total;
+      const uint32_t first = last > (uint32_t)S ? last - S : 0;
+      for (uint32_t i = first; i < last; ++i)
+        if (!mbar_wait(full0 + 8 * (i % S), (i / S) & 1u, a.watchdog, 3)) break;
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int c = tid % C, g = tid / C;
+  const uint32_t xlog = (uint32_t)(c * 16 * (int)sizeof(XT));
+  const uint32_t xo[2] = {swz128(xlog), swz128(xlog + 16)};
+  float Wsh[34];
+  if constexpr (!RADIAL) {
+#pragma unroll
+    for (int p = 0; p < 34; ++p) Wsh[p] = __ldg(a.w + p * C + c);
+  }
+  bool failed = false;
+  int buf = 0;
+  uint32_t n = 0;
+  for (int r = r_begin; r < r_end; ++r) {
+    const int a0 = min(max(__ldg(a.off + r), 0), a.E);
+    const int a1 = min(max(__ldg(a.off + r + 1), 0), a.E);
+    const int deg = min(max(a1 - a0, 0), total - (int)n);
+    float out[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) out[k] = 0.0f;
+    for (int j = 0; j < deg; ++j) {
+      const uint32_t m = n + j;
+      if ((int)(m % K::EG) != g) continue;
+      const uint32_t s = m % S, par = (m / S) & 1u;
+      if (!mbar_try_wait(full0 + 8 * s, par))
+        if (!mbar_wait_slow(full0 + 8 * s, par, a.watchdog, 1, failed)) failed = true;
+      const float* ent = ering + (size_t)(m % K::YR) * kEntryFloats;
+      float x[16];
+      {
+        const uint8_t* slot = smem + K::OFF_X + s * K::SLOT;
+        if constexpr (sizeof(XT) == 4) {
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const float4 v = *reinterpret_cast<const float4*>(slot + swz128(xlog + 16 * h));
+            x[4 * h] = v.x; x[4 * h + 1] = v.y; x[4 * h + 2] = v.z; x[4 * h + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint4 v = *reinterpret_cast<const uint4*>(slot + xo[h]);
+            x[8 * h + 0] = bf16_lo(v.x); x[8 * h + 1] = bf16_hi(v.x);
+            x[8 * h + 2] = bf16_lo(v.y); x[8 * h + 3] = bf16_hi(v.y);
+            x[8 * h + 4] = bf16_lo(v.z); x[8 * h + 5] = bf16_hi(v.z);
+            x[8 * h + 6] = bf16_lo(v.w); x[8 * h + 7] = bf16_hi(v.w);
+          }
+        }
+      }
+      float W[34];
+      if constexpr (RADIAL) {
+        float2 rr[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) rr[k] = make_float2(ent[kRad + k], ent[kRad + k]);
+        so2_weights<C, RADIAL>(Ms, c, rr, W, std::make_integer_sequence<int, 17>{});
+      } else {
+#pragma unroll
+        for (int p = 0; p < 34; ++p) W[p] = Wsh[p];
+      }
+      const bool zero_len = ent[kFlag] != 0.0f;
+      // every read of slot s and entry m is done once x, W and the flag are in registers
+      float D1[9], D2[25], D3[49];
+#pragma unroll
+      for (int i = 0; i < 9; ++i) D1[i] = ent[kD1 + i];
+#pragma unroll
+      for (int i = 0; i < 25; ++i) D2[i] = ent[kD2 + i];
+#pragma unroll
+      for (int i = 0; i < 49; ++i) D3[i] = ent[kD3 + i];
+      mbar_arrive(empty0 + 8 * s);
+      if (!zero_len) {
+        float xr[16], mp[16];
+        xr[0] = x[0];
+        rotate_in<1>(D1, x, xr);
+        rotate_in<2>(D2, x, xr);
+        rotate_in<3>(D3, x, xr);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) mp[k] = 0.0f;
+        so2_terms(W, xr, mp, std::make_integer_sequence<int, tables::kNumAligned>{});
+        out[0] += mp[0];
+        rotate_out<1>(D1, mp, out);
+        rotate_out<2>(D2, mp, out);
+        rotate_out<3>(D3, mp, out);
+      } else {
+        // n = 0: Y = (Y00, 0, ...): only the paths (l, 0, l), identity CG
+        constexpr float y00 = 0.28209479177387814f;
+        out[0] = fmaf(W[0] * y00, x[0], out[0]);
+#pragma unroll
+        for (int k = 1; k < 4; ++k) out[k] = fmaf(W[4] * y00, x[k], out[k]);
+#pragma unroll
+        for (int k = 4; k < 9; ++k) out[k] = fmaf(W[13] * y00, x[k], out[k]);
+#pragma unroll
+        for (int k = 9; k < 16; ++k) out[k] = fmaf(W[24] * y00, x[k], out[k]);
+      }
+    }
+    n += deg;
+    // group partials -> shared memory; thread (c, g) sums outputs k in its share
+    float* rb = red + buf * (K::EG * 16 * C);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) rb[(g * 16 + k) * C + c] = out[k];
+    named_barrier(1, K::NCONS);
+    constexpr int KPER = 16 / K::EG > 0 ? 16 / K::EG : 1;
+    if (g * KPER < 16) {
+      float o[16];
+#pragma unroll
+      for (int i = 0; i < KPER; ++i) {
+        float sum = 0.0f;
+#pragma unroll
+        for (int gg = 0; gg < K::EG; ++gg) sum += rb[(gg * 16 + g * KPER + i) * C + c];
+        o[i] = sum;
+      }
+      if constexpr (sizeof(XT) == 4) {
+        float* op = reinterpret_cast<float*>(a.out) + ((size_t)r * C + c) * 16 + g * KPER;
+#pragma unroll
+        for (int i = 0; i < KPER; ++i) op[i] = o[i];
+      } else {
+        __nv_bfloat16* op = reinterpret_cast<__nv_bfloat16*>(a.out) + ((size_t)r * C + c) * 16 + g * KPER;
+#pragma unroll
+        for (int i = 0; i < KPER; ++i) op[i] = __float2bfloat16_rn(o[i]);
+      }
+    }
+    buf ^= 1;
+  }
+}
+
+}  // namespace eqmp

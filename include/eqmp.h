@@ -198,6 +198,21 @@ eqmp_status eqmp_fused_backward_noalloc(const float* vec, const float* x, int64_
                                         eqmp_stream_t stream);
 
 /*
+ * The same layer as eqmp_fused, computed per edge in the aligned frame of
+ * E2Former-V2 section 2.1 (EAAS): the sender features are rotated into a
+ * frame whose z axis is the edge (Wigner-D blocks of the frame rotation),
+ * where the edge harmonics keep only m = 0 (Lemma 4.1) and each output order
+ * takes one input order (Eq. 13, 111 terms instead of 611), then rotated
+ * back and summed into the receiver.  Exact up to rounding; about 2.5x fewer
+ * FMAs per edge and channel, so it is the faster choice for per-edge
+ * (radial) weights.  Arguments and results as eqmp_fused.
+ */
+eqmp_status eqmp_fused_so2(const float* vec, const void* x, int64_t N_src, eqmp_dtype x_dtype,
+                           const int32_t* row_offsets, const int32_t* src, int64_t N, int64_t E,
+                           int32_t C, eqmp_weights weights, void* out, eqmp_dtype out_dtype,
+                           eqmp_stream_t stream);
+
+/*
  * Synchronous check of the graph preconditions on device data:
  * 0 <= row_offsets[0] <= ... <= row_offsets[N] <= E and
  * 0 <= src[e] < N_src for every e in [row_offsets[0], row_offsets[N]).

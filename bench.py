@@ -232,7 +232,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="pages_1k_c32")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--entry", default="fused", choices=["fused", "tp_scatter"])
+    ap.add_argument("--entry", default="fused", choices=["fused", "tp_scatter", "so2"])
     ap.add_argument("--pass", dest="which", default="forward", choices=["forward", "backward"],
                     help="backward: time eqmp_fused_backward (dx, dw or dR/dM, dvec) instead")
     args = ap.parse_args()
@@ -301,6 +301,8 @@ def main():
             eq.eqmp_fused_backward(*bwd_args[0], **bwd_args[1])
         elif args.entry == "fused":
             eq.eqmp_fused(vec, x, off, src, out=out, **wkw)
+        elif args.entry == "so2":
+            eq.eqmp_fused_so2(vec, x, off, src, out=out, **wkw)
         else:
             eq.eqmp_sh(vec, Yb)
             eq.eqmp_tp_scatter(Yb, x, off, src, out=out, **wkw)
@@ -413,7 +415,7 @@ def main():
             "value": wl.n_edges * world / (e2e_ms * 1e-3), "unit": "edges/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "pass": args.which,
-        "gpu_launches": args.steps * ((1 if args.entry == "fused" else 2) if bwd_args is None else 3),
+        "gpu_launches": args.steps * ((2 if args.entry == "tp_scatter" else 1) if bwd_args is None else 3),
         "clocks": clocks,
         "kernel_ms": {"min": float(np.min(kernel_ms)), "median": float(np.median(kernel_ms))},
         "watchdog": wd,

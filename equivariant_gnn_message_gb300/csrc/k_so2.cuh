@@ -32,10 +32,15 @@ constexpr float ir_v(int l, int m, int n) { return tables::kIrV[l - 2][m + 3][n 
 constexpr float ir_w(int l, int m, int n) { return tables::kIrW[l - 2][m + 3][n + 3]; }
 constexpr tables::AlignedTerm aligned_at(int i) { return tables::kAligned[i]; }
 
-// Edge ring entry (floats): D_1 (9) at 0, D_2 (25) at 9, D_3 (49) at 34,
-// radial features (8) at 84, zero-length flag at 92; 96 floats.
-constexpr int kEntryFloats = 96;
-constexpr int kD1 = 0, kD2 = 9, kD3 = 34, kRad = 84, kFlag = 92;
+// Edge ring entry (floats), rows padded to whole 16-byte chunks: D_1 rows of
+// 4 at 0 (3 x 4), D_2 rows of 8 at 12 (5 x 8), D_3 rows of 8 at 52 (7 x 8),
+// radial features (8) at 108, zero-length flag at 116; 120 floats.
+constexpr int kEntryFloats = 120;
+constexpr int kD1 = 0, kD2 = 12, kD3 = 52, kRad = 108, kFlag = 116;
+template <int L>
+constexpr int d_off() { return L == 1 ? kD1 : L == 2 ? kD2 : kD3; }
+template <int L>
+constexpr int d_stride() { return L == 1 ? 4 : 8; }
 
 // ---- Ivanic-Ruedenberg recursion (real SH without CS sign, (y,z,x) order) ---
 // R[i+1][j+1], i,j in {-1,0,1}; Dp: level L-1, (2L-1)^2 row-major.
@@ -93,13 +98,27 @@ __device__ __forceinline__ void ir_level(const float (&R)[3][3], const float* Dp
   ((Dl[Is] = ir_entry<L, Is / W - L, Is % W - L>(R, Dp)), ...);
 }
 
+constexpr float cs_sign_(int m) { return (m != 0 && (m & 1)) ? -1.0f : 1.0f; }
+
+// Level L straight into the edge entry (this library's signs, padded rows),
+// entry by entry, so the level is never held in registers.
+template <int L, int... Is>
+__device__ __forceinline__ void ir_level_store(const float (&R)[3][3], const float* Dp, float* out,
+                                               std::integer_sequence<int, Is...>) {
+  constexpr int W = 2 * L + 1, ST = L == 1 ? 4 : 8;
+  ((out[(Is / W) * ST + Is % W] =
+        cs_sign_(Is / W - L) * cs_sign_(Is % W - L) * ir_entry<L, Is / W - L, Is % W - L>(R, Dp)),
+   ...);
+}
+
 constexpr float cs_sign(int m) { return (m != 0 && (m & 1)) ? -1.0f : 1.0f; }
 
-// This library's basis: D[i][j] = s_i s_j D_IR[i][j], s = (-1)^|m|.
+// This library's basis: D[i][j] = s_i s_j D_IR[i][j], s = (-1)^|m|; rows
+// stored with the padded stride of the edge ring.
 template <int L, int... Is>
 __device__ __forceinline__ void store_block(const float* Dir, float* out, std::integer_sequence<int, Is...>) {
-  constexpr int W = 2 * L + 1;
-  ((out[Is] = cs_sign(Is / W - L) * cs_sign(Is % W - L) * Dir[Is]), ...);
+  constexpr int W = 2 * L + 1, ST = d_stride<L>();
+  ((out[(Is / W) * ST + Is % W] = cs_sign(Is / W - L) * cs_sign(Is % W - L) * Dir[Is]), ...);
 }
 
 // Frame and D_1..D_3 for unit direction (x, y, z) into entry e (83 floats).
@@ -115,12 +134,11 @@ __device__ __forceinline__ void wigner_blocks(float x, float y, float z, float* 
   const float R[3][3] = {{Q[1][1], Q[1][2], Q[1][0]},
                          {Q[2][1], Q[2][2], Q[2][0]},
                          {Q[0][1], Q[0][2], Q[0][0]}};
-  float D2[25], D3[49];
+  float D2[25];
   ir_level<2>(R, &R[0][0], D2, std::make_integer_sequence<int, 25>{});
-  ir_level<3>(R, D2, D3, std::make_integer_sequence<int, 49>{});
   store_block<1>(&R[0][0], e + kD1, std::make_integer_sequence<int, 9>{});
   store_block<2>(D2, e + kD2, std::make_integer_sequence<int, 25>{});
-  store_block<3>(D3, e + kD3, std::make_integer_sequence<int, 49>{});
+  ir_level_store<3>(R, D2, e + kD3, std::make_integer_sequence<int, 49>{});
 }
 
 template <int C, typename XT, bool RADIAL>
@@ -132,9 +150,13 @@ struct So2Cfg {
   static constexpr int ROWS = ROW_BYTES / 128;
   static constexpr int SLOT = ROW_BYTES < 1024 ? 1024 : ROW_BYTES;
   static constexpr int YR = 64;
-  static constexpr int M_BYTES = RADIAL ? 8 * 34 * C * 4 : 0;
+  // radial: M as [8][17][C] float2; shared: w as [34][C]
+  static constexpr int M_BYTES = RADIAL ? 8 * 34 * C * 4 : 34 * C * 4;
   static constexpr int FIXED = YR * kEntryFloats * 4 + 2 * EG * 16 * C * 4 + M_BYTES + 2 * 16 * 8 + 2048;
-  static constexpr int S_FIT = (227 * 1024 - FIXED) / SLOT;
+  // two CTAs per SM when at least 4 slots fit in half the shared memory
+  static constexpr int S_FIT2 = (113 * 1024 - FIXED) / SLOT;
+  static constexpr int MINB = S_FIT2 >= 4 ? 2 : 1;
+  static constexpr int S_FIT = MINB == 2 ? S_FIT2 : (227 * 1024 - FIXED) / SLOT;
   static constexpr int S = S_FIT >= 16 ? 16 : S_FIT >= 8 ? 8 : S_FIT >= 4 ? 4 : 2;
   static_assert(S % EG == 0 && S <= 32 && YR >= 32 + S && S_FIT >= 2, "ring layout");
   static constexpr int OFF_X = 0;
@@ -145,60 +167,93 @@ struct So2Cfg {
   static constexpr int SMEM_BYTES = OFF_BAR + 2 * S * 8 + 1024;
 };
 
-template <int P, int C, bool RADIAL>
-__device__ __forceinline__ void so2_weight_pair(const float2* Ms, int c, const float2 (&rr)[8], float (&W)[34]) {
-  // paths P, P+1 of channel c:  (W_P, W_P+1) = sum_k R_k (M[k][P][c], M[k][P+1][c])
-  float2 acc = make_float2(0.0f, 0.0f);
-#pragma unroll
-  for (int k = 0; k < 8; ++k) acc = __ffma2_rn(rr[k], Ms[(k * 17 + P / 2) * C + c], acc);
-  W[P] = acc.x;
-  W[P + 1] = acc.y;
-}
-
-template <int C, bool RADIAL, int... Ps>
-__device__ __forceinline__ void so2_weights(const float2* Ms, int c, const float2 (&rr)[8], float (&W)[34],
-                                            std::integer_sequence<int, Ps...>) {
-  (so2_weight_pair<2 * Ps, C, RADIAL>(Ms, c, rr, W), ...);
-}
-
-template <int I>
-__device__ __forceinline__ void so2_term(const float (&W)[34], const float (&xr)[16], float (&mp)[16]) {
-  constexpr tables::AlignedTerm t = aligned_at(I);
-  mp[t.k3] = fmaf(W[t.p], t.kappa * xr[t.k1], mp[t.k3]);
-}
-template <int... Is>
-__device__ __forceinline__ void so2_terms(const float (&W)[34], const float (&xr)[16], float (&mp)[16],
-                                          std::integer_sequence<int, Is...>) {
-  (so2_term<Is>(W, xr, mp), ...);
-}
-
-// x'_l[n] = sum_m D[m][n] x_l[m]
+// One padded D row (m) of level L from the edge entry into registers.
 template <int L>
-__device__ __forceinline__ void rotate_in(const float* D, const float (&x)[16], float (&xr)[16]) {
+__device__ __forceinline__ void load_row(const float* ent, int m, float (&row)[8]) {
+  const float4* p = reinterpret_cast<const float4*>(ent + d_off<L>() + m * d_stride<L>());
+  const float4 a = p[0];
+  row[0] = a.x; row[1] = a.y; row[2] = a.z; row[3] = a.w;
+  if constexpr (d_stride<L>() == 8) {
+    const float4 b = p[1];
+    row[4] = b.x; row[5] = b.y; row[6] = b.z; row[7] = b.w;
+  }
+}
+// x'_l[n] = sum_m D[m][n] x_l[m], rows of D streamed from shared memory
+template <int L>
+__device__ __forceinline__ void rotate_in(const float* ent, const float (&x)[16], float (&xr)[16]) {
   constexpr int W = 2 * L + 1, o = L * L;
 #pragma unroll
-  for (int n = 0; n < W; ++n) {
-    float s = 0.0f;
+  for (int n = 0; n < W; ++n) xr[o + n] = 0.0f;
 #pragma unroll
-    for (int m = 0; m < W; ++m) s = fmaf(D[m * W + n], x[o + m], s);
-    xr[o + n] = s;
+  for (int m = 0; m < W; ++m) {
+    float row[8];
+    load_row<L>(ent, m, row);
+#pragma unroll
+    for (int n = 0; n < W; ++n) xr[o + n] = fmaf(row[n], x[o + m], xr[o + n]);
   }
 }
 // out_l[m] += sum_n D[m][n] m'_l[n]
 template <int L>
-__device__ __forceinline__ void rotate_out(const float* D, const float (&mp)[16], float (&out)[16]) {
+__device__ __forceinline__ void rotate_out(const float* ent, const float (&mp)[16], float (&out)[16]) {
   constexpr int W = 2 * L + 1, o = L * L;
 #pragma unroll
   for (int m = 0; m < W; ++m) {
+    float row[8];
+    load_row<L>(ent, m, row);
     float s = out[o + m];
 #pragma unroll
-    for (int n = 0; n < W; ++n) s = fmaf(D[m * W + n], mp[o + n], s);
+    for (int n = 0; n < W; ++n) s = fmaf(row[n], mp[o + n], s);
     out[o + m] = s;
   }
 }
 
+// Aligned terms of one path (compile-time range of the table, sorted by path).
+constexpr int aligned_first(int p) {
+  for (int i = 0; i < tables::kNumAligned; ++i)
+    if (tables::kAligned[i].p == p) return i;
+  return tables::kNumAligned;
+}
+constexpr int aligned_count(int p) {
+  int c = 0;
+  for (int i = 0; i < tables::kNumAligned; ++i) c += tables::kAligned[i].p == p;
+  return c;
+}
+template <int First, int... Is>
+__device__ __forceinline__ void so2_path_terms(float wp, const float (&xr)[16], float (&mp)[16],
+                                               std::integer_sequence<int, Is...>) {
+  ((mp[aligned_at(First + Is).k3] =
+        fmaf(wp, aligned_at(First + Is).kappa * xr[aligned_at(First + Is).k1], mp[aligned_at(First + Is).k3])),
+   ...);
+}
+// Paths 2Q and 2Q+1: their weights (radial: one FFMA2 chain over k with M
+// pairs from shared memory; shared: registers), then their aligned terms.
+template <int Q, int C, bool RADIAL>
+__device__ __forceinline__ void so2_pair(const float2* Ms, int c, const float2 (&rr)[8],
+                                         const float (&xr)[16], float (&mp)[16]) {
+  constexpr int P0 = 2 * Q, P1 = 2 * Q + 1;
+  float w0, w1;
+  if constexpr (RADIAL) {
+    float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc = __ffma2_rn(rr[k], Ms[(k * 17 + Q) * C + c], acc);
+    w0 = acc.x;
+    w1 = acc.y;
+  } else {
+    const float* ws = reinterpret_cast<const float*>(Ms);
+    w0 = ws[P0 * C + c];
+    w1 = ws[P1 * C + c];
+  }
+  so2_path_terms<aligned_first(P0)>(w0, xr, mp, std::make_integer_sequence<int, aligned_count(P0)>{});
+  so2_path_terms<aligned_first(P1)>(w1, xr, mp, std::make_integer_sequence<int, aligned_count(P1)>{});
+}
+template <int C, bool RADIAL, int... Qs>
+__device__ __forceinline__ void so2_all(const float2* Ms, int c, const float2 (&rr)[8], const float (&xr)[16],
+                                        float (&mp)[16], std::integer_sequence<int, Qs...>) {
+  (so2_pair<Qs, C, RADIAL>(Ms, c, rr, xr, mp), ...);
+}
+
 template <int C, typename XT, bool RADIAL>
-__global__ void __launch_bounds__(So2Cfg<C, XT, RADIAL>::NTHREADS, 1)
+__global__ void __launch_bounds__(So2Cfg<C, XT, RADIAL>::NTHREADS, So2Cfg<C, XT, RADIAL>::MINB)
     k_so2(const __grid_constant__ CUtensorMap tmap, const LayerArgs a) {
   using K = So2Cfg<C, XT, RADIAL>;
   constexpr int S = K::S;
@@ -225,6 +280,9 @@ __global__ void __launch_bounds__(So2Cfg<C, XT, RADIAL>::NTHREADS, 1)
       Ms[i] = make_float2(__ldg(a.M + (size_t)k * 34 * C + (2 * pp) * C + c),
                           __ldg(a.M + (size_t)k * 34 * C + (2 * pp + 1) * C + c));
     }
+  } else {
+    float* ws = reinterpret_cast<float*>(Ms);
+    for (int i = tid; i < 34 * C; i += K::NTHREADS) ws[i] = __ldg(a.w + i);
   }
   __syncthreads();
   const int e_begin = min(max(__ldg(a.off + r_begin), 0), a.E);
@@ -288,11 +346,6 @@ __global__ void __launch_bounds__(So2Cfg<C, XT, RADIAL>::NTHREADS, 1)
   const int c = tid % C, g = tid / C;
   const uint32_t xlog = (uint32_t)(c * 16 * (int)sizeof(XT));
   const uint32_t xo[2] = {swz128(xlog), swz128(xlog + 16)};
-  float Wsh[34];
-  if constexpr (!RADIAL) {
-#pragma unroll
-    for (int p = 0; p < 34; ++p) Wsh[p] = __ldg(a.w + p * C + c);
-  }
   bool failed = false;
   int buf = 0;
   uint32_t n = 0;
@@ -330,50 +383,53 @@ __global__ void __launch_bounds__(So2Cfg<C, XT, RADIAL>::NTHREADS, 1)
           }
         }
       }
-      float W[34];
+      float2 rr[8];
       if constexpr (RADIAL) {
-        float2 rr[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) rr[k] = make_float2(ent[kRad + k], ent[kRad + k]);
-        so2_weights<C, RADIAL>(Ms, c, rr, W, std::make_integer_sequence<int, 17>{});
-      } else {
-#pragma unroll
-        for (int p = 0; p < 34; ++p) W[p] = Wsh[p];
       }
       const bool zero_len = ent[kFlag] != 0.0f;
-      // every read of slot s and entry m is done once x, W and the flag are in registers
-      float D1[9], D2[25], D3[49];
-#pragma unroll
-      for (int i = 0; i < 9; ++i) D1[i] = ent[kD1 + i];
-#pragma unroll
-      for (int i = 0; i < 25; ++i) D2[i] = ent[kD2 + i];
-#pragma unroll
-      for (int i = 0; i < 49; ++i) D3[i] = ent[kD3 + i];
-      mbar_arrive(empty0 + 8 * s);
       if (!zero_len) {
         float xr[16], mp[16];
         xr[0] = x[0];
-        rotate_in<1>(D1, x, xr);
-        rotate_in<2>(D2, x, xr);
-        rotate_in<3>(D3, x, xr);
+        rotate_in<1>(ent, x, xr);
+        rotate_in<2>(ent, x, xr);
+        rotate_in<3>(ent, x, xr);
 #pragma unroll
         for (int k = 0; k < 16; ++k) mp[k] = 0.0f;
-        so2_terms(W, xr, mp, std::make_integer_sequence<int, tables::kNumAligned>{});
+        so2_all<C, RADIAL>(Ms, c, rr, xr, mp, std::make_integer_sequence<int, 17>{});
         out[0] += mp[0];
-        rotate_out<1>(D1, mp, out);
-        rotate_out<2>(D2, mp, out);
-        rotate_out<3>(D3, mp, out);
+        rotate_out<1>(ent, mp, out);
+        rotate_out<2>(ent, mp, out);
+        rotate_out<3>(ent, mp, out);
       } else {
         // n = 0: Y = (Y00, 0, ...): only the paths (l, 0, l), identity CG
         constexpr float y00 = 0.28209479177387814f;
-        out[0] = fmaf(W[0] * y00, x[0], out[0]);
+        float w0, w4, w13, w24;
+        if constexpr (RADIAL) {
+          float2 a0 = make_float2(0.f, 0.f), a4 = a0, a12 = a0, a24 = a0;
 #pragma unroll
-        for (int k = 1; k < 4; ++k) out[k] = fmaf(W[4] * y00, x[k], out[k]);
+          for (int k = 0; k < 8; ++k) {
+            a0 = __ffma2_rn(rr[k], Ms[(k * 17 + 0) * C + c], a0);
+            a4 = __ffma2_rn(rr[k], Ms[(k * 17 + 2) * C + c], a4);
+            a12 = __ffma2_rn(rr[k], Ms[(k * 17 + 6) * C + c], a12);
+            a24 = __ffma2_rn(rr[k], Ms[(k * 17 + 12) * C + c], a24);
+          }
+          w0 = a0.x; w4 = a4.x; w13 = a12.y; w24 = a24.x;
+        } else {
+          const float* ws = reinterpret_cast<const float*>(Ms);
+          w0 = ws[0 * C + c]; w4 = ws[4 * C + c]; w13 = ws[13 * C + c]; w24 = ws[24 * C + c];
+        }
+        out[0] = fmaf(w0 * y00, x[0], out[0]);
 #pragma unroll
-        for (int k = 4; k < 9; ++k) out[k] = fmaf(W[13] * y00, x[k], out[k]);
+        for (int k = 1; k < 4; ++k) out[k] = fmaf(w4 * y00, x[k], out[k]);
 #pragma unroll
-        for (int k = 9; k < 16; ++k) out[k] = fmaf(W[24] * y00, x[k], out[k]);
+        for (int k = 4; k < 9; ++k) out[k] = fmaf(w13 * y00, x[k], out[k]);
+#pragma unroll
+        for (int k = 9; k < 16; ++k) out[k] = fmaf(w24 * y00, x[k], out[k]);
       }
+      // all reads of slot s and of edge entry m are done
+      mbar_arrive(empty0 + 8 * s);
     }
     n += deg;
     // group partials -> shared memory; thread (c, g) sums outputs k in its share

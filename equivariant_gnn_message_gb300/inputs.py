@@ -57,6 +57,8 @@ class Workload:
     w: Optional[np.ndarray]    # [34, C] float32
     R: Optional[np.ndarray]    # [E, 8] float32
     M: Optional[np.ndarray]    # [8, 34*C] float32
+    pos: Optional[np.ndarray] = None  # [N, 3] float32 atom positions (rounded from the draw)
+    cutoff: float = 0.0
 
     @property
     def n_edges(self) -> int:
@@ -129,4 +131,4 @@ def make_workload(name: str = None, *, n_atoms=None, cutoff=None, channels=None,
         name=name or "custom", n_atoms=n, channels=C, storage=spec["storage"],
         vec=np.ascontiguousarray(vec), src=src.astype(np.int32), dst=dst.astype(np.int32),
         off=csr_offsets(dst, n), x=np.ascontiguousarray(x), x_bf16_bits=bits,
-        w=w, R=R, M=M)
+        w=w, R=R, M=M, pos=pos.astype(np.float32), cutoff=float(spec["cutoff"]))

@@ -14,6 +14,10 @@ Modules
          their conversion to the real SH basis.
   layer  the channelwise CG tensor product with per-path channel weights (or
          per-edge radial weights W = R.M) and the sum into receivers.
+  backward  the chain rule of that layer: gradients of x, w (or R and M)
+         and of the edge vectors through the harmonics.
+  graph  the radius graph (ordered pairs closer than the cutoff, CSR by
+         receiver), with the cutoff decision taken in float32.
 
 Sources (web pages on the Batmobile kernels and on E2Former-V2):
   * "Batmobile CUDA内核优化：等变图神经网络的10-20倍加速策略" (blog post),

@@ -36,6 +36,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "edges/s fused SH+CG-TP+scatter (1k atoms, C=32, ~20 nbrs); % of roofline"
+METRIC_GRAPH = "edges/s radius graph (CSR by receiver, edge vectors)"
 FLUSH_BYTES = 256 << 20
 # DRAM bytes per launch of the layer kernel from the ncu capture recorded in
 # profiles/ (None until captured for the current kernel version).
@@ -233,8 +234,9 @@ def main():
     ap.add_argument("--workload", default="pages_1k_c32")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--entry", default="fused", choices=["fused", "tp_scatter", "so2"])
-    ap.add_argument("--pass", dest="which", default="forward", choices=["forward", "backward"],
-                    help="backward: time eqmp_fused_backward (dx, dw or dR/dM, dvec) instead")
+    ap.add_argument("--pass", dest="which", default="forward", choices=["forward", "backward", "graph"],
+                    help="backward: time eqmp_fused_backward (dx, dw or dR/dM, dvec) instead; "
+                         "graph: time eqmp_radius_graph on the workload's atom positions")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -296,8 +298,26 @@ def main():
         need = ("x", "vec", "w") if w is not None else ("x", "vec", "R", "M")
         bwd_args = ((vec, x, off, src, t(wl.dst), t(so), t(se), gout), dict(need=need, **wkw))
 
+    graph_args = None
+    if args.which == "graph":
+        import ctypes
+
+        lib = eq.load_library()
+        N = wl.n_atoms
+        g_pos = t(wl.pos)
+        g_ws = torch.empty(lib.eqmp_radius_graph_workspace_size(N), dtype=torch.uint8, device=dev)
+        g_E = torch.empty(1, dtype=torch.int64, device=dev)
+        g_out, E_graph = eq.eqmp_radius_graph(g_pos, wl.cutoff)
+        g_cap = E_graph
+        g_off, g_src, g_vec = g_out["off"], g_out["src"], g_out["vec"]
+        graph_args = (g_pos.data_ptr(), N, ctypes.c_float(wl.cutoff), g_off.data_ptr(), g_src.data_ptr(),
+                      g_vec.data_ptr(), None, None, g_cap, g_E.data_ptr(), g_ws.data_ptr(), g_ws.numel(),
+                      stream.cuda_stream)
+
     def step():
-        if bwd_args is not None:
+        if graph_args is not None:
+            lib.eqmp_radius_graph(*graph_args)
+        elif bwd_args is not None:
             eq.eqmp_fused_backward(*bwd_args[0], **bwd_args[1])
         elif args.entry == "fused":
             eq.eqmp_fused(vec, x, off, src, out=out, **wkw)
@@ -354,6 +374,19 @@ def main():
         eq.eqmp_fused(d_in["vec"], xd, d_in["off"], d_in["src"], out=out, **kw)
         h_out.copy_(out, non_blocking=True)
 
+    if graph_args is not None:
+        h_in = {"pos": pin(wl.pos)}
+        d_in = {"pos": g_pos}
+        h_out = [torch.empty(a.shape, dtype=a.dtype).pin_memory() for a in (g_off, g_src, g_vec)]
+        h2d = h_in["pos"].numel() * 4
+        d2h = sum(a.numel() * a.element_size() for a in h_out)
+
+        def e2e_step():
+            d_in["pos"].copy_(h_in["pos"], non_blocking=True)
+            lib.eqmp_radius_graph(*graph_args)
+            for h, d in zip(h_out, (g_off, g_src, g_vec)):
+                h.copy_(d, non_blocking=True)
+
     e2e_ms = None
     if bwd_args is None:  # the end-to-end figure is the forward layer's
         for _ in range(3):
@@ -388,16 +421,39 @@ def main():
     achieved = flops / (ms * 1e-3) / 1e12
     version = KERNEL_VERSION["shared" if wl.w is not None else "radial"] if bwd_args is None else "k_bwd-v1"
     traffic = NCU_TRAFFIC.get((args.workload, version)) if args.entry == "fused" else None
-    value = wl.n_edges * world / (ms * 1e-3)
+    n_edges = wl.n_edges if graph_args is None else E_graph
+    value = n_edges * world / (ms * 1e-3)
+    roofline = {"bound": "alu", "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
+                "frac": achieved / peak_tflops, "traffic": traffic, "traffic_unit": "bytes/launch",
+                "kernel": version,
+                "peak_basis": f"{props.multi_processor_count} SMs x 128 FP32 lanes x 2 x {max_mhz:.0f} MHz (derived)",
+                "hbm_gbs_compulsory": compulsory_bytes(wl) / (ms * 1e-3) / 1e9}
+    if graph_args is not None:
+        # positions in; offsets, senders and edge vectors out
+        gbytes = 12 * wl.n_atoms + 4 * (wl.n_atoms + 1) + 16 * E_graph
+        hbm = float(peaks.get("hbm_gbs", 6787.2))
+        gach = gbytes / (ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": gach, "peak": hbm, "unit": "GB/s", "frac": gach / hbm,
+                    "traffic": None, "kernel": "radius-graph-v1 (12 launches)",
+                    "algorithmic_bytes": gbytes, "peak_basis": "MEASURED_PEAKS.json hbm_gbs (measured copy)"}
 
     cpu = None
-    if pool is not None:
+    if pool is not None and graph_args is not None:
+        from oracle import graph as oracle_graph
+
+        pool.terminate()
+        tg = time.perf_counter()
+        E_cpu = len(oracle_graph.radius_graph(wl.pos, wl.cutoff)["src"])
+        wall = time.perf_counter() - tg
+        cpu = {"value": E_cpu / wall, "unit": "edges/s", "cores": 1, "kind": "oracle",
+               "sample": f"whole workload ({wl.n_atoms} atoms, {E_cpu} edges), k-d tree candidates + float32 test, {wall:.2f} s"}
+    elif pool is not None:
         rate, sample = cpu_oracle_rate(args.workload, wl, pool=pool, cores=cores)
         pool.terminate()
         cpu = {"value": rate, "unit": "edges/s", "cores": cores, "kind": "oracle", "sample": sample}
 
     line = {
-        "metric": METRIC, "value": value, "unit": "edges/s", "n_gpus": world,
+        "metric": METRIC if graph_args is None else METRIC_GRAPH, "value": value, "unit": "edges/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32" if wl.storage == "f32" else "bf16-storage/f32-compute", "data": "synthetic",
@@ -406,16 +462,14 @@ def main():
                    "weights": "shared" if wl.w is not None else "radial", "entry": args.entry,
                    "l2": "flushed (256 MB write) before every timed step",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
-                     "frac": achieved / peak_tflops, "traffic": traffic, "traffic_unit": "bytes/launch",
-                     "kernel": version,
-                     "peak_basis": f"{props.multi_processor_count} SMs x 128 FP32 lanes x 2 x {max_mhz:.0f} MHz (derived)",
-                     "hbm_gbs_compulsory": compulsory_bytes(wl) / (ms * 1e-3) / 1e9},
+        "roofline": roofline,
         "e2e": None if e2e_ms is None else {
-            "value": wl.n_edges * world / (e2e_ms * 1e-3), "unit": "edges/s",
+            "value": n_edges * world / (e2e_ms * 1e-3), "unit": "edges/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "pass": args.which,
-        "gpu_launches": args.steps * ((2 if args.entry == "tp_scatter" else 1) if bwd_args is None else 3),
+        "graph_edges": None if graph_args is None else E_graph,
+        "gpu_launches": args.steps * (12 if graph_args is not None else
+                                      (2 if args.entry == "tp_scatter" else 1) if bwd_args is None else 3),
         "clocks": clocks,
         "kernel_ms": {"min": float(np.min(kernel_ms)), "median": float(np.median(kernel_ms))},
         "watchdog": wd,

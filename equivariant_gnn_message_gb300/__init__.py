@@ -16,6 +16,8 @@ Entry points (same names as the C ABI):
   eqmp_device_error()                           -> int (watchdog code)
   eqmp_fused_backward(vec, x, row_offsets, src, dst, send_offsets, send_edges, grad_out, ...)
                                                 -> dict of gradients
+  eqmp_fused_backward_noalloc(...)              -> the same, no workspace
+  eqmp_radius_graph(pos, cutoff)                -> (dict(off, src, vec[, dst, rev]), E)
   eqmp_path_table()                             -> list of (l1, l2, l3)
 """
 import ctypes
@@ -24,7 +26,7 @@ import os
 __all__ = [
     "EqmpError", "load_library", "library_path", "eqmp_num_paths", "eqmp_path_table",
     "eqmp_status_string", "eqmp_sh", "eqmp_tp_scatter", "eqmp_fused", "eqmp_fused_so2", "eqmp_validate_graph",
-    "eqmp_device_error", "eqmp_fused_backward", "sender_view", "EQMP_OK", "EQMP_ERR_INVALID_ARG", "EQMP_ERR_UNSUPPORTED",
+    "eqmp_device_error", "eqmp_fused_backward", "eqmp_fused_backward_noalloc", "eqmp_radius_graph", "sender_view", "EQMP_OK", "EQMP_ERR_INVALID_ARG", "EQMP_ERR_UNSUPPORTED",
     "EQMP_ERR_CUDA", "EQMP_ERR_DEVICE_TIMEOUT", "EQMP_ERR_GRAPH",
 ]
 
@@ -85,6 +87,11 @@ def load_library():
     lib.eqmp_fused_backward.argtypes = [vp, vp, i64, vp, vp, vp, vp, vp, i64, i64, i64, i32, Weights,
                                         vp, vp, vp, vp, vp, vp, vp, i64, vp]
     lib.eqmp_fused_backward.restype = i32
+    lib.eqmp_radius_graph_workspace_size.argtypes = [i64]
+    lib.eqmp_radius_graph_workspace_size.restype = ctypes.c_size_t
+    lib.eqmp_radius_graph.argtypes = [vp, i64, ctypes.c_float, vp, vp, vp, vp, vp, i64, vp, vp,
+                                      ctypes.c_size_t, vp]
+    lib.eqmp_radius_graph.restype = i32
     _lib = lib
     return lib
 
@@ -233,6 +240,50 @@ def eqmp_device_error():
     if st not in (EQMP_OK, EQMP_ERR_DEVICE_TIMEOUT):
         _check(st, "eqmp_device_error")
     return int(code.value)
+
+
+def eqmp_radius_graph(pos, cutoff, e_cap=None, dst=False, rev=False, stream=None):
+    """Radius graph of pos [N, 3] fp32 (CUDA): dict(off, src, vec[, dst][, rev]), E.
+
+    Edges j -> i for i != j with the float32 squared distance below
+    cutoff^2, CSR by receiver with senders ascending.  When the edge count
+    exceeds the capacity (e_cap, default 64 N), the call is repeated once
+    with the exact count, which costs one device-to-host read of E.
+    """
+    import torch
+
+    _require(pos, "pos", torch.float32)
+    if pos.dim() != 2 or pos.shape[1] != 3:
+        raise ValueError("pos must be [N, 3]")
+    lib = load_library()
+    N = pos.shape[0]
+    dev = pos.device
+    ws = torch.empty(max(int(lib.eqmp_radius_graph_workspace_size(N)), 256), dtype=torch.uint8, device=dev)
+    off = torch.empty(N + 1, dtype=torch.int32, device=dev)
+    e_total = torch.empty(1, dtype=torch.int64, device=dev)
+    cap = int(64 * N if e_cap is None else e_cap)
+    st = _stream(stream)
+    for _ in range(2):
+        out = dict(off=off, src=torch.empty(cap, dtype=torch.int32, device=dev),
+                   vec=torch.empty((cap, 3), dtype=torch.float32, device=dev))
+        if dst:
+            out["dst"] = torch.empty(cap, dtype=torch.int32, device=dev)
+        if rev:
+            out["rev"] = torch.empty(cap, dtype=torch.int32, device=dev)
+        _check(lib.eqmp_radius_graph(_ptr(pos), N, float(cutoff), _ptr(off), _ptr(out["src"]),
+                                     _ptr(out["vec"]), _ptr(out.get("dst")), _ptr(out.get("rev")), cap,
+                                     _ptr(e_total), _ptr(ws), ws.numel(), st), "eqmp_radius_graph")
+        E = int(e_total.item())
+        if E < 0:
+            raise EqmpError(EQMP_ERR_INVALID_ARG, "eqmp_radius_graph: positions non-finite or out of range"
+                            if E == -1 else "eqmp_radius_graph: 2^31 edges or more")
+        if E <= cap:
+            break
+        cap = E
+    for k in ("src", "vec", "dst", "rev"):
+        if k in out:
+            out[k] = out[k][:E]
+    return out, E
 
 
 def sender_view(src, n_src):

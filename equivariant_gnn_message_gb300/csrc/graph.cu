@@ -1,0 +1,410 @@
+// Radius graph on the GPU: every ordered pair i != j with |p_j - p_i| < r_c,
+// as CSR rows by receiver with senders ascending, plus the edge vectors
+// p_j - p_i.  E2Former-V2 (section 4.2) builds neighbour lists by a radius
+// cutoff; the Batmobile blog (monitoring section) uses 4-6 Angstrom.
+//
+// The cutoff decision is taken in float32 in one fixed order, each operation
+// rounded on its own (no contraction into FMA):
+//     d_a = p_j[a] - p_i[a];  d2 = (d_x*d_x + d_y*d_y) + d_z*d_z;  edge iff d2 < r_c*r_c.
+//
+// Pipeline (all on the caller's stream, no host synchronisation):
+//   k_clear    zero the bucket counters
+//   k_bin      cell of each atom (cell side = r_c (1 + 2^-10)), hashed into
+//              H = 2^k >= 2N buckets; count atoms per bucket
+//   scan       bucket starts (exclusive prefix sum)
+//   k_scatter  atoms listed bucket by bucket
+//   k_neigh    (count) one thread per receiver, visited in bucket order so
+//              neighbouring threads read the same buckets: test every atom
+//              of the 27 surrounding cells' buckets (each bucket once)
+//   scan       degrees -> row_offsets, E_total
+//   k_neigh    (fill) the same walk writes each receiver's senders, unsorted
+//   k_sort     one warp per receiver: rank sort of its senders, writes
+//              src, vec (and dst) at the sorted position
+//   k_rev      (optional) position of the reverse edge, by binary search
+// Bucket order and fill order depend on atomics; the output does not: the
+// degree is a count and each row is sorted, so the result is bitwise
+// deterministic.
+#include <math.h>
+#include <stdint.h>
+
+#include "eqmp.h"
+#include "launch.h"
+
+namespace eqmp {
+namespace {
+
+constexpr int kScanThreads = 1024;
+constexpr int kScanItems = 4;
+constexpr int kScanTile = kScanThreads * kScanItems;
+constexpr int kNeighThreads = 256;
+constexpr int kSortWarps = 8;
+constexpr int kSortCap = 512;          // row length sorted in shared memory
+constexpr float kCellRange = 4096.0f;  // |p| / cell side must stay below this
+constexpr long long kGraphMaxAtoms = 1ll << 30;  // keeps the bucket count <= 2^31
+
+// Cell coordinates hashed as in Teschner et al. 2003 (optimised spatial
+// hashing: XOR of coordinates times three large primes), then mixed by the
+// MurmurHash3 finaliser so that masking to the low bits stays uniform.
+__device__ __forceinline__ uint32_t cell_hash(int cx, int cy, int cz, uint32_t mask) {
+  uint32_t h = (uint32_t)cx * 73856093u ^ (uint32_t)cy * 19349663u ^ (uint32_t)cz * 83492791u;
+  h ^= h >> 16;
+  h *= 0x85ebca6bu;
+  h ^= h >> 13;
+  h *= 0xc2b2ae35u;
+  h ^= h >> 16;
+  return h & mask;
+}
+
+__device__ __forceinline__ int cell_of(float p, float inv) {
+  const float c = floorf(__fmul_rn(p, inv));
+  return (int)fminf(fmaxf(c, -kCellRange - 2.0f), kCellRange + 2.0f);
+}
+
+__device__ __forceinline__ float dist2(float3 a, float3 b) {
+  const float dx = __fsub_rn(b.x, a.x), dy = __fsub_rn(b.y, a.y), dz = __fsub_rn(b.z, a.z);
+  return __fadd_rn(__fadd_rn(__fmul_rn(dx, dx), __fmul_rn(dy, dy)), __fmul_rn(dz, dz));
+}
+
+__device__ __forceinline__ float3 load_pos(const float* __restrict__ pos, int i) {
+  return make_float3(__ldg(pos + 3 * (size_t)i), __ldg(pos + 3 * (size_t)i + 1), __ldg(pos + 3 * (size_t)i + 2));
+}
+
+// ------------------------------------------------------------ scan
+// Exclusive prefix sum of int32 data in place, with 64-bit block totals so
+// that the grand total is exact even where the int32 prefix would wrap.
+__device__ __forceinline__ long long block_exclusive(long long v, long long* warp_tot, long long* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  long long incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) warp_tot[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    long long w = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
+    long long wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long t = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += t;
+    }
+    warp_tot[lane] = wi - w;
+    if (lane == 31) *total = wi;
+  }
+  __syncthreads();
+  const long long r = warp_tot[wid] + incl - v;
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kScanThreads) k_scan_local(int32_t* __restrict__ data, long long n,
+                                                             long long* __restrict__ block_sums) {
+  __shared__ long long warp_tot[32];
+  __shared__ long long total;
+  const long long base = (long long)blockIdx.x * kScanTile + (long long)threadIdx.x * kScanItems;
+  int v[kScanItems];
+  long long s = 0;
+#pragma unroll
+  for (int k = 0; k < kScanItems; ++k) {
+    v[k] = base + k < n ? data[base + k] : 0;
+    s += v[k];
+  }
+  long long run = block_exclusive(s, warp_tot, &total);
+#pragma unroll
+  for (int k = 0; k < kScanItems; ++k) {
+    if (base + k < n) data[base + k] = (int32_t)run;
+    run += v[k];
+  }
+  if (threadIdx.x == 0) block_sums[blockIdx.x] = total;
+}
+
+// One block: exclusive scan of the block totals (any count, in tiles), the
+// grand total, and the edge count reported to the caller when asked.
+__global__ void __launch_bounds__(kScanThreads) k_scan_top(long long* __restrict__ sums, long long nb,
+                                                           const int* __restrict__ bad,
+                                                           long long* __restrict__ e_total) {
+  __shared__ long long warp_tot[32];
+  __shared__ long long total;
+  long long carry = 0;
+  for (long long b0 = 0; b0 < nb; b0 += kScanThreads) {
+    const long long b = b0 + threadIdx.x;
+    const long long v = b < nb ? sums[b] : 0;
+    const long long r = block_exclusive(v, warp_tot, &total);
+    if (b < nb) sums[b] = carry + r;
+    carry += total;
+    __syncthreads();
+  }
+  if (e_total && threadIdx.x == 0) {
+    long long e = carry;
+    if (e > INT32_MAX) e = -2;
+    if (*bad) e = -1;
+    *e_total = e;
+  }
+}
+
+__global__ void __launch_bounds__(kScanThreads) k_scan_add(int32_t* __restrict__ data, long long n,
+                                                           const long long* __restrict__ block_sums) {
+  const int add = (int)block_sums[blockIdx.x];
+  const long long base = (long long)blockIdx.x * kScanTile;
+  for (int k = threadIdx.x; k < kScanTile; k += kScanThreads)
+    if (base + k < n) data[base + k] += add;
+}
+
+cudaError_t exclusive_scan(int32_t* data, long long n, long long* block_sums, const int* bad, long long* e_total,
+                           cudaStream_t st) {
+  const long long nb = (n + kScanTile - 1) / kScanTile;
+  k_scan_local<<<(unsigned)nb, kScanThreads, 0, st>>>(data, n, block_sums);
+  k_scan_top<<<1, kScanThreads, 0, st>>>(block_sums, nb, bad, e_total);
+  k_scan_add<<<(unsigned)nb, kScanThreads, 0, st>>>(data, n, block_sums);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ binning
+__global__ void k_clear(int32_t* __restrict__ a, long long n, int* __restrict__ bad) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+    a[i] = 0;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *bad = 0;
+}
+
+__global__ void k_bin(const float* __restrict__ pos, int N, float inv, uint32_t mask, int32_t* __restrict__ atom_bucket,
+                      int32_t* __restrict__ count, int* __restrict__ bad) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= N) return;
+  const float3 p = load_pos(pos, i);
+  const float qx = __fmul_rn(p.x, inv), qy = __fmul_rn(p.y, inv), qz = __fmul_rn(p.z, inv);
+  // false for NaN as well as for out-of-range coordinates
+  const bool ok = fabsf(qx) < kCellRange && fabsf(qy) < kCellRange && fabsf(qz) < kCellRange;
+  if (!ok) atomicOr(bad, 1);
+  const uint32_t h = cell_hash(cell_of(p.x, inv), cell_of(p.y, inv), cell_of(p.z, inv), mask);
+  atom_bucket[i] = (int32_t)h;
+  atomicAdd(count + h, 1);
+}
+
+__global__ void k_scatter(int N, const int32_t* __restrict__ atom_bucket, const int32_t* __restrict__ start,
+                          int32_t* __restrict__ fill, int32_t* __restrict__ bucket_atoms) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= N) return;
+  const int h = atom_bucket[i];
+  bucket_atoms[start[h] + atomicAdd(fill + h, 1)] = i;
+}
+
+// ------------------------------------------------------------ neighbour walk
+// FILL = false: row_offsets[i] = degree of i (row_offsets[N] = 0).
+// FILL = true:  senders of i written, unsorted, to src[off[i] .. off[i+1]).
+template <bool FILL>
+__global__ void __launch_bounds__(kNeighThreads) k_neigh(const float* __restrict__ pos, int N, float inv, float rc2,
+                                                         uint32_t mask, const int32_t* __restrict__ start,
+                                                         const int32_t* __restrict__ bucket_atoms,
+                                                         int32_t* __restrict__ row_offsets,
+                                                         int32_t* __restrict__ src, long long e_cap) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (!FILL && t == 0) row_offsets[N] = 0;
+  if (t >= N) return;
+  const int i = bucket_atoms[t];
+  const float3 pi = load_pos(pos, i);
+  const int cx = cell_of(pi.x, inv), cy = cell_of(pi.y, inv), cz = cell_of(pi.z, inv);
+  long long w = 0, w_end = 0;
+  if (FILL) {
+    w = row_offsets[i];
+    w_end = row_offsets[i + 1];
+    if (w < 0 || w_end > e_cap || w_end < w) return;  // row outside the caller's capacity
+  }
+  int count = 0;
+  uint32_t seen[27];  // fully unrolled below: stays in registers
+#pragma unroll
+  for (int c = 0; c < 27; ++c) {
+    const uint32_t h = cell_hash(cx + c % 3 - 1, cy + (c / 3) % 3 - 1, cz + c / 9 - 1, mask);
+    seen[c] = h;
+    bool dup = false;  // two cells in one bucket: visit the bucket once
+#pragma unroll
+    for (int k = 0; k < c; ++k) dup |= seen[k] == h;
+    if (dup) continue;
+    const int b1 = start[h + 1];
+    for (int s = start[h]; s < b1; ++s) {
+      const int j = bucket_atoms[s];
+      if (j == i) continue;
+      if (dist2(pi, load_pos(pos, j)) < rc2) {
+        if (FILL) {
+          if (w < w_end) src[w++] = j;
+        } else {
+          ++count;
+        }
+      }
+    }
+  }
+  if (!FILL) row_offsets[i] = count;
+}
+
+// ------------------------------------------------------------ row sort
+// One warp per receiver.  Senders in a row are distinct, so the rank of a
+// sender (the number of smaller ones) is its sorted position.  Rows up to
+// kSortCap are ranked from shared memory; longer rows are staged in the
+// row's own vec storage (3 words per edge, so it holds the row) and ranked
+// from there before vec is written.
+__global__ void __launch_bounds__(kSortWarps * 32) k_sort(const float* __restrict__ pos, int N,
+                                                          const int32_t* __restrict__ row_offsets,
+                                                          int32_t* __restrict__ src, float* __restrict__ vec,
+                                                          int32_t* __restrict__ dst, long long e_cap) {
+  __shared__ int32_t rows[kSortWarps][kSortCap];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int i = blockIdx.x * kSortWarps + wid;
+  if (i >= N) return;
+  const long long beg = row_offsets[i], end = row_offsets[i + 1];
+  if (beg < 0 || end > e_cap || end < beg) return;
+  const int k = (int)(end - beg);
+  const float3 pi = load_pos(pos, i);
+  int32_t* row = src + beg;
+  if (k <= kSortCap) {
+    int32_t* sm = rows[wid];
+    for (int a = lane; a < k; a += 32) sm[a] = row[a];
+    __syncwarp();
+    for (int a = lane; a < k; a += 32) {
+      const int v = sm[a];
+      int r = 0;
+      for (int b = 0; b < k; ++b) r += sm[b] < v;
+      row[r] = v;
+      const float3 pj = load_pos(pos, v);
+      float* o = vec + 3 * (beg + r);
+      o[0] = __fsub_rn(pj.x, pi.x);
+      o[1] = __fsub_rn(pj.y, pi.y);
+      o[2] = __fsub_rn(pj.z, pi.z);
+      if (dst) dst[beg + r] = i;
+    }
+    return;
+  }
+  int32_t* stage = reinterpret_cast<int32_t*>(vec + 3 * beg);
+  for (int a = lane; a < k; a += 32) stage[a] = row[a];
+  __syncwarp();
+  for (int a = lane; a < k; a += 32) {
+    const int v = stage[a];
+    int r = 0;
+    for (int b = 0; b < k; ++b) r += stage[b] < v;
+    row[r] = v;
+  }
+  __syncwarp();
+  for (int a = lane; a < k; a += 32) {
+    const float3 pj = load_pos(pos, row[a]);
+    float* o = vec + 3 * (beg + a);
+    o[0] = __fsub_rn(pj.x, pi.x);
+    o[1] = __fsub_rn(pj.y, pi.y);
+    o[2] = __fsub_rn(pj.z, pi.z);
+    if (dst) dst[beg + a] = i;
+  }
+}
+
+// rev[e] for e = (i <- j): the position of (j <- i) in row j (binary search;
+// the relation is symmetric, so it exists).
+__global__ void k_rev(int N, const int32_t* __restrict__ row_offsets, const int32_t* __restrict__ src,
+                      int32_t* __restrict__ rev, long long e_cap) {
+  const int lane = threadIdx.x & 31;
+  const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (i >= N) return;
+  const long long beg = row_offsets[i], end = row_offsets[i + 1];
+  if (beg < 0 || end > e_cap || end < beg) return;
+  for (long long e = beg + lane; e < end; e += 32) {
+    const int j = src[e];
+    long long lo = row_offsets[j], hi = row_offsets[j + 1];
+    if (lo < 0 || hi > e_cap || hi < lo) {
+      rev[e] = -1;
+      continue;
+    }
+    while (lo < hi) {
+      const long long mid = (lo + hi) >> 1;
+      if (src[mid] < i) lo = mid + 1;
+      else hi = mid;
+    }
+    rev[e] = (lo < row_offsets[j + 1] && src[lo] == i) ? (int32_t)lo : -1;
+  }
+}
+
+// ------------------------------------------------------------ workspace
+struct GraphWs {
+  long long H = 0;
+  size_t atom_bucket = 0, start = 0, fill = 0, bucket_atoms = 0, sums = 0, bad = 0, bytes = 0;
+};
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+GraphWs graph_ws(long long N) {
+  GraphWs w;
+  long long H = 64;
+  while (H < 2 * N) H <<= 1;
+  w.H = H;
+  const long long scan_n = (H + 1 > N + 1 ? H + 1 : N + 1);
+  const long long nb = (scan_n + kScanTile - 1) / kScanTile;
+  size_t o = 0;
+  w.atom_bucket = o; o = align256(o + 4 * (size_t)N);
+  w.start = o;       o = align256(o + 4 * (size_t)(H + 1));
+  w.fill = o;        o = align256(o + 4 * (size_t)H);
+  w.bucket_atoms = o; o = align256(o + 4 * (size_t)N);
+  w.sums = o;        o = align256(o + 8 * (size_t)nb);
+  w.bad = o;         o = align256(o + 4);
+  w.bytes = o;
+  return w;
+}
+
+}  // namespace
+}  // namespace eqmp
+
+using namespace eqmp;
+
+extern "C" {
+
+size_t eqmp_radius_graph_workspace_size(int64_t N) {
+  if (N < 0 || N > kGraphMaxAtoms) return 0;
+  return graph_ws(N).bytes;
+}
+
+eqmp_status eqmp_radius_graph(const float* pos, int64_t N, float cutoff, int32_t* row_offsets, int32_t* src,
+                              float* vec, int32_t* dst, int32_t* rev, int64_t E_cap, int64_t* E_total,
+                              void* workspace, size_t workspace_bytes, eqmp_stream_t stream) {
+  if (N < 0 || E_cap < 0) return EQMP_ERR_INVALID_ARG;
+  if (N > kGraphMaxAtoms) return EQMP_ERR_UNSUPPORTED;
+  if (!(cutoff > 0.0f) || !isfinite(cutoff)) return EQMP_ERR_INVALID_ARG;
+  if (!row_offsets || !E_total) return EQMP_ERR_INVALID_ARG;
+  if (N > 0 && !pos) return EQMP_ERR_INVALID_ARG;
+  if (E_cap > 0 && (!src || !vec)) return EQMP_ERR_INVALID_ARG;
+  const GraphWs w = graph_ws(N);
+  if (!workspace || workspace_bytes < w.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return EQMP_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(workspace);
+  int32_t* atom_bucket = reinterpret_cast<int32_t*>(base + w.atom_bucket);
+  int32_t* start = reinterpret_cast<int32_t*>(base + w.start);
+  int32_t* fill = reinterpret_cast<int32_t*>(base + w.fill);
+  int32_t* bucket_atoms = reinterpret_cast<int32_t*>(base + w.bucket_atoms);
+  long long* sums = reinterpret_cast<long long*>(base + w.sums);
+  int* bad = reinterpret_cast<int*>(base + w.bad);
+  // start and fill are adjacent: one clear covers both
+  const long long n_clear = (long long)((w.bucket_atoms - w.start) / 4);
+
+  const double cell = (double)cutoff * (1.0 + 1.0 / 1024.0);
+  const float inv = (float)(1.0 / cell);
+  const float rc2 = cutoff * cutoff;
+  const uint32_t mask = (uint32_t)(w.H - 1);
+  const int nblk = (int)((N + kNeighThreads - 1) / kNeighThreads);
+
+  k_clear<<<256, 256, 0, st>>>(start, n_clear, bad);
+  if (N > 0) {
+    k_bin<<<nblk, kNeighThreads, 0, st>>>(pos, (int)N, inv, mask, atom_bucket, start, bad);
+  }
+  cudaError_t err = exclusive_scan(start, w.H + 1, sums, bad, nullptr, st);
+  if (err != cudaSuccess) return EQMP_ERR_CUDA;
+  if (N > 0) k_scatter<<<nblk, kNeighThreads, 0, st>>>((int)N, atom_bucket, start, fill, bucket_atoms);
+  k_neigh<false><<<nblk > 0 ? nblk : 1, kNeighThreads, 0, st>>>(pos, (int)N, inv, rc2, mask, start, bucket_atoms,
+                                                               row_offsets, nullptr, E_cap);
+  err = exclusive_scan(row_offsets, N + 1, sums, bad, reinterpret_cast<long long*>(E_total), st);
+  if (err != cudaSuccess) return EQMP_ERR_CUDA;
+  if (N > 0 && E_cap > 0) {
+    k_neigh<true><<<nblk, kNeighThreads, 0, st>>>(pos, (int)N, inv, rc2, mask, start, bucket_atoms, row_offsets, src,
+                                                  E_cap);
+    const int sblk = (int)((N + kSortWarps - 1) / kSortWarps);
+    k_sort<<<sblk, kSortWarps * 32, 0, st>>>(pos, (int)N, row_offsets, src, vec, dst, E_cap);
+    if (rev) k_rev<<<sblk, kSortWarps * 32, 0, st>>>((int)N, row_offsets, src, rev, E_cap);
+  }
+  return cuda_status(cudaGetLastError());
+}
+
+}  // extern "C"

@@ -226,7 +226,8 @@ __device__ __forceinline__ void so2_path_terms(float wp, const float (&xr)[16], 
    ...);
 }
 // Paths 2Q and 2Q+1: their weights (radial: one FFMA2 chain over k with M
-// pairs from shared memory; shared: registers), then their aligned terms.
+// pairs from shared memory; shared: w[p][c] from shared memory), then their
+// aligned terms.
 template <int Q, int C, bool RADIAL>
 __device__ __forceinline__ void so2_pair(const float2* Ms, int c, const float2 (&rr)[8],
                                          const float (&xr)[16], float (&mp)[16]) {

@@ -52,6 +52,7 @@
 #ifndef EQMP_H
 #define EQMP_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -211,6 +212,51 @@ eqmp_status eqmp_fused_so2(const float* vec, const void* x, int64_t N_src, eqmp_
                            const int32_t* row_offsets, const int32_t* src, int64_t N, int64_t E,
                            int32_t C, eqmp_weights weights, void* out, eqmp_dtype out_dtype,
                            eqmp_stream_t stream);
+
+/*
+ * Radius graph: the step before the layer.  E2Former-V2 (section 4.2,
+ * deployment notes) builds neighbour lists by a radius cutoff instead of a
+ * fixed k nearest neighbours; the Batmobile blog (monitoring section) takes
+ * the cutoff as 4-6 Angstrom.  Open boundaries (no periodic images).
+ *
+ * Edges: sender j -> receiver i for every ordered pair i != j with
+ * d2 < cutoff*cutoff, where, in float32 with each operation rounded on its
+ * own, d_a = pos[j][a] - pos[i][a] and d2 = (d_x*d_x + d_y*d_y) + d_z*d_z.
+ * The result is bitwise deterministic and independent of the hardware's
+ * scheduling.
+ *
+ *   pos          [N][3] fp32, device.  |pos| / cutoff < about 4096 per
+ *                coordinate and finite, else *E_total = -1 and the other
+ *                outputs are unspecified.
+ *   cutoff       > 0, finite (EQMP_ERR_INVALID_ARG otherwise).
+ *   row_offsets  [N+1] int32, device, written: CSR rows by receiver,
+ *                row_offsets[0] = 0, row_offsets[N] = E.
+ *   src          [E_cap] int32, device, written: senders, ascending in a row.
+ *   vec          [E_cap][3] fp32, device, written: pos[src] - pos[receiver]
+ *                (one float32 subtraction per component).
+ *   dst          [E_cap] int32 or NULL: receiver of each edge.
+ *   rev          [E_cap] int32 or NULL: index of the reverse edge
+ *                (receiver <- sender).  For this symmetric relation
+ *                (row_offsets, rev) is the sender view that
+ *                eqmp_fused_backward takes as (send_offsets, send_edges).
+ *   E_cap        capacity of src/vec/dst/rev in edges (>= 0).
+ *   E_total      one int64 in device memory, written with E, or -1 (bad
+ *                positions) or -2 (E >= 2^31).  If E > E_cap, row_offsets is
+ *                still valid but src/vec/dst/rev are unspecified: allocate
+ *                E edges and call again.
+ *   workspace    device memory, 256-byte aligned, of at least
+ *                eqmp_radius_graph_workspace_size(N) bytes; owned by the
+ *                caller; no other call may use it until this one completes.
+ * N up to 2^30 (EQMP_ERR_UNSUPPORTED above).  Asynchronous on `stream`; no
+ * host synchronisation.  Cost is linear in N for bounded density; a row
+ * longer than 512 edges is sorted in time quadratic in its length.
+ */
+size_t eqmp_radius_graph_workspace_size(int64_t N);
+
+eqmp_status eqmp_radius_graph(const float* pos, int64_t N, float cutoff, int32_t* row_offsets,
+                              int32_t* src, float* vec, int32_t* dst, int32_t* rev, int64_t E_cap,
+                              int64_t* E_total, void* workspace, size_t workspace_bytes,
+                              eqmp_stream_t stream);
 
 /*
  * Synchronous check of the graph preconditions on device data:

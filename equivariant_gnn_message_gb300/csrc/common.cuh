@@ -35,6 +35,67 @@ __device__ __forceinline__ unsigned long long global_ns() {
 
 __device__ __forceinline__ void watchdog_trip(int* wd, int code) { atomicCAS(wd, 0, code); }
 
+// ---------------------------------------------------------------- work split
+// Receiver range [x, y) of CTA b out of G, balancing the work
+//   work(r) = (off[r] - off[0]) + alpha * r
+// (edges plus a per-receiver cost in edge units): the range starts at the
+// first r with work(r) >= b T / G and ends at the first r with
+// work(r) >= (b+1) T / G, T = work(N).  Found by a warp-wide 32-ary search:
+// the candidates lo..hi are cut into 32 groups, lane l probes the last
+// candidate of group l (lane 31 probes hi, true by construction), and the
+// first lane whose probe reaches the target names the group that holds the
+// answer; about log32 N dependent loads.  Every warp of a CTA computes the
+// same range.  The interval shrinks every round whatever the offsets hold,
+// so a malformed CSR still ends in a range inside [0, N].
+constexpr int kReceiverCost = 3;  // per-receiver work of the fused kernels, in edges
+
+__device__ __forceinline__ int split_probe(int lo, int hi, int lane) {
+  const long long d = (long long)hi - lo + 1;
+  return lo + (int)(((lane + 1) * d + 31) / 32) - 1;
+}
+
+__device__ __forceinline__ int2 balanced_range(const int* __restrict__ off, int N, int G, int b, int alpha) {
+  const int lane = threadIdx.x & 31;
+  // round 1: the probes of both bounds coincide; off[0] and off[N] load with them
+  const int p1 = split_probe(0, N, lane);
+  const int o_p1 = __ldg(off + p1);
+  const int o0 = __ldg(off), oN = __ldg(off + N);
+  const long long total = (long long)max(oN - o0, 0) + (long long)alpha * N;
+  const long long tgt[2] = {total * b / G, total * (b + 1) / G};
+  int lo[2], hi[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const long long w = (long long)(o_p1 - o0) + (long long)alpha * p1;
+    const unsigned ge = __ballot_sync(0xffffffffu, p1 == N || w >= tgt[k]);
+    const int f = __ffs(ge) - 1;
+    hi[k] = __shfl_sync(0xffffffffu, p1, f);
+    const int prev = __shfl_sync(0xffffffffu, p1, f > 0 ? f - 1 : 0);
+    lo[k] = f == 0 ? 0 : prev + 1;
+  }
+  if (b == 0) lo[0] = hi[0] = 0;
+  if (b == G - 1) lo[1] = hi[1] = N;
+  while (lo[0] < hi[0] || lo[1] < hi[1]) {
+    int p[2], o[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      p[k] = split_probe(lo[k], hi[k], lane);
+      o[k] = lo[k] < hi[k] && p[k] < hi[k] ? __ldg(off + p[k]) : 0;
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      if (lo[k] >= hi[k]) continue;  // warp-uniform
+      const long long w = (long long)(o[k] - o0) + (long long)alpha * p[k];
+      const unsigned ge = __ballot_sync(0xffffffffu, p[k] == hi[k] || w >= tgt[k]);
+      const int f = __ffs(ge) - 1;
+      const int nh = __shfl_sync(0xffffffffu, p[k], f);
+      const int prev = __shfl_sync(0xffffffffu, p[k], f > 0 ? f - 1 : 0);
+      lo[k] = f == 0 ? lo[k] : prev + 1;
+      hi[k] = nh;
+    }
+  }
+  return make_int2(hi[0], max(hi[1], hi[0]));
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -259,10 +259,11 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
   const uint32_t empty0 = full0 + 8 * S;
   const int tid = threadIdx.x;
 
-  // Contiguous receiver range of this CTA (equal receiver counts).
-  const int G = gridDim.x, b = blockIdx.x;
-  const int r_begin = (int)((long long)a.N * b / G);
-  const int r_end = (int)((long long)a.N * (b + 1) / G);
+  // Contiguous receiver range of this CTA, balanced on edges + 3 per
+  // receiver (the contraction and store of a receiver cost about three
+  // edges' accumulation).
+  const int2 rr = balanced_range(a.off, a.N, gridDim.x, blockIdx.x, kReceiverCost);
+  const int r_begin = rr.x, r_end = rr.y;
 
   if (tid < S) {
     mbar_init(full0 + 8 * tid, 1);

@@ -266,9 +266,10 @@ __global__ void __launch_bounds__(So2Cfg<C, XT, RADIAL>::NTHREADS, So2Cfg<C, XT,
   const uint32_t full0 = smem_u32(smem + K::OFF_BAR);
   const uint32_t empty0 = full0 + 8 * S;
   const int tid = threadIdx.x;
-  const int G = gridDim.x, b = blockIdx.x;
-  const int r_begin = (int)((long long)a.N * b / G);
-  const int r_end = (int)((long long)a.N * (b + 1) / G);
+  // Contiguous receiver range, balanced on edges (a receiver's group sum and
+  // store cost about one edge here).
+  const int2 rr = balanced_range(a.off, a.N, gridDim.x, blockIdx.x, 1);
+  const int r_begin = rr.x, r_end = rr.y;
   if (tid < S) {
     mbar_init(full0 + 8 * tid, 1);
     mbar_init(empty0 + 8 * tid, C);  // the C threads of the owning edge group

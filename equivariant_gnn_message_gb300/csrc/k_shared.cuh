@@ -418,41 +418,66 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
   uint32_t n = 0;  // ordinal of the CTA's next edge
   int buf = 0;
   bool failed = false;
-  // Edge m lives in slot m % S, phase (m / S) & 1; its SH in ring entry m % YR.
-  auto full_bar = [&](uint32_t m) { return full0 + 8 * (m % S); };
-  auto full_par = [&](uint32_t m) { return (m / S) & 1u; };
-  auto wait_full = [&](uint32_t m) {
-    if (!mbar_try_wait(full_bar(m), full_par(m)))
-      if (!mbar_wait_slow(full_bar(m), full_par(m), a.watchdog, 1, failed)) failed = true;
+  // Edge m lives in slot m % S, phase (m / S) & 1, with its SH in ring entry
+  // m % YR.  A cursor holds these for one ordinal (full barrier address,
+  // parity, byte offsets of the slot and of the SH entry) and steps to the
+  // next ordinal with a few warp-uniform adds and selects, so the edge loop
+  // never recomputes them from the ordinal.
+  struct Cursor {
+    uint32_t bar, par, xs, ys;
   };
-  auto load_edge = [&](uint32_t m, float2 (&yv)[8], float (&xv)[KQ]) {
-    const float4* yp = ys + 4 * (m % K::YR);
+  auto advance = [&](Cursor& u) {
+    u.bar += 8;
+    u.xs += K::SLOT;
+    u.ys += 64;
+    if (u.bar == full0 + 8 * S) {
+      u.bar = full0;
+      u.xs = K::OFF_X;
+      u.par ^= 1u;
+    }
+    if (u.ys == (uint32_t)(K::OFF_Y + 64 * K::YR)) u.ys = K::OFF_Y;
+  };
+  auto wait_cur = [&](const Cursor& u) {
+    if (!mbar_try_wait(u.bar, u.par))
+      if (!mbar_wait_slow(u.bar, u.par, a.watchdog, 1, failed)) failed = true;
+  };
+  auto load_cur = [&](const Cursor& u, float2 (&yv)[8], float (&xv)[KQ]) {
+    const float4* yp = reinterpret_cast<const float4*>(smem + u.ys);
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
       const float4 t = yp[h];
       yv[2 * h] = make_float2(t.x, t.y);
       yv[2 * h + 1] = make_float2(t.z, t.w);
     }
-    load_x<XT, KQ>(smem + K::OFF_X + (m % S) * K::SLOT, xo, xv);
+    load_x<XT, KQ>(smem + u.xs, xo, xv);
   };
-  // Each consumer thread arrives once its own reads of slot m are done.
-  auto release = [&](uint32_t m) { mbar_arrive(empty0 + 8 * (m % S)); };
-  // One edge: test (non-blocking) that edge m+2 has landed, run the FMAs of
-  // edge m from registers, release m, then (waiting only if the early test
-  // failed) load edge m+2 into the registers just freed.
-  auto step = [&](float2 (&acc)[KQ][8], uint32_t m, float2 (&yv)[8], float (&xv)[KQ]) {
-    const bool ready = mbar_test_wait(full_bar(m + 2), full_par(m + 2));
+  // The look-ahead cursor `la` is two ordinals past the edge being summed.
+  // One edge: test (non-blocking) that the look-ahead edge has landed, run
+  // the FMAs of the edge held in (yv, xv) from registers, release its slot
+  // (every consumer thread arrives on its empty barrier, 8 S bytes past the
+  // full one), then (waiting only if the early test failed) load the
+  // look-ahead edge into the registers just freed and step the cursor.
+  Cursor la = {full0, 0u, (uint32_t)K::OFF_X, (uint32_t)K::OFF_Y};
+  auto step = [&](float2 (&acc)[KQ][8], float2 (&yv)[8], float (&xv)[KQ], uint32_t& bar) {
+    const bool ready = mbar_test_wait(la.bar, la.par);
     fma_edge(acc, yv, xv);
-    release(m);
-    if (!ready) wait_full(m + 2);
-    load_edge(m + 2, yv, xv);
+    mbar_arrive(bar + 8 * S);
+    if (!ready) wait_cur(la);
+    load_cur(la, yv, xv);
+    bar = la.bar;
+    advance(la);
   };
   float2 yA[8], yB[8];
   float xA[KQ], xB[KQ];
-  wait_full(0);
-  load_edge(0, yA, xA);
-  wait_full(1);
-  load_edge(1, yB, xB);
+  uint32_t barA, barB;
+  wait_cur(la);
+  load_cur(la, yA, xA);
+  barA = la.bar;
+  advance(la);
+  wait_cur(la);
+  load_cur(la, yB, xB);
+  barB = la.bar;
+  advance(la);
   for (int r = r_begin; r < r_end; ++r) {
     if (r - chunk == 32) {
       chunk += 32;
@@ -475,19 +500,22 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
     // look-ahead may reach the producer's empty tail edges (never used).
     int j = 0;
     for (; j + 2 <= deg; j += 2, n += 2) {
-      step(acc, n, yA, xA);
-      step(acc, n + 1, yB, xB);
+      step(acc, yA, xA, barA);
+      step(acc, yB, xB, barB);
     }
     if (j < deg) {  // odd degree: edge n from A, then A takes n+1 and B loads n+2
-      const bool ready = mbar_test_wait(full_bar(n + 2), full_par(n + 2));
+      const bool ready = mbar_test_wait(la.bar, la.par);
       fma_edge(acc, yA, xA);
-      release(n);
+      mbar_arrive(barA + 8 * S);
 #pragma unroll
       for (int k = 0; k < 8; ++k) yA[k] = yB[k];
 #pragma unroll
       for (int i = 0; i < KQ; ++i) xA[i] = xB[i];
-      if (!ready) wait_full(n + 2);
-      load_edge(n + 2, yB, xB);
+      barA = barB;
+      if (!ready) wait_cur(la);
+      load_cur(la, yB, xB);
+      barB = la.bar;
+      advance(la);
       ++n;
     }
 

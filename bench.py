@@ -371,7 +371,13 @@ def main():
             d_in[k].copy_(v, non_blocking=True)
         xd = d_in["x"].view(torch.bfloat16) if wl.storage == "bf16" else d_in["x"]
         kw = dict(w=d_in["w"]) if "w" in d_in else dict(R=d_in["R"], M=d_in["M"])
-        eq.eqmp_fused(d_in["vec"], xd, d_in["off"], d_in["src"], out=out, **kw)
+        if args.entry == "so2":
+            eq.eqmp_fused_so2(d_in["vec"], xd, d_in["off"], d_in["src"], out=out, **kw)
+        elif args.entry == "tp_scatter":
+            eq.eqmp_sh(d_in["vec"], Yb)
+            eq.eqmp_tp_scatter(Yb, xd, d_in["off"], d_in["src"], out=out, **kw)
+        else:
+            eq.eqmp_fused(d_in["vec"], xd, d_in["off"], d_in["src"], out=out, **kw)
         h_out.copy_(out, non_blocking=True)
 
     if graph_args is not None:

@@ -12,10 +12,10 @@
 //   k_bin      cell of each atom (cell side = r_c (1 + 2^-10)), hashed into
 //              H = 2^k >= 2N buckets; count atoms per bucket
 //   scan       bucket starts (exclusive prefix sum)
-//   k_scatter  atoms listed bucket by bucket
-//   k_neigh    (count) one thread per receiver, visited in bucket order so
-//              neighbouring threads read the same buckets: test every atom
-//              of the 27 surrounding cells' buckets (each bucket once)
+//   k_scatter  atoms (and a copy of their positions) listed bucket by bucket
+//   k_neigh    (count) one warp per receiver, visited in bucket order so
+//              neighbouring warps read the same buckets: the lanes test the
+//              atoms of the 27 surrounding cells' buckets (each bucket once)
 //   scan       degrees -> row_offsets, E_total
 //   k_neigh    (fill) the same walk writes each receiver's senders, unsorted
 //   k_sort     one warp per receiver: rank sort of its senders, writes
@@ -182,59 +182,91 @@ __global__ void k_bin(const float* __restrict__ pos, int N, float inv, uint32_t 
   atomicAdd(count + h, 1);
 }
 
-__global__ void k_scatter(int N, const int32_t* __restrict__ atom_bucket, const int32_t* __restrict__ start,
-                          int32_t* __restrict__ fill, int32_t* __restrict__ bucket_atoms) {
+// Atoms listed bucket by bucket, with a copy of their positions in the same
+// order, so that the neighbour walk reads candidates' positions contiguously.
+__global__ void k_scatter(const float* __restrict__ pos, int N, const int32_t* __restrict__ atom_bucket,
+                          const int32_t* __restrict__ start, int32_t* __restrict__ fill,
+                          int32_t* __restrict__ bucket_atoms, float4* __restrict__ bucket_pos) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= N) return;
   const int h = atom_bucket[i];
-  bucket_atoms[start[h] + atomicAdd(fill + h, 1)] = i;
+  const int slot = start[h] + atomicAdd(fill + h, 1);
+  bucket_atoms[slot] = i;
+  const float3 p = load_pos(pos, i);
+  bucket_pos[slot] = make_float4(p.x, p.y, p.z, 0.0f);
 }
 
 // ------------------------------------------------------------ neighbour walk
+// One warp per receiver, receivers taken in bucket order so that the warps
+// of a CTA read the same buckets.  Lanes 0..26 each name one of the 27
+// surrounding cells' buckets (a bucket two cells hash to is kept once, by
+// its lowest lane); the warp then walks the concatenation of those buckets,
+// one candidate per lane per round, finding each candidate's bucket by a
+// binary search over the lanes' running sizes.
 // FILL = false: row_offsets[i] = degree of i (row_offsets[N] = 0).
 // FILL = true:  senders of i written, unsorted, to src[off[i] .. off[i+1]).
 template <bool FILL>
-__global__ void __launch_bounds__(kNeighThreads) k_neigh(const float* __restrict__ pos, int N, float inv, float rc2,
-                                                         uint32_t mask, const int32_t* __restrict__ start,
+__global__ void __launch_bounds__(kNeighThreads) k_neigh(const float4* __restrict__ bucket_pos, int N, float inv,
+                                                         float rc2, uint32_t mask, const int32_t* __restrict__ start,
                                                          const int32_t* __restrict__ bucket_atoms,
                                                          int32_t* __restrict__ row_offsets,
                                                          int32_t* __restrict__ src, long long e_cap) {
-  const int t = blockIdx.x * blockDim.x + threadIdx.x;
-  if (!FILL && t == 0) row_offsets[N] = 0;
-  if (t >= N) return;
-  const int i = bucket_atoms[t];
-  const float3 pi = load_pos(pos, i);
-  const int cx = cell_of(pi.x, inv), cy = cell_of(pi.y, inv), cz = cell_of(pi.z, inv);
+  const int lane = threadIdx.x & 31;
+  const long long wg = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (!FILL && wg == 0 && lane == 0) row_offsets[N] = 0;
+  if (wg >= N) return;  // warp-uniform
+  const int i = bucket_atoms[wg];  // the receiver sits at slot wg of the bucket order
+  const float4 pw = bucket_pos[wg];
+  const float3 pi = make_float3(pw.x, pw.y, pw.z);
   long long w = 0, w_end = 0;
   if (FILL) {
     w = row_offsets[i];
     w_end = row_offsets[i + 1];
     if (w < 0 || w_end > e_cap || w_end < w) return;  // row outside the caller's capacity
   }
+  const int cx = cell_of(pi.x, inv), cy = cell_of(pi.y, inv), cz = cell_of(pi.z, inv);
+  const uint32_t h = lane < 27 ? cell_hash(cx + lane % 3 - 1, cy + (lane / 3) % 3 - 1, cz + lane / 9 - 1, mask)
+                               : 0xffffffffu;
+  const unsigned same = __match_any_sync(0xffffffffu, h);
+  const bool keep = lane < 27 && (same & ((1u << lane) - 1u)) == 0u;
+  const int b0 = keep ? start[h] : 0;
+  const int nb = keep ? start[h + 1] - b0 : 0;
+  int incl = nb;  // running size of the buckets of lanes 0..lane
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const int total = __shfl_sync(0xffffffffu, incl, 31);
   int count = 0;
-  uint32_t seen[27];  // fully unrolled below: stays in registers
+  for (int base = 0; base < total; base += 32) {
+    const int t = base + lane;
+    // smallest lane L with incl[L] > t
+    int L = 0;
 #pragma unroll
-  for (int c = 0; c < 27; ++c) {
-    const uint32_t h = cell_hash(cx + c % 3 - 1, cy + (c / 3) % 3 - 1, cz + c / 9 - 1, mask);
-    seen[c] = h;
-    bool dup = false;  // two cells in one bucket: visit the bucket once
-#pragma unroll
-    for (int k = 0; k < c; ++k) dup |= seen[k] == h;
-    if (dup) continue;
-    const int b1 = start[h + 1];
-    for (int s = start[h]; s < b1; ++s) {
-      const int j = bucket_atoms[s];
-      if (j == i) continue;
-      if (dist2(pi, load_pos(pos, j)) < rc2) {
-        if (FILL) {
-          if (w < w_end) src[w++] = j;
-        } else {
-          ++count;
-        }
-      }
+    for (int step = 16; step >= 1; step >>= 1) {
+      const int v = __shfl_sync(0xffffffffu, incl, L + step - 1);
+      if (v <= t) L += step;
+    }
+    L = min(L, 31);
+    const int lb0 = __shfl_sync(0xffffffffu, b0, L);
+    const int lex = __shfl_sync(0xffffffffu, incl - nb, L);
+    bool hit = false;
+    const int slot = lb0 + (t - lex);
+    if (t < total) {
+      const float4 q = bucket_pos[slot];
+      hit = slot != wg && dist2(pi, make_float3(q.x, q.y, q.z)) < rc2;
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, hit);
+    if (FILL) {
+      const long long at = w + __popc(bal & ((1u << lane) - 1u));
+      if (hit && at < w_end) src[at] = bucket_atoms[slot];
+      w += __popc(bal);
+    } else {
+      count += __popc(bal);
     }
   }
-  if (!FILL) row_offsets[i] = count;
+  if (!FILL && lane == 0) row_offsets[i] = count;
 }
 
 // ------------------------------------------------------------ row sort
@@ -322,7 +354,7 @@ __global__ void k_rev(int N, const int32_t* __restrict__ row_offsets, const int3
 // ------------------------------------------------------------ workspace
 struct GraphWs {
   long long H = 0;
-  size_t atom_bucket = 0, start = 0, fill = 0, bucket_atoms = 0, sums = 0, bad = 0, bytes = 0;
+  size_t atom_bucket = 0, start = 0, fill = 0, bucket_atoms = 0, bucket_pos = 0, sums = 0, bad = 0, bytes = 0;
 };
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -339,6 +371,7 @@ GraphWs graph_ws(long long N) {
   w.start = o;       o = align256(o + 4 * (size_t)(H + 1));
   w.fill = o;        o = align256(o + 4 * (size_t)H);
   w.bucket_atoms = o; o = align256(o + 4 * (size_t)N);
+  w.bucket_pos = o;  o = align256(o + 16 * (size_t)N);
   w.sums = o;        o = align256(o + 8 * (size_t)nb);
   w.bad = o;         o = align256(o + 4);
   w.bytes = o;
@@ -375,6 +408,7 @@ eqmp_status eqmp_radius_graph(const float* pos, int64_t N, float cutoff, int32_t
   int32_t* start = reinterpret_cast<int32_t*>(base + w.start);
   int32_t* fill = reinterpret_cast<int32_t*>(base + w.fill);
   int32_t* bucket_atoms = reinterpret_cast<int32_t*>(base + w.bucket_atoms);
+  float4* bucket_pos = reinterpret_cast<float4*>(base + w.bucket_pos);
   long long* sums = reinterpret_cast<long long*>(base + w.sums);
   int* bad = reinterpret_cast<int*>(base + w.bad);
   // start and fill are adjacent: one clear covers both
@@ -392,14 +426,16 @@ eqmp_status eqmp_radius_graph(const float* pos, int64_t N, float cutoff, int32_t
   }
   cudaError_t err = exclusive_scan(start, w.H + 1, sums, bad, nullptr, st);
   if (err != cudaSuccess) return EQMP_ERR_CUDA;
-  if (N > 0) k_scatter<<<nblk, kNeighThreads, 0, st>>>((int)N, atom_bucket, start, fill, bucket_atoms);
-  k_neigh<false><<<nblk > 0 ? nblk : 1, kNeighThreads, 0, st>>>(pos, (int)N, inv, rc2, mask, start, bucket_atoms,
-                                                               row_offsets, nullptr, E_cap);
+  if (N > 0)
+    k_scatter<<<nblk, kNeighThreads, 0, st>>>(pos, (int)N, atom_bucket, start, fill, bucket_atoms, bucket_pos);
+  const long long wblk = (N * 32 + kNeighThreads - 1) / kNeighThreads;  // one warp per receiver
+  k_neigh<false><<<(unsigned)(wblk > 0 ? wblk : 1), kNeighThreads, 0, st>>>(bucket_pos, (int)N, inv, rc2, mask, start,
+                                                                           bucket_atoms, row_offsets, nullptr, E_cap);
   err = exclusive_scan(row_offsets, N + 1, sums, bad, reinterpret_cast<long long*>(E_total), st);
   if (err != cudaSuccess) return EQMP_ERR_CUDA;
   if (N > 0 && E_cap > 0) {
-    k_neigh<true><<<nblk, kNeighThreads, 0, st>>>(pos, (int)N, inv, rc2, mask, start, bucket_atoms, row_offsets, src,
-                                                  E_cap);
+    k_neigh<true><<<(unsigned)wblk, kNeighThreads, 0, st>>>(bucket_pos, (int)N, inv, rc2, mask, start, bucket_atoms,
+                                                            row_offsets, src, E_cap);
     const int sblk = (int)((N + kSortWarps - 1) / kSortWarps);
     k_sort<<<sblk, kSortWarps * 32, 0, st>>>(pos, (int)N, row_offsets, src, vec, dst, E_cap);
     if (rev) k_rev<<<sblk, kSortWarps * 32, 0, st>>>((int)N, row_offsets, src, rev, E_cap);

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(BUILD, "libeqmp.so")
-UNITS = ["abi.cu", "shared_f32.cu", "shared_bf16.cu", "radial.cu", "bwd.cu", "so2.cu", "graph.cu"]
+UNITS = ["abi.cu", "shared_f32.cu", "shared_bf16.cu", "radial.cu", "bwd.cu", "so2.cu", "graph.cu", "shared_dx.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -27,15 +27,52 @@ static long long slots_for(int C, long long N, int sms) {
   return -1;
 }
 
+// Gradient of x with shared weights:
+//   gx[j,c,k1] = sum_p w[p,c] sum_{k3,k2} C_p[k3,k1,k2] B[j,c,k3,k2],
+//   B[j,c,k3,k2] = sum_{e: src_e = j} g[dst_e,c,k3] Y_e[k2],
+// which is the forward layer's schedule (accumulate outer products, then
+// contract once per row) over the sender view, gathering rows of g, with the
+// CG tables transposed.  The fused shared-weight kernel runs it.
+static eqmp_status run_dx_shared(const BwdArgs& b, int C, cudaStream_t st, const DeviceInfo& dev) {
+  if (b.N_src == 0) return EQMP_OK;
+  if (b.N == 0) return cuda_status(cudaMemsetAsync(b.gx, 0, (size_t)b.N_src * C * 16 * 4, st));
+  LayerArgs a{};
+  a.vec = b.vec;
+  a.x = b.g;
+  a.off = b.send_off;
+  a.w = b.w;
+  a.out = b.gx;
+  a.watchdog = dev.watchdog;
+  a.N = b.N_src;
+  a.E = b.n_send;
+  a.N_src = b.N;
+  a.perm = b.send_edges;
+  a.dst = b.dst;
+  a.E_edges = b.E;
+  CUtensorMap map;
+  if (b.n_send > 0) {
+    const eqmp_status s = encode_x_map(b.g, b.N, C, false, &map);
+    if (s != EQMP_OK) return s;
+  } else {
+    memset(&map, 0, sizeof(map));  // never dereferenced: no edge, no load
+  }
+  return launch_shared_dx_f32(a, C, map, st, dev);
+}
+
 template <int C, bool RADIAL>
 static eqmp_status run_bwd(const BwdArgs& a, bool want_x, bool want_wv, float* gw, float* gM, int e0, int e1,
                            cudaStream_t st, const DeviceInfo& dev) {
   using K = BwdCfg<C, RADIAL>;
-  if (want_x && a.N_src > 0) {
-    const long long want = (a.N_src + K::GROUPS - 1) / K::GROUPS;
-    const long long cap = (long long)dev.sms * 16;
-    k_bwd_x<C, RADIAL><<<(int)(want < cap ? want : cap), K::NT, 0, st>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
+  if (!RADIAL && want_x) {
+    const eqmp_status s = run_dx_shared(a, C, st, dev);
+    if (s != EQMP_OK) return s;
+  } else if (want_x && a.N_src > 0) {
+    if constexpr (RADIAL) {  // per-edge weights: one group of lanes per sender
+      const long long want = (a.N_src + K::GROUPS - 1) / K::GROUPS;
+      const long long cap = (long long)dev.sms * 16;
+      k_bwd_x<C, RADIAL><<<(int)(want < cap ? want : cap), K::NT, 0, st>>>(a);
+      if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
+    }
   }
   if (want_wv && a.N > 0) {
     const int grid = (int)(bwd_slots<C>(a.N, dev.sms) / K::GROUPS);
@@ -187,11 +224,16 @@ template <int C, bool RADIAL>
 static eqmp_status run_bwd_noalloc(const BwdArgs& a, bool want_x, bool want_wv, float* gw, float* gM, int e0,
                                    int e1, cudaStream_t st, const DeviceInfo& dev) {
   using K = BwdCfg<C, RADIAL>;
-  if (want_x && a.N_src > 0) {
-    const long long want = (a.N_src + K::GROUPS - 1) / K::GROUPS;
-    const long long cap = (long long)dev.sms * 16;
-    k_bwd_x<C, RADIAL><<<(int)(want < cap ? want : cap), K::NT, 0, st>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
+  if (!RADIAL && want_x) {
+    const eqmp_status s = run_dx_shared(a, C, st, dev);
+    if (s != EQMP_OK) return s;
+  } else if (want_x && a.N_src > 0) {
+    if constexpr (RADIAL) {  // per-edge weights: one group of lanes per sender
+      const long long want = (a.N_src + K::GROUPS - 1) / K::GROUPS;
+      const long long cap = (long long)dev.sms * 16;
+      k_bwd_x<C, RADIAL><<<(int)(want < cap ? want : cap), K::NT, 0, st>>>(a);
+      if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
+    }
   }
   if (want_wv && a.N > 0) {
     // as many receiver groups as the static scratch holds partial rows for

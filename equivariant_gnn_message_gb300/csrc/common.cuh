@@ -285,4 +285,32 @@ constexpr bool path_touches(int P, int k1lo, int n) {
   return false;
 }
 
+// The same tables with the roles of k1 and k3 exchanged (T = true): the
+// transposed product sum_{k3,k2} C_p[k3,k1,k2] g[k3] Y[k2] -> out[k1] that
+// the gradient of x needs.  Same paths, same coefficients.
+template <bool T>
+constexpr tables::Term term_t(int i) {
+  tables::Term t = tables::kTerms[i];
+  if (T) {
+    const int k = t.k1;
+    t.k1 = t.k3;
+    t.k3 = k;
+  }
+  return t;
+}
+
+template <bool T>
+constexpr bool path_has_t(int P, int k1lo, int n, int k3) {
+  for (int i = tables::kPaths[P].first; i < tables::kPaths[P].first + tables::kPaths[P].count; ++i)
+    if (term_t<T>(i).k3 == k3 && term_t<T>(i).k1 >= k1lo && term_t<T>(i).k1 < k1lo + n) return true;
+  return false;
+}
+
+template <bool T>
+constexpr bool path_touches_t(int P, int k1lo, int n) {
+  for (int k3 = 0; k3 < 16; ++k3)
+    if (path_has_t<T>(P, k1lo, n, k3)) return true;
+  return false;
+}
+
 }  // namespace eqmp

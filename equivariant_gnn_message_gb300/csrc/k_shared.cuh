@@ -126,9 +126,9 @@ __device__ __forceinline__ uint32_t swz128(uint32_t o) {
 }
 
 // ---- compile-time contraction: partial outputs of quad Q -----------------
-template <int KQ, int Q, int I>
+template <int KQ, int Q, int I, bool T>
 __device__ __forceinline__ void apply_term(const float2 (&acc)[KQ][8], float (&tmp)[16]) {
-  constexpr tables::Term t = term_at(I);
+  constexpr tables::Term t = term_t<T>(I);
   if constexpr (t.k1 >= Q * KQ && t.k1 < Q * KQ + KQ) {
     constexpr int i = t.k1 - Q * KQ;
     const float a = (t.k2 & 1) ? acc[i][t.k2 >> 1].y : acc[i][t.k2 >> 1].x;
@@ -136,52 +136,53 @@ __device__ __forceinline__ void apply_term(const float2 (&acc)[KQ][8], float (&t
   }
 }
 
-template <int KQ, int Q, int First, int... Is>
+template <int KQ, int Q, int First, bool T, int... Is>
 __device__ __forceinline__ void apply_terms(const float2 (&acc)[KQ][8], float (&tmp)[16],
                                             std::integer_sequence<int, Is...>) {
-  (apply_term<KQ, Q, First + Is>(acc, tmp), ...);
+  (apply_term<KQ, Q, First + Is, T>(acc, tmp), ...);
 }
 
-template <int KQ, int Q, int P, int... K3>
+template <int KQ, int Q, int P, bool T, int... K3>
 __device__ __forceinline__ void weight_outputs(float w, const float (&tmp)[16], float (&part)[16],
                                                std::integer_sequence<int, K3...>) {
-  ((path_has(P, Q * KQ, KQ, K3) ? (void)(part[K3] = fmaf(w, tmp[K3], part[K3])) : (void)0), ...);
+  ((path_has_t<T>(P, Q * KQ, KQ, K3) ? (void)(part[K3] = fmaf(w, tmp[K3], part[K3])) : (void)0), ...);
 }
 
-template <int C, int KQ, int Q, int P>
+template <int C, int KQ, int Q, int P, bool T>
 __device__ __forceinline__ void contract_path(const float2 (&acc)[KQ][8], const float* wcol,
                                               float (&part)[16]) {
-  if constexpr (path_touches(P, Q * KQ, KQ)) {
+  if constexpr (path_touches_t<T>(P, Q * KQ, KQ)) {
     constexpr tables::Path path = path_at(P);
     float tmp[16];
 #pragma unroll
     for (int k = 0; k < 16; ++k) tmp[k] = 0.0f;
-    apply_terms<KQ, Q, path.first>(acc, tmp, std::make_integer_sequence<int, path.count>{});
+    apply_terms<KQ, Q, path.first, T>(acc, tmp, std::make_integer_sequence<int, path.count>{});
     const float w = wcol[P * C];
-    weight_outputs<KQ, Q, P>(w, tmp, part, std::make_integer_sequence<int, 16>{});
+    weight_outputs<KQ, Q, P, T>(w, tmp, part, std::make_integer_sequence<int, 16>{});
   }
 }
 
-template <int C, int KQ, int Q, int... Ps>
+template <int C, int KQ, int Q, bool T, int... Ps>
 __device__ __forceinline__ void contract_quad(const float2 (&acc)[KQ][8], const float* wcol,
                                               float (&part)[16], std::integer_sequence<int, Ps...>) {
-  (contract_path<C, KQ, Q, Ps>(acc, wcol, part), ...);
+  (contract_path<C, KQ, Q, Ps, T>(acc, wcol, part), ...);
 }
 
-template <int C, int KQ>
+// T = true contracts with the transposed tables (gradient of x).
+template <int C, int KQ, bool T>
 __device__ __forceinline__ void contract(int q, const float2 (&acc)[KQ][8], const float* wcol,
                                          float (&part)[16]) {
   using Seq = std::make_integer_sequence<int, tables::kNumPaths>;
   if constexpr (KQ == 4) {
     switch (q) {
-      case 0: contract_quad<C, KQ, 0>(acc, wcol, part, Seq{}); break;
-      case 1: contract_quad<C, KQ, 1>(acc, wcol, part, Seq{}); break;
-      case 2: contract_quad<C, KQ, 2>(acc, wcol, part, Seq{}); break;
-      default: contract_quad<C, KQ, 3>(acc, wcol, part, Seq{}); break;
+      case 0: contract_quad<C, KQ, 0, T>(acc, wcol, part, Seq{}); break;
+      case 1: contract_quad<C, KQ, 1, T>(acc, wcol, part, Seq{}); break;
+      case 2: contract_quad<C, KQ, 2, T>(acc, wcol, part, Seq{}); break;
+      default: contract_quad<C, KQ, 3, T>(acc, wcol, part, Seq{}); break;
     }
   } else {
-    if (q == 0) contract_quad<C, KQ, 0>(acc, wcol, part, Seq{});
-    else contract_quad<C, KQ, 1>(acc, wcol, part, Seq{});
+    if (q == 0) contract_quad<C, KQ, 0, T>(acc, wcol, part, Seq{});
+    else contract_quad<C, KQ, 1, T>(acc, wcol, part, Seq{});
   }
 }
 
@@ -243,10 +244,14 @@ __device__ __forceinline__ void store_out(void* out, size_t elem, const float (&
   }
 }
 
-template <int C, int KQ, typename XT, bool FROM_VEC>
+// TRANS = true: the transposed walk of the gradient of x (rows are senders,
+// edges come through a.perm, rows gathered from the upstream gradient by
+// the edge's receiver, contraction with the transposed tables).
+template <int C, int KQ, typename XT, bool FROM_VEC, bool TRANS>
 __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
                                   SharedCfg<C, KQ, XT, FROM_VEC>::MIN_BLOCKS)
     k_shared(const __grid_constant__ CUtensorMap tmap, const LayerArgs a) {
+  static_assert(!TRANS || FROM_VEC, "the transposed walk computes the harmonics");
   using K = SharedCfg<C, KQ, XT, FROM_VEC>;
   constexpr int S = K::S;
   extern __shared__ uint8_t smem_raw[];
@@ -307,8 +312,17 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
     auto load_edge = [&](uint32_t n, int& node, float& vx, float& vy, float& vz) {
       node = 0; vx = vy = vz = 0.0f;
       if (n < (uint32_t)total) {
-        const int e = e_begin + (int)n;
-        node = __ldg(a.src + e);
+        int e = e_begin + (int)n;
+        if constexpr (TRANS) {
+          e = __ldg(a.perm + e);
+          if ((unsigned)e >= (unsigned)a.E_edges) {
+            node = -1;  // a bad edge id gathers the zero fill and adds nothing
+            return;
+          }
+          node = __ldg(a.dst + e);
+        } else {
+          node = __ldg(a.src + e);
+        }
         if constexpr (FROM_VEC) {
           const float* v = a.vec + 3 * (size_t)e;
           vx = __ldg(v); vy = __ldg(v + 1); vz = __ldg(v + 2);
@@ -522,7 +536,7 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
     float part[16];
 #pragma unroll
     for (int k = 0; k < 16; ++k) part[k] = 0.0f;
-    contract<C, KQ>(q, acc, wcol, part);
+    contract<C, KQ, TRANS>(q, acc, wcol, part);
 
     float* rb = red + buf * (K::NQ * 16 * C);
 #pragma unroll

@@ -26,6 +26,10 @@ eqmp_status launch_shared_f32(const LayerArgs& a, int C, bool from_vec, const CU
                               cudaStream_t st, const DeviceInfo& dev);
 eqmp_status launch_shared_bf16(const LayerArgs& a, int C, bool from_vec, const CUtensorMap& map,
                                cudaStream_t st, const DeviceInfo& dev);
+// Gradient of x, shared weights: LayerArgs of the transposed walk (rows =
+// senders through perm/dst, x = upstream gradient, map over its rows).
+eqmp_status launch_shared_dx_f32(const LayerArgs& a, int C, const CUtensorMap& map, cudaStream_t st,
+                                 const DeviceInfo& dev);
 eqmp_status launch_radial_f32(const LayerArgs& a, int C, bool from_vec, cudaStream_t st,
                               const DeviceInfo& dev);
 eqmp_status launch_radial_bf16(const LayerArgs& a, int C, bool from_vec, cudaStream_t st,

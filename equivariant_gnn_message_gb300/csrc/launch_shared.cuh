@@ -6,11 +6,11 @@
 
 namespace eqmp {
 
-template <int C, int KQ, typename XT, bool FV>
+template <int C, int KQ, typename XT, bool FV, bool TRANS = false>
 eqmp_status launch_shared_t(const LayerArgs& a, const CUtensorMap& map, cudaStream_t st,
                             const DeviceInfo& dev) {
   using K = SharedCfg<C, KQ, XT, FV>;
-  auto kern = k_shared<C, KQ, XT, FV>;
+  auto kern = k_shared<C, KQ, XT, FV, TRANS>;
   static unsigned long long attr_done = 0;
   static int occ_cache[64] = {0};
   cudaError_t err = ensure_smem_attr(kern, K::SMEM_BYTES, &attr_done);
@@ -41,15 +41,15 @@ eqmp_status launch_shared_t(const LayerArgs& a, const CUtensorMap& map, cudaStre
 }
 
 // KQ per channel count and storage comes from SharedTune (k_shared.cuh).
-template <typename XT, bool FV>
+template <typename XT, bool FV, bool TRANS = false>
 eqmp_status launch_shared_c(const LayerArgs& a, int C, const CUtensorMap& map, cudaStream_t st,
                             const DeviceInfo& dev) {
   switch (C) {
-    case 8: return launch_shared_t<8, SharedTune<8, XT>::KQ, XT, FV>(a, map, st, dev);
-    case 16: return launch_shared_t<16, SharedTune<16, XT>::KQ, XT, FV>(a, map, st, dev);
-    case 32: return launch_shared_t<32, SharedTune<32, XT>::KQ, XT, FV>(a, map, st, dev);
-    case 64: return launch_shared_t<64, SharedTune<64, XT>::KQ, XT, FV>(a, map, st, dev);
-    case 128: return launch_shared_t<128, SharedTune<128, XT>::KQ, XT, FV>(a, map, st, dev);
+    case 8: return launch_shared_t<8, SharedTune<8, XT>::KQ, XT, FV, TRANS>(a, map, st, dev);
+    case 16: return launch_shared_t<16, SharedTune<16, XT>::KQ, XT, FV, TRANS>(a, map, st, dev);
+    case 32: return launch_shared_t<32, SharedTune<32, XT>::KQ, XT, FV, TRANS>(a, map, st, dev);
+    case 64: return launch_shared_t<64, SharedTune<64, XT>::KQ, XT, FV, TRANS>(a, map, st, dev);
+    case 128: return launch_shared_t<128, SharedTune<128, XT>::KQ, XT, FV, TRANS>(a, map, st, dev);
     default: return EQMP_ERR_UNSUPPORTED;
   }
 }

@@ -18,6 +18,13 @@ struct LayerArgs {
   int N;                  // receivers
   int E;                  // edges in vec / Y / src / R
   int N_src;              // rows of x
+  // Transposed pass (gradient of x): row r of the walk is sender r; its
+  // edges are perm[off[r] .. off[r+1]) (edge ids), each gathering the row
+  // x[dst[e]] with the harmonics of vec[e].  E counts perm; E_edges counts
+  // the edge arrays vec and dst.
+  const int32_t* perm;    // [E] edge ids, or nullptr
+  const int32_t* dst;     // [E_edges] receiver of each edge, or nullptr
+  int E_edges;
 };
 
 __host__ __device__ constexpr int round_up(int v, int m) { return (v + m - 1) / m * m; }

@@ -19,6 +19,11 @@ Modules
   graph  the radius graph (ordered pairs closer than the cutoff, CSR by
          receiver), with the cutoff decision taken in float32.
 
+sh, cg and layer take the degree as a parameter (l_max = 3 by default, the
+Batmobile layer; l_max = 4..6 for the higher-degree variant the blog lists
+as future work); the layer reads it from the feature array's last axis,
+(l_max+1)^2 components.
+
 Sources (web pages on the Batmobile kernels and on E2Former-V2):
   * "Batmobile CUDA内核优化：等变图神经网络的10-20倍加速策略" (blog post),
     sections "1. 编译时常量", "2. 寄存器中间计算", "3. 操作融合".

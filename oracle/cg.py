@@ -36,12 +36,13 @@ import numpy as np
 L_MAX = 3
 
 
-def paths():
-    """The 34 triangle-allowed (l1, l2, l3), lexicographic."""
+def paths(l_max: int = L_MAX):
+    """The triangle-allowed (l1, l2, l3), all <= l_max, lexicographic
+    (34 for l_max = 3)."""
     out = []
-    for l1 in range(L_MAX + 1):
-        for l2 in range(L_MAX + 1):
-            for l3 in range(abs(l1 - l2), min(L_MAX, l1 + l2) + 1):
+    for l1 in range(l_max + 1):
+        for l2 in range(l_max + 1):
+            for l3 in range(abs(l1 - l2), min(l_max, l1 + l2) + 1):
                 out.append((l1, l2, l3))
     return out
 
@@ -124,6 +125,6 @@ def real_cg_block(l1, l2, l3) -> np.ndarray:
     return out
 
 
-def real_cg_tables():
-    """[(l1, l2, l3, C^R block)] for all 34 paths in order."""
-    return [(l1, l2, l3, real_cg_block(l1, l2, l3)) for (l1, l2, l3) in paths()]
+def real_cg_tables(l_max: int = L_MAX):
+    """[(l1, l2, l3, C^R block)] for all paths (34 for l_max = 3) in order."""
+    return [(l1, l2, l3, real_cg_block(l1, l2, l3)) for (l1, l2, l3) in paths(l_max)]

@@ -40,15 +40,29 @@ def edge_weights(p_index, C, edges, w=None, R=None, M=None):
     return Rm @ Mp
 
 
+def _l_max(x):
+    """Degree of a feature array [.., C, (l_max+1)^2]."""
+    n = int(np.asarray(x).shape[-1])
+    l_max = int(round(np.sqrt(n))) - 1
+    if (l_max + 1) ** 2 != n:
+        raise ValueError(f"{n} components is not (l_max+1)^2")
+    return l_max
+
+
 def edge_messages(vec, x, src, edges, w=None, R=None, M=None):
-    """m[e, c, 16] for the listed edge indices (definition, per path)."""
+    """m[e, c, (l_max+1)^2] for the listed edge indices (definition, per path).
+
+    The degree comes from x's last axis: 16 components is the l <= 3 layer;
+    (l_max+1)^2 components the same layer over all paths with l <= l_max.
+    """
     x = np.asarray(x, np.float64)
     C = x.shape[1]
+    l_max = _l_max(x)
     edges = np.asarray(edges, dtype=np.int64)
-    Y = _sh.real_sh(np.asarray(vec, np.float64)[edges])          # [e, 16]
-    xs = x[np.asarray(src)[edges]]                                # [e, C, 16]
-    msg = np.zeros((len(edges), C, N_SH))
-    for p, (l1, l2, l3, cr) in enumerate(_cg.real_cg_tables()):
+    Y = _sh.real_sh(np.asarray(vec, np.float64)[edges], l_max)   # [e, (l_max+1)^2]
+    xs = x[np.asarray(src)[edges]]                                # [e, C, (l_max+1)^2]
+    msg = np.zeros((len(edges), C, x.shape[2]))
+    for p, (l1, l2, l3, cr) in enumerate(_cg.real_cg_tables(l_max)):
         t = np.einsum("kab,eca,eb->eck", cr, xs[:, :, _block(l1)],
                       Y[:, _block(l2)], optimize=True)
         msg[:, :, _block(l3)] += edge_weights(p, C, edges, w, R, M)[:, :, None] * t
@@ -57,7 +71,8 @@ def edge_messages(vec, x, src, edges, w=None, R=None, M=None):
 
 def message_pass(vec, x, off, src, w=None, R=None, M=None, receivers=None,
                  chunk_edges=200_000):
-    """out[len(receivers), C, 16] (float64) for the chosen receivers.
+    """out[len(receivers), C, (l_max+1)^2] (float64) for the chosen receivers
+    (16 components for the l <= 3 layer).
 
     ``receivers`` defaults to all N = len(off) - 1.  Receivers are
     evaluated a group at a time (at most ``chunk_edges`` edges per group)
@@ -72,7 +87,7 @@ def message_pass(vec, x, off, src, w=None, R=None, M=None, receivers=None,
     if receivers is None:
         receivers = np.arange(len(off) - 1)
     receivers = np.asarray(receivers, dtype=np.int64)
-    out = np.zeros((len(receivers), C, N_SH))
+    out = np.zeros((len(receivers), C, x.shape[2]))
     start = 0
     while start < len(receivers):
         stop, n_e = start, 0

@@ -19,7 +19,8 @@ Definition followed
   (1-z^2)^(m/2) e^(i m phi) = (x + i y)^m, so everything is a polynomial in
   the unit vector (x, y, z).
 
-Layout: component index k = l*l + l + m, m = -l..l (16 components).
+Layout: component index k = l*l + l + m, m = -l..l (16 components for
+l <= 3; (l_max+1)^2 in general).
 
 Zero-length vectors (not produced by the graph generator) are given n = 0,
 so Y_00 is the constant and every l >= 1 component is 0: defined, never NaN.
@@ -59,13 +60,18 @@ def unit_vectors(vec: np.ndarray) -> np.ndarray:
     return out
 
 
-def real_sh(vec: np.ndarray) -> np.ndarray:
-    """Y[E, 16] for edge vectors vec[E, 3] (need not be unit length)."""
+def real_sh(vec: np.ndarray, l_max: int = L_MAX) -> np.ndarray:
+    """Y[E, (l_max+1)^2] for edge vectors vec[E, 3] (need not be unit length).
+
+    The same definition for every degree; l_max = 3 (16 components) is the
+    Batmobile layer, larger l_max the higher-degree variant that the blog
+    names as its limitation (section on limits and future work).
+    """
     n = unit_vectors(vec)
     x, y, z = n[:, 0], n[:, 1], n[:, 2]
     xy = x + 1j * y
-    out = np.zeros((n.shape[0], N_SH), dtype=np.float64)
-    for l in range(L_MAX + 1):
+    out = np.zeros((n.shape[0], (l_max + 1) ** 2), dtype=np.float64)
+    for l in range(l_max + 1):
         pl = legendre_polynomial(l)
         for m in range(0, l + 1):
             # P_l^m(z) (1-z^2)^(-m/2) = (-1)^m d^m P_l / dz^m

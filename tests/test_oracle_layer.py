@@ -127,7 +127,7 @@ def test_planted_dropped_term_fails_brute_force(monkeypatch):
     bad[tuple(idx)] = 0.0
     planted = list(tables)
     planted[23] = (l1, l2, l3, bad)
-    monkeypatch.setattr(cg, "real_cg_tables", lambda: planted)
+    monkeypatch.setattr(cg, "real_cg_tables", lambda l_max=3: planted)
     got = layer.message_pass(vec, x, off, src, w=w)
     assert not np.allclose(got, want, atol=1e-9)
 

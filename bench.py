@@ -64,10 +64,30 @@ def fma_count(wl):
     return ((611 + 156 + 272) * C + 611) * E
 
 
+def sum_rot(l_max):
+    """FMAs of one rotation of all blocks l = 1..l_max: sum (2l+1)^2."""
+    return sum((2 * l + 1) ** 2 for l in range(1, l_max + 1))
+
+
+def aligned_fma_count(wl, l_max, n_terms):
+    """FMAs of the aligned-frame schedule at degree l_max (per launch):
+    rotate in and out (2 sum (2l+1)^2), one FMA per aligned term, and for
+    radial weights 8 per path; per edge and channel."""
+    from equivariant_gnn_message_gb300.inputs import n_paths
+
+    per = 2 * sum_rot(l_max) + n_terms + (8 * n_paths(l_max) if wl.w is None else 0)
+    return per * wl.channels * wl.n_edges
+
+
+# aligned-frame terms per degree (one per output order and path with m2 = 0)
+ALIGNED_TERMS = {4: 272, 5: 565, 6: 1036}
+
+
 def compulsory_bytes(wl):
     s = 2 if wl.storage == "bf16" else 4
     C, E, N = wl.channels, wl.n_edges, wl.n_atoms
-    b = N * C * 16 * s + 12 * E + 4 * E + 4 * (N + 1) + N * C * 16 * s
+    nc = wl.x.shape[2]
+    b = N * C * nc * s + 12 * E + 4 * E + 4 * (N + 1) + N * C * nc * s
     b += 4 * 34 * C if wl.w is not None else 32 * E + 4 * 8 * 34 * C
     return b
 
@@ -130,11 +150,11 @@ class ClockSampler:
 
 def _oracle_chunk(args):
     """Child-process worker: oracle on a receiver subset (single-threaded BLAS)."""
-    name, receivers = args
+    name, receivers, l_max = args
     from equivariant_gnn_message_gb300.inputs import make_workload
     from oracle import layer
 
-    wl = make_workload(name)
+    wl = make_workload(name, l_max=l_max)
     kw = dict(w=wl.w) if wl.w is not None else dict(R=wl.R, M=wl.M)
     t = time.perf_counter()
     layer.message_pass(wl.vec, wl.x, wl.off, wl.src, receivers=np.asarray(receivers), **kw)
@@ -183,7 +203,8 @@ def cpu_oracle_rate(name, wl, seconds_target=12.0, pool=None, cores=1):
         parts = np.array_split(receivers, cores)
         # each worker times its own oracle call (graph generation excluded);
         # the parallel wall time is the slowest worker's
-        wall = max(pool.map(_oracle_chunk, [(name, p.tolist()) for p in parts if len(p)]))
+        l_max = int(round(np.sqrt(wl.x.shape[2]))) - 1
+        wall = max(pool.map(_oracle_chunk, [(name, p.tolist(), l_max) for p in parts if len(p)]))
     else:
         layer.message_pass(wl.vec, wl.x, wl.off, wl.src, receivers=receivers, **kw)
         wall = time.perf_counter() - t
@@ -234,6 +255,8 @@ def main():
     ap.add_argument("--workload", default="pages_1k_c32")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--entry", default="fused", choices=["fused", "tp_scatter", "so2"])
+    ap.add_argument("--lmax", type=int, default=3,
+                    help="4..6: the higher-degree layer (eqmp_fused_lmax) on the workload's graph")
     ap.add_argument("--pass", dest="which", default="forward", choices=["forward", "backward", "graph"],
                     help="backward: time eqmp_fused_backward (dx, dw or dR/dM, dvec) instead; "
                          "graph: time eqmp_radius_graph on the workload's atom positions")
@@ -243,7 +266,9 @@ def main():
     from equivariant_gnn_message_gb300.inputs import make_workload
     from equivariant_gnn_message_gb300.sharding import max_over_ranks
 
-    wl = make_workload(args.workload)
+    wl = make_workload(args.workload, l_max=args.lmax)
+    if args.lmax != 3 and (args.which != "forward" or wl.storage != "f32"):
+        raise SystemExit("--lmax: forward pass on fp32 workloads only")
     if args.impl == "reference":
         run_reference(args, wl)
         return
@@ -314,8 +339,13 @@ def main():
                       g_vec.data_ptr(), None, None, g_cap, g_E.data_ptr(), g_ws.data_ptr(), g_ws.numel(),
                       stream.cuda_stream)
 
+    if args.lmax != 3:
+        out = torch.empty((wl.n_atoms, wl.channels, (args.lmax + 1) ** 2), dtype=torch.float32, device=dev)
+
     def step():
-        if graph_args is not None:
+        if args.lmax != 3:
+            eq.eqmp_fused_lmax(args.lmax, vec, x, off, src, out=out, **wkw)
+        elif graph_args is not None:
             lib.eqmp_radius_graph(*graph_args)
         elif bwd_args is not None:
             eq.eqmp_fused_backward(*bwd_args[0], **bwd_args[1])
@@ -371,7 +401,9 @@ def main():
             d_in[k].copy_(v, non_blocking=True)
         xd = d_in["x"].view(torch.bfloat16) if wl.storage == "bf16" else d_in["x"]
         kw = dict(w=d_in["w"]) if "w" in d_in else dict(R=d_in["R"], M=d_in["M"])
-        if args.entry == "so2":
+        if args.lmax != 3:
+            eq.eqmp_fused_lmax(args.lmax, d_in["vec"], xd, d_in["off"], d_in["src"], out=out, **kw)
+        elif args.entry == "so2":
             eq.eqmp_fused_so2(d_in["vec"], xd, d_in["off"], d_in["src"], out=out, **kw)
         elif args.entry == "tp_scatter":
             eq.eqmp_sh(d_in["vec"], Yb)
@@ -424,8 +456,12 @@ def main():
     # backward: three forward-sized contractions (dx, the weight gradient,
     # dY) of the lowest-FMA schedule plus the SH Jacobian (48 FMA per edge)
     flops = 2.0 * fma_count(wl) if bwd_args is None else 2.0 * (3 * fma_count(wl) + 48 * wl.n_edges)
+    if args.lmax != 3:
+        flops = 2.0 * aligned_fma_count(wl, args.lmax, ALIGNED_TERMS[args.lmax])
     achieved = flops / (ms * 1e-3) / 1e12
     version = KERNEL_VERSION["shared" if wl.w is not None else "radial"] if bwd_args is None else "k_bwd-v1"
+    if args.lmax != 3:
+        version = f"k_hl<{args.lmax}>-v1"
     traffic = NCU_TRAFFIC.get((args.workload, version)) if args.entry == "fused" else None
     n_edges = wl.n_edges if graph_args is None else E_graph
     value = n_edges * world / (ms * 1e-3)
@@ -473,8 +509,9 @@ def main():
             "value": n_edges * world / (e2e_ms * 1e-3), "unit": "edges/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "pass": args.which,
+        "l_max": args.lmax,
         "graph_edges": None if graph_args is None else E_graph,
-        "gpu_launches": args.steps * (12 if graph_args is not None else
+        "gpu_launches": args.steps * (1 if args.lmax != 3 else 12 if graph_args is not None else
                                       (2 if args.entry == "tp_scatter" else 1) if bwd_args is None else 3),
         "clocks": clocks,
         "kernel_ms": {"min": float(np.min(kernel_ms)), "median": float(np.median(kernel_ms))},

@@ -18,6 +18,7 @@ Entry points (same names as the C ABI):
                                                 -> dict of gradients
   eqmp_fused_backward_noalloc(...)              -> the same, no workspace
   eqmp_radius_graph(pos, cutoff)                -> (dict(off, src, vec[, dst, rev]), E)
+  eqmp_fused_lmax(l_max, vec, x, row_offsets, src, ...) -> out, degree 4..6
   eqmp_path_table()                             -> list of (l1, l2, l3)
 """
 import ctypes
@@ -26,7 +27,8 @@ import os
 __all__ = [
     "EqmpError", "load_library", "library_path", "eqmp_num_paths", "eqmp_path_table",
     "eqmp_status_string", "eqmp_sh", "eqmp_tp_scatter", "eqmp_fused", "eqmp_fused_so2", "eqmp_validate_graph",
-    "eqmp_device_error", "eqmp_fused_backward", "eqmp_fused_backward_noalloc", "eqmp_radius_graph", "sender_view", "EQMP_OK", "EQMP_ERR_INVALID_ARG", "EQMP_ERR_UNSUPPORTED",
+    "eqmp_device_error", "eqmp_fused_backward", "eqmp_fused_backward_noalloc", "eqmp_radius_graph", "eqmp_fused_lmax",
+    "eqmp_num_paths_lmax", "sender_view", "EQMP_OK", "EQMP_ERR_INVALID_ARG", "EQMP_ERR_UNSUPPORTED",
     "EQMP_ERR_CUDA", "EQMP_ERR_DEVICE_TIMEOUT", "EQMP_ERR_GRAPH",
 ]
 
@@ -87,6 +89,10 @@ def load_library():
     lib.eqmp_fused_backward.argtypes = [vp, vp, i64, vp, vp, vp, vp, vp, i64, i64, i64, i32, Weights,
                                         vp, vp, vp, vp, vp, vp, vp, i64, vp]
     lib.eqmp_fused_backward.restype = i32
+    lib.eqmp_num_paths_lmax.argtypes = [i32]
+    lib.eqmp_num_paths_lmax.restype = i32
+    lib.eqmp_fused_lmax.argtypes = [i32, vp, vp, i64, vp, vp, i64, i64, i32, Weights, vp, vp]
+    lib.eqmp_fused_lmax.restype = i32
     lib.eqmp_radius_graph_workspace_size.argtypes = [i64]
     lib.eqmp_radius_graph_workspace_size.restype = ctypes.c_size_t
     lib.eqmp_radius_graph.argtypes = [vp, i64, ctypes.c_float, vp, vp, vp, vp, vp, i64, vp, vp,
@@ -240,6 +246,41 @@ def eqmp_device_error():
     if st not in (EQMP_OK, EQMP_ERR_DEVICE_TIMEOUT):
         _check(st, "eqmp_device_error")
     return int(code.value)
+
+
+def eqmp_num_paths_lmax(l_max):
+    return int(load_library().eqmp_num_paths_lmax(int(l_max)))
+
+
+def eqmp_fused_lmax(l_max, vec, x, row_offsets, src, w=None, R=None, M=None, out=None, stream=None):
+    """The layer at degree l_max = 4..6: x [N_src, C, (l_max+1)^2] fp32 -> out [N, C, (l_max+1)^2]."""
+    import torch
+
+    l_max = int(l_max)
+    nc = (l_max + 1) ** 2
+    for name, t in (("vec", vec), ("x", x), ("w", w), ("R", R), ("M", M)):
+        _require(t, name, torch.float32)
+    _require(row_offsets, "row_offsets", torch.int32)
+    _require(src, "src", torch.int32)
+    if x.dim() != 3 or x.shape[2] != nc:
+        raise ValueError(f"x must be [N_src, C, {nc}]")
+    n_src, C = x.shape[0], x.shape[1]
+    N = row_offsets.shape[0] - 1
+    if out is None:
+        out = torch.empty((N, C, nc), dtype=torch.float32, device=x.device)
+    _require(out, "out", torch.float32)
+    if tuple(out.shape) != (N, C, nc):
+        raise ValueError(f"out must be [N, C, {nc}]")
+    if w is not None:
+        wt = Weights(ctypes.c_void_p(w.data_ptr()), None, None, 0)
+    else:
+        wt = Weights(None, ctypes.c_void_p(R.data_ptr()) if R is not None else None,
+                     ctypes.c_void_p(M.data_ptr()) if M is not None else None,
+                     R.shape[1] if R is not None and R.dim() == 2 else 0)
+    st = load_library().eqmp_fused_lmax(l_max, _ptr(vec), _ptr(x), n_src, _ptr(row_offsets), _ptr(src), N,
+                                        vec.shape[0], C, wt, _ptr(out), _stream(stream))
+    _check(st, "eqmp_fused_lmax")
+    return out
 
 
 def eqmp_radius_graph(pos, cutoff, e_cap=None, dst=False, rev=False, stream=None):

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(BUILD, "libeqmp.so")
-UNITS = ["abi.cu", "shared_f32.cu", "shared_bf16.cu", "radial.cu", "bwd.cu", "so2.cu", "graph.cu", "shared_dx.cu"]
+UNITS = ["abi.cu", "shared_f32.cu", "shared_bf16.cu", "radial.cu", "bwd.cu", "so2.cu", "graph.cu", "shared_dx.cu", "hl.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -45,6 +45,8 @@ def generate_tables():
     os.makedirs(BUILD, exist_ok=True)
     out = os.path.join(BUILD, "eqmp_tables.h")
     subprocess.check_call([sys.executable, os.path.join(CSRC, "gen_tables.py"), out])
+    subprocess.check_call([sys.executable, os.path.join(CSRC, "gen_tables.py"), "--high",
+                           os.path.join(BUILD, "eqmp_tables_hl.h")])
     return out
 
 

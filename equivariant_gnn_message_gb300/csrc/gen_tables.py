@@ -95,9 +95,9 @@ def real_cg(l1, l2, l3):
     return out
 
 
-def all_paths():
-    return [(a, b, c) for a in range(LMAX + 1) for b in range(LMAX + 1)
-            for c in range(abs(a - b), min(LMAX, a + b) + 1)]
+def all_paths(lmax=LMAX):
+    return [(a, b, c) for a in range(lmax + 1) for b in range(lmax + 1)
+            for c in range(abs(a - b), min(lmax, a + b) + 1)]
 
 
 def k_of(l, m):
@@ -218,13 +218,13 @@ def main(argv):
 # input m1 (Eq. 13); rotate the result back.  Everything below is computed
 # here independently and emitted as constexpr tables.
 
-def aligned_terms():
+def aligned_terms(lmax=LMAX):
     """[(p, k3, k1, kappa)]: m'[k3] += W_p kappa x'[k1] in the edge frame.
 
     kappa = C_p[m3, m1, m2=0] * Y_l2,0(z-axis), Y_l,0(z) = sqrt((2l+1)/(4 pi)).
     """
     out = []
-    for p, (l1, l2, l3) in enumerate(all_paths()):
+    for p, (l1, l2, l3) in enumerate(all_paths(lmax)):
         ent = real_cg(l1, l2, l3)
         yz = sqrt((2 * l2 + 1) / (4 * pi))
         for (m3, m1, m2), v in sorted(ent.items()):
@@ -246,11 +246,11 @@ def frame_from_direction(n):
     return [[t1[0], t2[0], x], [t1[1], t2[1], y], [t1[2], t2[2], z]]
 
 
-def ir_coefficients():
-    """Ivanic-Ruedenberg recursion coefficients u, v, w for l = 2, 3:
+def ir_coefficients(levels=(2, 3)):
+    """Ivanic-Ruedenberg recursion coefficients u, v, w for the given l:
     {l: [[(u, v, w) for n in -l..l] for m in -l..l]}."""
     out = {}
-    for l in (2, 3):
+    for l in levels:
         rows = []
         for m in range(-l, l + 1):
             row = []
@@ -266,15 +266,15 @@ def ir_coefficients():
     return out
 
 
-def wigner_real(Q):
-    """Real Wigner-D blocks D_1..D_3 in this library's SH basis (CS phase,
+def wigner_real(Q, lmax=3):
+    """Real Wigner-D blocks D_1..D_lmax in this library's SH basis (CS phase,
     k = l*l+l+m) for rotation Q: Y_l(Q v) = D_l Y_l(v).  Plain Python
     reference of the device recursion."""
     # l = 1 in the (y, z, x) ordering without signs
     idx = [1, 2, 0]
     R = [[Q[idx[i]][idx[j]] for j in range(3)] for i in range(3)]
     D = {1: R}
-    coef = ir_coefficients()
+    coef = ir_coefficients(tuple(range(2, lmax + 1)))
 
     def Rm(i, j):
         return R[i + 1][j + 1]
@@ -289,7 +289,7 @@ def wigner_real(Q):
             return Rm(i, 1) * Dl(l - 1, a, -l + 1) + Rm(i, -1) * Dl(l - 1, a, l - 1)
         return Rm(i, 0) * Dl(l - 1, a, b)
 
-    for l in (2, 3):
+    for l in range(2, lmax + 1):
         M = []
         for m in range(-l, l + 1):
             row = []
@@ -317,11 +317,76 @@ def wigner_real(Q):
         D[l] = M
     # this library's basis carries the Condon-Shortley sign (-1)^|m| on m != 0
     out = {}
-    for l in (1, 2, 3):
+    for l in range(1, lmax + 1):
         sg = [(-1) ** abs(m) if m != 0 else 1 for m in range(-l, l + 1)]
         out[l] = [[sg[i] * D[l][i][j] * sg[j] for j in range(2 * l + 1)] for i in range(2 * l + 1)]
     return out
 
 
+# ---------------------------------------------------------------------------
+# Higher degrees (l_max = 4..6), the aligned-frame schedule only: the blog
+# names l <= 3 as its limit; at higher degree the dense product grows as
+# l^6 terms while the aligned one grows as l^3 (E2Former-V2 sections 1.1 and
+# 2.1), so only the aligned tables are emitted.
+
+HIGH_DEGREES = (4, 5, 6)
+
+
+def render_high():
+    lines = [
+        "// Generated by gen_tables.py at build time. Do not edit.",
+        "#pragma once",
+        "#include <cuda_runtime.h>",
+        "namespace eqmp { namespace tables_hl {",
+        "struct HlPath { int l1, l2, l3, first, count; };",
+        "struct HlTerm { int k3, k1; float kappa; };",
+        "template <int L> struct Hl;",
+    ]
+    for L in HIGH_DEGREES:
+        paths = all_paths(L)
+        at = aligned_terms(L)
+        first, count = [], []
+        for p in range(len(paths)):
+            idx = [i for i, t in enumerate(at) if t[0] == p]
+            first.append(idx[0] if idx else len(at))
+            count.append(len(idx))
+        lines.append(f"template <> struct Hl<{L}> {{")
+        lines.append(f"  static constexpr int kNumPaths = {len(paths)};")
+        lines.append(f"  static constexpr int kNumTerms = {len(at)};")
+        lines.append(f"  static constexpr HlPath kPaths[{len(paths)}] = {{")
+        for p, (l1, l2, l3) in enumerate(paths):
+            lines.append(f"    {{{l1}, {l2}, {l3}, {first[p]}, {count[p]}}},")
+        lines.append("  };")
+        lines.append(f"  static constexpr HlTerm kTerms[{len(at)}] = {{")
+        for (pp, k3, k1, kap) in at:
+            lines.append(f"    {{{k3}, {k1}, {_f(kap)}}},")
+        lines.append("  };")
+        lines.append("};")
+    top = max(HIGH_DEGREES)
+    ir = ir_coefficients(tuple(range(2, top + 1)))
+    W = 2 * top + 1
+    lines.append(f"// Ivanic-Ruedenberg (u, v, w) for l = 2..{top}: [l-2][m+{top}][n+{top}][3]")
+    lines.append(f"static __device__ const float kHlIr[{top - 1}][{W}][{W}][3] = {{")
+    for l in range(2, top + 1):
+        rows = []
+        for m in range(-top, top + 1):
+            vals = []
+            for n in range(-top, top + 1):
+                if abs(m) <= l and abs(n) <= l:
+                    u, v, w = ir[l][m + l][n + l]
+                else:
+                    u = v = w = 0.0
+                vals.append("{" + ", ".join(_f(t) for t in (u, v, w)) + "}")
+            rows.append("{" + ", ".join(vals) + "}")
+        lines.append("  {" + ", ".join(rows) + "},")
+    lines.append("};")
+    lines.append("}}  // namespace eqmp::tables_hl")
+    return "\n".join(lines) + "\n"
+
+
 if __name__ == "__main__":
-    main(sys.argv)
+    if len(sys.argv) > 2 and sys.argv[1] == "--high":
+        with open(sys.argv[2], "w") as fh:
+            fh.write(render_high())
+    else:
+        main(sys.argv)

@@ -101,9 +101,18 @@ def radial_basis(d: np.ndarray, n_basis: int = 8, r_max: float = 5.0, sigma: flo
     return (g * env[:, None]).astype(np.float32)
 
 
+def n_paths(l_max: int) -> int:
+    """Number of (l1, l2, l3) with |l1-l2| <= l3 <= l1+l2, all <= l_max."""
+    return sum(min(l_max, a + b) - abs(a - b) + 1 for a in range(l_max + 1) for b in range(l_max + 1))
+
+
 def make_workload(name: str = None, *, n_atoms=None, cutoff=None, channels=None,
-                  weights=None, storage=None, seed=None) -> Workload:
-    """Build a named workload, or a custom one from keyword overrides."""
+                  weights=None, storage=None, seed=None, l_max: int = 3) -> Workload:
+    """Build a named workload, or a custom one from keyword overrides.
+
+    l_max > 3 gives the higher-degree variant: x [N, C, (l_max+1)^2] and
+    weights over all n_paths(l_max) paths (fp32 storage only).
+    """
     spec = dict(WORKLOADS[name]) if name else {}
     for k, v in dict(n_atoms=n_atoms, cutoff=cutoff, channels=channels,
                      weights=weights, storage=storage, seed=seed).items():
@@ -113,12 +122,13 @@ def make_workload(name: str = None, *, n_atoms=None, cutoff=None, channels=None,
     rng = np.random.default_rng(spec["seed"])
     side = (n / DENSITY) ** (1.0 / 3.0)
     pos = rng.uniform(0.0, side, size=(n, 3))
-    x = rng.standard_normal((n, C, N_SH), dtype=np.float32)
+    P = n_paths(l_max)
+    x = rng.standard_normal((n, C, (l_max + 1) ** 2), dtype=np.float32)
     w = R = M = None
     if spec["weights"] == "shared":
-        w = (rng.standard_normal((N_PATHS, C)) / np.sqrt(N_PATHS)).astype(np.float32)
+        w = (rng.standard_normal((P, C)) / np.sqrt(P)).astype(np.float32)
     else:
-        M = (rng.standard_normal((8, N_PATHS * C)) / np.sqrt(8.0)).astype(np.float32)
+        M = (rng.standard_normal((8, P * C)) / np.sqrt(8.0)).astype(np.float32)
     src, dst = radius_graph(pos, float(spec["cutoff"]))
     vec = (pos[src] - pos[dst]).astype(np.float32)
     if spec["weights"] != "shared":

@@ -214,6 +214,26 @@ eqmp_status eqmp_fused_so2(const float* vec, const void* x, int64_t N_src, eqmp_
                            eqmp_stream_t stream);
 
 /*
+ * The fused layer at degree l_max = 4, 5 or 6 (the Batmobile blog stops at
+ * l <= 3 and names higher degrees as future work).  Same definition as
+ * eqmp_fused with every path (l1, l2, l3), all <= l_max, in the order
+ * l1 = 0..l_max, l2 = 0..l_max, l3 = |l1-l2|..min(l_max, l1+l2)
+ * (eqmp_num_paths_lmax: 65, 111, 175 paths), components k = l*l + l + m.
+ * Computed in the aligned frame of E2Former-V2 section 2.1 (Lemma 4.1,
+ * Eq. 13: O(l^3) terms per edge instead of the dense O(l^6)); exact up to
+ * rounding.
+ *   x    [N_src][C][(l_max+1)^2] fp32;  out [N][C][(l_max+1)^2] fp32, written
+ *   weights  shared w[P][C], or radial R[E][8] (16-byte aligned), M[8][P*C]
+ *   other arguments as eqmp_fused; C in {8, 16, 32, 64, 128}.
+ * EQMP_ERR_UNSUPPORTED for other l_max (l_max = 3 is eqmp_fused).
+ */
+int32_t eqmp_num_paths_lmax(int32_t l_max);
+
+eqmp_status eqmp_fused_lmax(int32_t l_max, const float* vec, const float* x, int64_t N_src,
+                            const int32_t* row_offsets, const int32_t* src, int64_t N, int64_t E,
+                            int32_t C, eqmp_weights weights, float* out, eqmp_stream_t stream);
+
+/*
  * Radius graph: the step before the layer.  E2Former-V2 (section 4.2,
  * deployment notes) builds neighbour lists by a radius cutoff instead of a
  * fixed k nearest neighbours; the Batmobile blog (monitoring section) takes

@@ -10,8 +10,9 @@
 // at build time from this library's real CG coefficients).
 //
 // Organisation: 128 threads per CTA in groups of C threads (thread =
-// channel); a group owns one receiver at a time and walks its edges in CSR
-// order.  Per edge the group builds the real Wigner-D blocks D_1..D_L of the
+// channel); a CTA owns one receiver at a time and deals its edges to its
+// groups, whose partial sums it adds in group order at the end.  Per edge
+// the group builds the real Wigner-D blocks D_1..D_L of the
 // edge frame in shared memory (frame by Duff et al. 2017; levels 2..L by the
 // Ivanic-Ruedenberg recursion, the entries of a level spread over the
 // group's threads), then every thread rotates its channel in, applies the
@@ -76,20 +77,20 @@ __device__ __forceinline__ void group_sync(int C, int g) {
 }
 
 // One entry (m, n) of level l in the Ivanic-Ruedenberg basis (real SH
-// without the Condon-Shortley sign, l = 1 block in (y, z, x) order).  Dp is
-// level l-1 with row stride sp; R the l = 1 block.
-__device__ float ir_entry(int l, int m, int n, const float (&R)[3][3], const float* Dp, int sp) {
+// without the Condon-Shortley sign, l = 1 block in (y, z, x) order).  R is
+// the stored l = 1 block (row stride 4), Dp level l-1 with row stride sp.
+__device__ __forceinline__ float ir_entry(int l, int m, int n, const float* R, const float* Dp, int sp) {
   const float* cf = &tables_hl::kHlIr[l - 2][m + 6][n + 6][0];
   const float u = __ldg(cf), v = __ldg(cf + 1), w = __ldg(cf + 2);
   auto dp = [&](int a, int b) { return Dp[(a + l - 1) * sp + (b + l - 1)]; };
-  auto P = [&](const float* Ri, int a, int b) {  // Ri = R[i + 1]
+  auto P = [&](const float* Ri, int a, int b) {  // Ri = row i + 1 of R
     if (b == l) return Ri[2] * dp(a, l - 1) - Ri[0] * dp(a, -l + 1);
     if (b == -l) return Ri[2] * dp(a, -l + 1) + Ri[0] * dp(a, l - 1);
     return Ri[1] * dp(a, b);
   };
-  const float* Rm = R[0];
-  const float* R0 = R[1];
-  const float* Rp = R[2];
+  const float* Rm = R;
+  const float* R0 = R + 4;
+  const float* Rp = R + 8;
   float val = 0.0f;
   if (u != 0.0f) val = u * P(R0, m, n);
   if (v != 0.0f) {
@@ -114,17 +115,30 @@ constexpr float sgn_m(int m) { return (m & 1) ? -1.0f : 1.0f; }  // (-1)^|m|
 
 // x'_l[n] = sum_m D_l[m][n] x_l[m], this library's basis (signs s_m s_n on
 // the recursion's entries); x_l read from global memory as needed.
+// Row m of level l (padded to whole float4s) from shared memory.
+template <int L, int l>
+__device__ __forceinline__ void load_row(const float* D, int m, float (&row)[HlCfg<L>::stride(l)]) {
+  constexpr int st = HlCfg<L>::stride(l), base = HlCfg<L>::off(l);
+  const float4* p = reinterpret_cast<const float4*>(D + base + m * st);
+#pragma unroll
+  for (int h = 0; h < st / 4; ++h) {
+    const float4 v = p[h];
+    row[4 * h] = v.x; row[4 * h + 1] = v.y; row[4 * h + 2] = v.z; row[4 * h + 3] = v.w;
+  }
+}
+
 template <int L, int l>
 __device__ __forceinline__ void rotate_in(const float* D, const float* xrow, float (&xr)[HlCfg<L>::NC]) {
-  constexpr int W = 2 * l + 1, o = l * l, st = HlCfg<L>::stride(l), base = HlCfg<L>::off(l);
+  constexpr int W = 2 * l + 1, o = l * l;
 #pragma unroll
   for (int n = 0; n < W; ++n) xr[o + n] = 0.0f;
 #pragma unroll
   for (int m = 0; m < W; ++m) {
     const float xm = __ldg(xrow + o + m);
+    float row[HlCfg<L>::stride(l)];
+    load_row<L, l>(D, m, row);
 #pragma unroll
-    for (int n = 0; n < W; ++n)
-      xr[o + n] = fmaf(sgn_m(m - l) * sgn_m(n - l) * D[base + m * st + n], xm, xr[o + n]);
+    for (int n = 0; n < W; ++n) xr[o + n] = fmaf(sgn_m(m - l) * sgn_m(n - l) * row[n], xm, xr[o + n]);
   }
 }
 
@@ -133,12 +147,14 @@ __device__ __forceinline__ void rotate_in(const float* D, const float* xrow, flo
 // this thread at acc[k * C] (the group's C threads side by side).
 template <int L, int l>
 __device__ __forceinline__ void rotate_out(const float* D, const float (&mp)[2 * L + 1], float* acc, int C) {
-  constexpr int W = 2 * l + 1, o = l * l, st = HlCfg<L>::stride(l), base = HlCfg<L>::off(l);
+  constexpr int W = 2 * l + 1, o = l * l;
 #pragma unroll
   for (int m = 0; m < W; ++m) {
+    float row[HlCfg<L>::stride(l)];
+    load_row<L, l>(D, m, row);
     float s = acc[(o + m) * C];
 #pragma unroll
-    for (int n = 0; n < W; ++n) s = fmaf(sgn_m(m - l) * sgn_m(n - l) * D[base + m * st + n], mp[n], s);
+    for (int n = 0; n < W; ++n) s = fmaf(sgn_m(m - l) * sgn_m(n - l) * row[n], mp[n], s);
     acc[(o + m) * C] = s;
   }
 }
@@ -166,7 +182,9 @@ __device__ __forceinline__ float path_weight(const HlArgs& a, int p, int c, cons
     asm volatile("" : "+f"(s));
     return s;
   } else {
-    return __ldg(a.w + (size_t)p * a.C + c);
+    float wv = __ldg(a.w + (size_t)p * a.C + c);
+    asm volatile("" : "+f"(wv));  // load as it is needed, not all paths ahead
+    return wv;
   }
 }
 
@@ -242,19 +260,23 @@ __global__ void __launch_bounds__(kHlThreads) k_hl(const HlArgs a) {
   const int C = a.C, G = kHlThreads / C;
   const int t = threadIdx.x, g = t / C, c = t % C;
   float* Dg = hsm + (size_t)g * 2 * K::DS;
-  // receiver accumulators: [NC][128] after the D buffers of all groups
-  float* acc = hsm + (size_t)G * 2 * K::DS + (size_t)g * NC * C + c;
+  // partial accumulators of each group: [G][NC][C] after the D buffers
+  float* accs = hsm + (size_t)G * 2 * K::DS;
+  float* acc = accs + (size_t)g * NC * C + c;
   // D buffer of the group's step-th edge is step & 1, counted across
   // receivers, and every step passes at least one group barrier: a buffer is
   // rewritten only after every thread of the group has left the step that
   // last read it.
   unsigned step = 0;
-  for (long long r = (long long)blockIdx.x * G + g; r < a.N; r += (long long)gridDim.x * G) {
+  // One receiver per CTA at a time; its edges are dealt to the G groups
+  // (group g takes e0 + g, e0 + g + G, ...), whose partial sums are added
+  // in group order at the end: deterministic.
+  for (long long r = blockIdx.x; r < a.N; r += gridDim.x) {
     const int e0 = min(max(__ldg(a.off + r), 0), a.E);
     const int e1 = max(e0, min(max(__ldg(a.off + r + 1), 0), a.E));
 #pragma unroll
     for (int k = 0; k < NC; ++k) acc[k * C] = 0.0f;
-    for (int e = e0; e < e1; ++e, ++step) {
+    for (int e = e0 + g; e < e1; e += G, ++step) {
       float* D = Dg + (step & 1u) * K::DS;
       const float vx = __ldg(a.vec + 3 * (size_t)e), vy = __ldg(a.vec + 3 * (size_t)e + 1),
                   vz = __ldg(a.vec + 3 * (size_t)e + 2);
@@ -271,23 +293,28 @@ __global__ void __launch_bounds__(kHlThreads) k_hl(const HlArgs a) {
       const bool in_range = (unsigned)s < (unsigned)a.N_src;  // an out-of-range sender adds nothing
       const float* xrow = a.x + ((size_t)(in_range ? s : 0) * C + c) * NC;
       if (!zero) {
-        // frame Q (columns t1, t2, n; Duff et al. 2017), then R in (y, z, x) order
-        const float inv = rsqrtf(r2);
-        const float x = vx * inv, y = vy * inv, z = vz * inv;
-        const float sg = z >= 0.0f ? 1.0f : -1.0f;
-        const float ia = -1.0f / (sg + z);
-        const float b = x * y * ia;
-        const float Q[3][3] = {{fmaf(sg * x * x, ia, 1.0f), b, x},
-                               {sg * b, fmaf(y * y, ia, sg), y},
-                               {-sg * x, -y, z}};
-        const float R[3][3] = {{Q[1][1], Q[1][2], Q[1][0]},
-                               {Q[2][1], Q[2][2], Q[2][0]},
-                               {Q[0][1], Q[0][2], Q[0][0]}};
-        if (c == 0) {
+        {
+          // frame Q (columns t1, t2, n; Duff et al. 2017); level 1 is Q in
+          // (y, z, x) order, entry (i, j) = 3 i + j written by thread
+          // (3 i + j) mod C
+          const float inv = rsqrtf(r2);
+          const float x = vx * inv, y = vy * inv, z = vz * inv;
+          const float sg = z >= 0.0f ? 1.0f : -1.0f;
+          const float ia = -1.0f / (sg + z);
+          const float b = x * y * ia;
+          const float Q[3][3] = {{fmaf(sg * x * x, ia, 1.0f), b, x},
+                                 {sg * b, fmaf(y * y, ia, sg), y},
+                                 {-sg * x, -y, z}};
+          for (int ij = c; ij < 9; ij += C) {
+            const int i = ij / 3, j = ij % 3;
+            const int qi = i == 0 ? 1 : i == 1 ? 2 : 0, qj = j == 0 ? 1 : j == 1 ? 2 : 0;
+            float q = 0.0f;
 #pragma unroll
-          for (int i = 0; i < 3; ++i)
+            for (int u = 0; u < 3; ++u)
 #pragma unroll
-            for (int j = 0; j < 3; ++j) D[K::off(1) + i * K::stride(1) + j] = R[i][j];
+              for (int v = 0; v < 3; ++v) q = (u == qi && v == qj) ? Q[u][v] : q;
+            D[K::off(1) + i * K::stride(1) + j] = q;
+          }
         }
         group_sync(C, g);
 #pragma unroll 1
@@ -301,7 +328,7 @@ __global__ void __launch_bounds__(kHlThreads) k_hl(const HlArgs a) {
           }
           for (int i = c; i < n_ent; i += C) {
             const int m = i / W - l, n = i % W - l;
-            D[base + (m + l) * st + (n + l)] = ir_entry(l, m, n, R, D + basep, stp);
+            D[base + (m + l) * st + (n + l)] = ir_entry(l, m, n, D + K::off(1), D + basep, stp);
           }
           group_sync(C, g);
         }
@@ -316,9 +343,15 @@ __global__ void __launch_bounds__(kHlThreads) k_hl(const HlArgs a) {
         if (in_range) zero_len_terms<L, RADIAL>(a, c, rad, xrow, acc, std::make_integer_sequence<int, K::P>{});
       }
     }
+    __syncthreads();
+    // out[r][c][k] = sum over groups in order; thread (g, c) takes k = g, g + G, ...
     float* orow = a.out + ((size_t)r * C + c) * NC;
-#pragma unroll
-    for (int k = 0; k < NC; ++k) orow[k] = acc[k * C];
+    for (int k = g; k < NC; k += G) {
+      float v = 0.0f;
+      for (int h = 0; h < G; ++h) v += accs[((size_t)h * NC + k) * C + c];
+      orow[k] = v;
+    }
+    __syncthreads();  // the partials are zeroed for the next receiver
   }
 }
 
@@ -331,8 +364,7 @@ eqmp_status launch_hl(const HlArgs& a, cudaStream_t st, const DeviceInfo& dev) {
   int occ = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kHlThreads, smem) != cudaSuccess || occ < 1)
     return EQMP_ERR_CUDA;
-  const int G = kHlThreads / a.C;
-  const long long want = ((long long)a.N + G - 1) / G;
+  const long long want = a.N;  // one receiver per CTA at a time
   const long long cap = (long long)dev.sms * occ;
   const int grid = (int)(want < cap ? want : cap);
   if (grid <= 0) return EQMP_OK;

@@ -59,7 +59,11 @@ struct SharedCfg {
   static constexpr bool WS = NCW % 4 == 0;           // warp-specialised with setmaxnreg
   static constexpr int CONS0 = WS ? 128 : 0;         // first consumer thread
   static constexpr int NTHREADS = WS ? 128 + NCONS : NCONS + 32;
+#ifdef EQMP_TUNE_MINB
+  static constexpr int MIN_BLOCKS = WS ? (NCONS >= 256 ? 1 : KQ == 4 ? EQMP_TUNE_MINB : 2) : 4;
+#else
   static constexpr int MIN_BLOCKS = WS ? (NCONS >= 256 ? 1 : 2) : 4;
+#endif
   // Registers: the launch gives every thread R0 (per-SMSP file of 16K
   // registers shared by the warps resident on it); the producer warpgroup
   // drops to RP and the consumer warpgroups rise to RC within that pool.

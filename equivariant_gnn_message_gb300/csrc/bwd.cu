@@ -2,11 +2,58 @@
 #include <mutex>
 
 #include "k_bwd.cuh"
+#include "k_bwd_sw.cuh"
 #include "launch.h"
 
 namespace eqmp {
 
 constexpr int kBwdGridPerSm = 8;
+
+// dw and dvec with shared weights in the forward kernel's schedule
+// (k_bwd_sw.cuh); C = 32 and 64.  One workspace row of [34][C] partial dw
+// per CTA (at most max_rows CTAs), summed in order by k_bwd_reduce_w.
+template <int C>
+static eqmp_status launch_bwd_sw(const BwdArgs& a, float* gw, long long max_rows, cudaStream_t st,
+                                 const DeviceInfo& dev) {
+  using K = BwdSwCfg<C>;
+  auto kern = k_bwd_sw<C>;
+  static unsigned long long attr_done = 0;
+  static int occ_cache[64] = {0};
+  if (ensure_smem_attr(kern, K::SMEM_BYTES, &attr_done) != cudaSuccess) return EQMP_ERR_CUDA;
+  int d = 0;
+  cudaGetDevice(&d);
+  int occ = __atomic_load_n(&occ_cache[d & 63], __ATOMIC_RELAXED);
+  if (occ == 0) {
+    // setmaxnreg.inc waits, without a limit, for the registers it asks for:
+    // launch only if the compiled count gives a pool that covers the split
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return EQMP_ERR_CUDA;
+    if ((long long)fa.numRegs * K::NTHREADS < (long long)K::RP * 128 + (long long)K::RC * K::NCONS)
+      return EQMP_ERR_UNSUPPORTED;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, K::NTHREADS, K::SMEM_BYTES) != cudaSuccess ||
+        occ < 1)
+      return EQMP_ERR_CUDA;
+    __atomic_store_n(&occ_cache[d & 63], occ, __ATOMIC_RELAXED);
+  }
+  long long grid = (long long)dev.sms * occ;
+  if (grid > a.N) grid = a.N;
+  if (grid > max_rows) grid = max_rows;
+  if (grid <= 0) return EQMP_OK;
+  CUtensorMap map;
+  if (a.E > 0) {
+    const eqmp_status s = encode_x_map(a.x, a.N_src, C, false, &map);
+    if (s != EQMP_OK) return s;
+  } else {
+    memset(&map, 0, sizeof(map));  // never dereferenced: no edge, no load
+  }
+  kern<<<(int)grid, K::NTHREADS, K::SMEM_BYTES, st>>>(map, a, dev.watchdog);
+  if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
+  if (gw) {
+    k_bwd_reduce_w<<<(34 * C + kRedX - 1) / kRedX, dim3(kRedX, kRedY), 0, st>>>(a.ws, (int)grid, 34 * C, gw);
+    if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
+  }
+  return EQMP_OK;
+}
 
 template <int C>
 static long long bwd_slots(long long N, int sms) {
@@ -73,6 +120,10 @@ static eqmp_status run_bwd(const BwdArgs& a, bool want_x, bool want_wv, float* g
       k_bwd_x<C, RADIAL><<<(int)(want < cap ? want : cap), K::NT, 0, st>>>(a);
       if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
     }
+  }
+  if constexpr (!RADIAL && (C == 32 || C == 64)) {
+    if (want_wv && a.N > 0) return launch_bwd_sw<C>(a, gw, 1ll << 40, st, dev);
+    return EQMP_OK;
   }
   if (want_wv && a.N > 0) {
     const int grid = (int)(bwd_slots<C>(a.N, dev.sms) / K::GROUPS);
@@ -234,6 +285,11 @@ static eqmp_status run_bwd_noalloc(const BwdArgs& a, bool want_x, bool want_wv, 
       k_bwd_x<C, RADIAL><<<(int)(want < cap ? want : cap), K::NT, 0, st>>>(a);
       if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
     }
+  }
+  if constexpr (!RADIAL && (C == 32 || C == 64)) {
+    if (want_wv && a.N > 0)
+      return launch_bwd_sw<C>(a, gw, (long long)(kNoAllocBytes / ((size_t)34 * C * 4)), st, dev);
+    return EQMP_OK;
   }
   if (want_wv && a.N > 0) {
     // as many receiver groups as the static scratch holds partial rows for

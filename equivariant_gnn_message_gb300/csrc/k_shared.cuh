@@ -146,10 +146,21 @@ __device__ __forceinline__ void apply_terms(const float2 (&acc)[KQ][8], float (&
   (apply_term<KQ, Q, First + Is, T>(acc, tmp), ...);
 }
 
+// Bit k3 set when path P reaches output k3 from k1 in [k1lo, k1lo + n);
+// used only in constant expressions (the tables are host constants).
+template <bool T>
+constexpr unsigned path_mask_t(int P, int k1lo, int n) {
+  unsigned m = 0;
+  for (int k3 = 0; k3 < 16; ++k3)
+    if (path_has_t<T>(P, k1lo, n, k3)) m |= 1u << k3;
+  return m;
+}
+
 template <int KQ, int Q, int P, bool T, int... K3>
 __device__ __forceinline__ void weight_outputs(float w, const float (&tmp)[16], float (&part)[16],
                                                std::integer_sequence<int, K3...>) {
-  ((path_has_t<T>(P, Q * KQ, KQ, K3) ? (void)(part[K3] = fmaf(w, tmp[K3], part[K3])) : (void)0), ...);
+  constexpr unsigned mask = path_mask_t<T>(P, Q * KQ, KQ);
+  ((((mask >> K3) & 1u) ? (void)(part[K3] = fmaf(w, tmp[K3], part[K3])) : (void)0), ...);
 }
 
 template <int C, int KQ, int Q, int P, bool T>

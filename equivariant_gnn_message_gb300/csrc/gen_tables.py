@@ -365,21 +365,18 @@ def render_high():
     top = max(HIGH_DEGREES)
     ir = ir_coefficients(tuple(range(2, top + 1)))
     W = 2 * top + 1
-    lines.append(f"// Ivanic-Ruedenberg (u, v, w) for l = 2..{top}: [l-2][m+{top}][n+{top}][3]")
-    lines.append(f"static __device__ const float kHlIr[{top - 1}][{W}][{W}][3] = {{")
-    for l in range(2, top + 1):
-        rows = []
-        for m in range(-top, top + 1):
-            vals = []
-            for n in range(-top, top + 1):
-                if abs(m) <= l and abs(n) <= l:
-                    u, v, w = ir[l][m + l][n + l]
-                else:
-                    u = v = w = 0.0
-                vals.append("{" + ", ".join(_f(t) for t in (u, v, w)) + "}")
-            rows.append("{" + ", ".join(vals) + "}")
-        lines.append("  {" + ", ".join(rows) + "},")
-    lines.append("};")
+    for nm, idx in (("kHlIrU", 0), ("kHlIrV", 1), ("kHlIrW", 2)):
+        lines.append(f"// Ivanic-Ruedenberg {nm[-1].lower()} for l = 2..{top}: [l-2][m+{top}][n+{top}] (0 outside |m|,|n| <= l)")
+        lines.append(f"constexpr float {nm}[{top - 1}][{W}][{W}] = {{")
+        for l in range(2, top + 1):
+            rows = []
+            for m in range(-top, top + 1):
+                vals = []
+                for n in range(-top, top + 1):
+                    vals.append(_f(ir[l][m + l][n + l][idx]) if abs(m) <= l and abs(n) <= l else "0.0f")
+                rows.append("{" + ", ".join(vals) + "}")
+            lines.append("  {" + ", ".join(rows) + "},")
+        lines.append("};")
     lines.append("}}  // namespace eqmp::tables_hl")
     return "\n".join(lines) + "\n"
 

@@ -10,15 +10,15 @@
 // at build time from this library's real CG coefficients).
 //
 // Organisation: 128 threads per CTA in groups of C threads (thread =
-// channel); a CTA owns one receiver at a time and deals its edges to its
-// groups, whose partial sums it adds in group order at the end.  Per edge
-// the group builds the real Wigner-D blocks D_1..D_L of the
-// edge frame in shared memory (frame by Duff et al. 2017; levels 2..L by the
-// Ivanic-Ruedenberg recursion, the entries of a level spread over the
-// group's threads), then every thread rotates its channel in, applies the
-// aligned terms with its path weights, and rotates back into its receiver
-// accumulators.  D is double-buffered so one group barrier per level is the
-// only synchronisation.  Deterministic (fixed order everywhere), no atomics.
+// channel); a CTA owns one receiver at a time.  For each batch of its edges,
+// one thread per edge builds the real Wigner-D blocks D_1..D_L of the edge
+// frame in shared memory (frame by Duff et al. 2017; levels 2..L by the
+// Ivanic-Ruedenberg recursion with compile-time coefficients, so the threads
+// never diverge).  The groups then take the batch's edges: the sender row is
+// staged in shared memory with coalesced loads, every thread rotates its
+// channel in, applies the aligned terms with its path weights, and rotates
+// back into its partial accumulators; the partials are added in group order
+// at the end.  Deterministic (fixed order everywhere), no atomics.
 // Zero-length edges (r^2 < 1e-30) take Y = (Y00, 0, ...): only the paths
 // (l, 0, l) contribute, as W_p Y00 x_l.
 #include <stdint.h>
@@ -36,6 +36,7 @@ namespace {
 using tables_hl::Hl;
 
 constexpr int kHlThreads = 128;
+constexpr int kBatch = 16;  // edges whose Wigner blocks are built at once
 
 struct HlArgs {
   const float* vec;
@@ -60,10 +61,17 @@ struct HlCfg {
     for (int j = 1; j < l; ++j) o += (2 * j + 1) * stride(j);
     return o;
   }
-  static constexpr int DS = (off(L + 1) + 31) / 32 * 32;  // floats per D set
-  // D double buffers of every group + accumulators of every thread
-  static constexpr int smem(int C) { return ((kHlThreads / C) * 2 * DS + NC * kHlThreads) * 4; }
-  static constexpr int SMEM = smem(8);  // largest: 16 groups of 8
+  static constexpr int DS = (off(L + 1) + 31) / 32 * 32;  // floats per edge slot (D_1..D_L)
+  static constexpr int XV = (NC + 3) / 4;                  // float4s of a staged row per thread
+  // floats: a batch of kBatch edge slots (+ zero-length flags), the
+  // accumulators of every thread [NC][128], the staged sender rows
+  // [G][C][NC] (= [128][NC]), then the weights: shared [P][C], or the
+  // current edge's radial weights of every thread [P][128]
+  static constexpr int off_flag() { return kBatch * DS; }
+  static constexpr int off_acc() { return off_flag() + kBatch; }
+  static constexpr int off_x() { return off_acc() + NC * kHlThreads; }
+  static constexpr int off_w() { return off_x() + NC * kHlThreads; }
+  static constexpr int smem(int C, bool radial) { return (off_w() + (radial ? P * kHlThreads : P * C)) * 4; }
 };
 
 __device__ __forceinline__ void group_sync(int C, int g) {
@@ -76,39 +84,87 @@ __device__ __forceinline__ void group_sync(int C, int g) {
   }
 }
 
-// One entry (m, n) of level l in the Ivanic-Ruedenberg basis (real SH
-// without the Condon-Shortley sign, l = 1 block in (y, z, x) order).  R is
-// the stored l = 1 block (row stride 4), Dp level l-1 with row stride sp.
-__device__ __forceinline__ float ir_entry(int l, int m, int n, const float* R, const float* Dp, int sp) {
-  const float* cf = &tables_hl::kHlIr[l - 2][m + 6][n + 6][0];
-  const float u = __ldg(cf), v = __ldg(cf + 1), w = __ldg(cf + 2);
+// ---- Wigner-D of one edge, computed by one thread -----------------------
+// Ivanic-Ruedenberg basis (real SH without the Condon-Shortley sign, l = 1
+// block = the frame rotation in (y, z, x) order).  Level l entry (M, N) from
+// level l-1 (Dp, padded rows) and R, with compile-time coefficients: no
+// branches on the data, so the threads of a warp, each on its own edge,
+// never diverge.
+template <int L>
+constexpr float hl_u(int l, int m, int n) { return tables_hl::kHlIrU[l - 2][m + 6][n + 6]; }
+template <int L>
+constexpr float hl_v(int l, int m, int n) { return tables_hl::kHlIrV[l - 2][m + 6][n + 6]; }
+template <int L>
+constexpr float hl_w(int l, int m, int n) { return tables_hl::kHlIrW[l - 2][m + 6][n + 6]; }
+
+template <int LL, int l, int I, int A, int B>
+__device__ __forceinline__ float hl_P(const float (&R)[3][3], const float* Dp) {
+  constexpr int sp = HlCfg<LL>::stride(l - 1);
   auto dp = [&](int a, int b) { return Dp[(a + l - 1) * sp + (b + l - 1)]; };
-  auto P = [&](const float* Ri, int a, int b) {  // Ri = row i + 1 of R
-    if (b == l) return Ri[2] * dp(a, l - 1) - Ri[0] * dp(a, -l + 1);
-    if (b == -l) return Ri[2] * dp(a, -l + 1) + Ri[0] * dp(a, l - 1);
-    return Ri[1] * dp(a, b);
-  };
-  const float* Rm = R;
-  const float* R0 = R + 4;
-  const float* Rp = R + 8;
+  if constexpr (B == l) {
+    return R[I + 1][2] * dp(A, l - 1) - R[I + 1][0] * dp(A, -l + 1);
+  } else if constexpr (B == -l) {
+    return R[I + 1][2] * dp(A, -l + 1) + R[I + 1][0] * dp(A, l - 1);
+  } else {
+    return R[I + 1][1] * dp(A, B);
+  }
+}
+
+template <int LL, int l, int M, int N>
+__device__ __forceinline__ float hl_entry(const float (&R)[3][3], const float* Dp) {
+  constexpr float u = hl_u<LL>(l, M, N), v = hl_v<LL>(l, M, N), w = hl_w<LL>(l, M, N);
   float val = 0.0f;
-  if (u != 0.0f) val = u * P(R0, m, n);
-  if (v != 0.0f) {
+  if constexpr (u != 0.0f) val = u * hl_P<LL, l, 0, M, N>(R, Dp);
+  if constexpr (v != 0.0f) {
     float V;
-    if (m == 0) {
-      V = P(Rp, 1, n) + P(Rm, -1, n);
-    } else if (m > 0) {
-      V = m == 1 ? P(Rp, 0, n) * 1.41421356237309515f : P(Rp, m - 1, n) - P(Rm, -m + 1, n);
+    if constexpr (M == 0) {
+      V = hl_P<LL, l, 1, 1, N>(R, Dp) + hl_P<LL, l, -1, -1, N>(R, Dp);
+    } else if constexpr (M == 1) {
+      V = hl_P<LL, l, 1, 0, N>(R, Dp) * 1.41421356237309515f;
+    } else if constexpr (M > 1) {
+      V = hl_P<LL, l, 1, M - 1, N>(R, Dp) - hl_P<LL, l, -1, -M + 1, N>(R, Dp);
+    } else if constexpr (M == -1) {
+      V = hl_P<LL, l, -1, 0, N>(R, Dp) * 1.41421356237309515f;
     } else {
-      V = m == -1 ? P(Rm, 0, n) * 1.41421356237309515f : P(Rp, m + 1, n) + P(Rm, -m - 1, n);
+      V = hl_P<LL, l, 1, M + 1, N>(R, Dp) + hl_P<LL, l, -1, -M - 1, N>(R, Dp);
     }
     val = fmaf(v, V, val);
   }
-  if (w != 0.0f) {
-    const float Wt = m > 0 ? P(Rp, m + 1, n) + P(Rm, -m - 1, n) : P(Rp, m - 1, n) - P(Rm, -m + 1, n);
+  if constexpr (w != 0.0f) {
+    float Wt;
+    if constexpr (M > 0)
+      Wt = hl_P<LL, l, 1, M + 1, N>(R, Dp) + hl_P<LL, l, -1, -M - 1, N>(R, Dp);
+    else
+      Wt = hl_P<LL, l, 1, M - 1, N>(R, Dp) - hl_P<LL, l, -1, -M + 1, N>(R, Dp);
     val = fmaf(w, Wt, val);
   }
   return val;
+}
+
+template <int LL, int l, int... Is>
+__device__ __forceinline__ void hl_level(const float (&R)[3][3], float* D, std::integer_sequence<int, Is...>) {
+  constexpr int W = 2 * l + 1, st = HlCfg<LL>::stride(l), base = HlCfg<LL>::off(l), pbase = HlCfg<LL>::off(l - 1);
+  ((D[base + (Is / W) * st + Is % W] = hl_entry<LL, l, Is / W - l, Is % W - l>(R, D + pbase)), ...);
+}
+
+template <int LL, int... ls>
+__device__ __forceinline__ void hl_levels(const float (&R)[3][3], float* D, std::integer_sequence<int, ls...>) {
+  (hl_level<LL, ls + 2>(R, D, std::make_integer_sequence<int, (2 * (ls + 2) + 1) * (2 * (ls + 2) + 1)>{}), ...);
+}
+
+// Frame of unit direction (x, y, z) and D_1..D_L into one edge slot.
+template <int L>
+__device__ __forceinline__ void hl_wigner(float x, float y, float z, float* D) {
+  const float sg = z >= 0.0f ? 1.0f : -1.0f;
+  const float ia = -1.0f / (sg + z);
+  const float b = x * y * ia;
+  const float Q[3][3] = {{fmaf(sg * x * x, ia, 1.0f), b, x}, {sg * b, fmaf(y * y, ia, sg), y}, {-sg * x, -y, z}};
+  const float R[3][3] = {{Q[1][1], Q[1][2], Q[1][0]}, {Q[2][1], Q[2][2], Q[2][0]}, {Q[0][1], Q[0][2], Q[0][0]}};
+#pragma unroll
+  for (int i = 0; i < 3; ++i)
+#pragma unroll
+    for (int j = 0; j < 3; ++j) D[HlCfg<L>::off(1) + i * HlCfg<L>::stride(1) + j] = R[i][j];
+  hl_levels<L>(R, D, std::make_integer_sequence<int, L - 1>{});
 }
 
 constexpr float sgn_m(int m) { return (m & 1) ? -1.0f : 1.0f; }  // (-1)^|m|
@@ -134,7 +190,7 @@ __device__ __forceinline__ void rotate_in(const float* D, const float* xrow, flo
   for (int n = 0; n < W; ++n) xr[o + n] = 0.0f;
 #pragma unroll
   for (int m = 0; m < W; ++m) {
-    const float xm = __ldg(xrow + o + m);
+    const float xm = xrow[o + m];
     float row[HlCfg<L>::stride(l)];
     load_row<L, l>(D, m, row);
 #pragma unroll
@@ -164,27 +220,15 @@ __device__ __forceinline__ void rotate_in_all(const float* D, const float* xrow,
                                               std::integer_sequence<int, ls...>) {
   (rotate_in<L, ls + 1>(D, xrow, xr), ...);
 }
-// Weight of path p for channel c of edge e.
+// Weight of path p for this thread's channel: shared weights staged in
+// shared memory (ws[p * C + c]); radial weights of the current edge, formed
+// per thread at the start of the edge (ws[p * 128 + thread]).
 template <int L, bool RADIAL>
-__device__ __forceinline__ float path_weight(const HlArgs& a, int p, int c, const float (&rad)[8]) {
-  constexpr int P = HlCfg<L>::P;
+__device__ __forceinline__ float path_weight(const HlArgs& a, const float* ws, int p, int c, const float (&rad)[8]) {
   if constexpr (RADIAL) {
-    // the eight loads of one path together; the empty asm keeps the
-    // compiler from hoisting the loads of every path ahead at once
-    const float* mp = a.M + (size_t)p * a.C + c;
-    const size_t stride = (size_t)P * a.C;
-    float m[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) m[k] = __ldg(mp + k * stride);
-    float s = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) s = fmaf(rad[k], m[k], s);
-    asm volatile("" : "+f"(s));
-    return s;
+    return ws[p * kHlThreads + threadIdx.x];
   } else {
-    float wv = __ldg(a.w + (size_t)p * a.C + c);
-    asm volatile("" : "+f"(wv));  // load as it is needed, not all paths ahead
-    return wv;
+    return ws[p * a.C + c];
   }
 }
 
@@ -202,22 +246,22 @@ __device__ __forceinline__ void path_terms(float wp, const float (&xr)[HlCfg<L>:
 // its weight, then the rotation back into the accumulators.  Working one
 // output block at a time keeps only 2 l3 + 1 partial outputs live.
 template <int L, bool RADIAL, int L3, int p>
-__device__ __forceinline__ void block_path(const HlArgs& a, int c, const float (&rad)[8],
+__device__ __forceinline__ void block_path(const HlArgs& a, const float* ws, int c, const float (&rad)[8],
                                            const float (&xr)[HlCfg<L>::NC], float (&mp)[2 * L + 1]) {
   constexpr tables_hl::HlPath path = Hl<L>::kPaths[p];
   if constexpr (path.l3 == L3 && path.count > 0)
-    path_terms<L, path.first, L3 * L3>(path_weight<L, RADIAL>(a, p, c, rad), xr, mp,
+    path_terms<L, path.first, L3 * L3>(path_weight<L, RADIAL>(a, ws, p, c, rad), xr, mp,
                                        std::make_integer_sequence<int, path.count>{});
 }
 
 template <int L, bool RADIAL, int L3, int... Ps>
-__device__ __forceinline__ void out_block(const HlArgs& a, int c, const float (&rad)[8], const float* D,
-                                          const float (&xr)[HlCfg<L>::NC], float* acc,
+__device__ __forceinline__ void out_block(const HlArgs& a, const float* ws, int c, const float (&rad)[8],
+                                          const float* D, const float (&xr)[HlCfg<L>::NC], float* acc,
                                           std::integer_sequence<int, Ps...>) {
   float mp[2 * L + 1];
 #pragma unroll
   for (int k = 0; k < 2 * L + 1; ++k) mp[k] = 0.0f;
-  (block_path<L, RADIAL, L3, Ps>(a, c, rad, xr, mp), ...);
+  (block_path<L, RADIAL, L3, Ps>(a, ws, c, rad, xr, mp), ...);
   if constexpr (L3 == 0) {
     acc[0] += mp[0];
   } else {
@@ -226,30 +270,30 @@ __device__ __forceinline__ void out_block(const HlArgs& a, int c, const float (&
 }
 
 template <int L, bool RADIAL, int... L3s>
-__device__ __forceinline__ void all_blocks(const HlArgs& a, int c, const float (&rad)[8], const float* D,
-                                           const float (&xr)[HlCfg<L>::NC], float* acc,
+__device__ __forceinline__ void all_blocks(const HlArgs& a, const float* ws, int c, const float (&rad)[8],
+                                           const float* D, const float (&xr)[HlCfg<L>::NC], float* acc,
                                            std::integer_sequence<int, L3s...>) {
-  (out_block<L, RADIAL, L3s>(a, c, rad, D, xr, acc, std::make_integer_sequence<int, HlCfg<L>::P>{}), ...);
+  (out_block<L, RADIAL, L3s>(a, ws, c, rad, D, xr, acc, std::make_integer_sequence<int, HlCfg<L>::P>{}), ...);
 }
 
 // Zero-length edge: out_l += W_(l,0,l) Y00 x_l.
 template <int L, bool RADIAL, int p>
-__device__ __forceinline__ void zero_len_path(const HlArgs& a, int c, const float (&rad)[8], const float* xrow,
-                                              float* acc) {
+__device__ __forceinline__ void zero_len_path(const HlArgs& a, const float* ws, int c, const float (&rad)[8],
+                                              const float* xrow, float* acc) {
   constexpr float y00 = 0.28209479177387814f;
   constexpr tables_hl::HlPath path = Hl<L>::kPaths[p];
   if constexpr (path.l2 == 0) {
-    const float wy = path_weight<L, RADIAL>(a, p, c, rad) * y00;
+    const float wy = path_weight<L, RADIAL>(a, ws, p, c, rad) * y00;
 #pragma unroll
     for (int k = path.l1 * path.l1; k < (path.l1 + 1) * (path.l1 + 1); ++k)
-      acc[k * a.C] = fmaf(wy, __ldg(xrow + k), acc[k * a.C]);
+      acc[k * a.C] = fmaf(wy, xrow[k], acc[k * a.C]);
   }
 }
 
 template <int L, bool RADIAL, int... Ps>
-__device__ __forceinline__ void zero_len_terms(const HlArgs& a, int c, const float (&rad)[8], const float* xrow,
-                                               float* acc, std::integer_sequence<int, Ps...>) {
-  (zero_len_path<L, RADIAL, Ps>(a, c, rad, xrow, acc), ...);
+__device__ __forceinline__ void zero_len_terms(const HlArgs& a, const float* ws, int c, const float (&rad)[8],
+                                               const float* xrow, float* acc, std::integer_sequence<int, Ps...>) {
+  (zero_len_path<L, RADIAL, Ps>(a, ws, c, rad, xrow, acc), ...);
 }
 
 template <int L, bool RADIAL>
@@ -259,88 +303,100 @@ __global__ void __launch_bounds__(kHlThreads) k_hl(const HlArgs a) {
   extern __shared__ float hsm[];
   const int C = a.C, G = kHlThreads / C;
   const int t = threadIdx.x, g = t / C, c = t % C;
-  float* Dg = hsm + (size_t)g * 2 * K::DS;
-  // partial accumulators of each group: [G][NC][C] after the D buffers
-  float* accs = hsm + (size_t)G * 2 * K::DS;
+  float* slots = hsm;                      // [kBatch][DS]
+  float* flags = hsm + K::off_flag();      // [kBatch]: 1 for a zero-length edge
+  float* accs = hsm + K::off_acc();        // partial accumulators [G][NC][C]
   float* acc = accs + (size_t)g * NC * C + c;
-  // D buffer of the group's step-th edge is step & 1, counted across
-  // receivers, and every step passes at least one group barrier: a buffer is
-  // rewritten only after every thread of the group has left the step that
-  // last read it.
-  unsigned step = 0;
-  // One receiver per CTA at a time; its edges are dealt to the G groups
-  // (group g takes e0 + g, e0 + g + G, ...), whose partial sums are added
-  // in group order at the end: deterministic.
+  float* xs = hsm + K::off_x() + (size_t)g * C * NC;  // the group's staged sender row [C][NC]
+  float* ws = hsm + K::off_w();
+  if constexpr (!RADIAL) {
+    for (int i = t; i < K::P * C; i += kHlThreads) ws[i] = __ldg(a.w + i);
+    __syncthreads();
+  }
+  // One receiver per CTA at a time.  Its edges go in batches of kBatch:
+  // thread j builds the Wigner blocks of edge j of the batch (one edge per
+  // thread, no divergence), then the G groups take the batch's edges
+  // g, g + G, ... and add them into their partial sums, which are summed in
+  // group order at the end: deterministic.
   for (long long r = blockIdx.x; r < a.N; r += gridDim.x) {
     const int e0 = min(max(__ldg(a.off + r), 0), a.E);
     const int e1 = max(e0, min(max(__ldg(a.off + r + 1), 0), a.E));
 #pragma unroll
     for (int k = 0; k < NC; ++k) acc[k * C] = 0.0f;
-    for (int e = e0 + g; e < e1; e += G, ++step) {
-      float* D = Dg + (step & 1u) * K::DS;
-      const float vx = __ldg(a.vec + 3 * (size_t)e), vy = __ldg(a.vec + 3 * (size_t)e + 1),
-                  vz = __ldg(a.vec + 3 * (size_t)e + 2);
-      const float r2 = fmaf(vx, vx, fmaf(vy, vy, vz * vz));
-      const bool zero = !(r2 >= 1e-30f);  // group-uniform
-      float rad[8];
-      if constexpr (RADIAL) {
-        const float4* rp = reinterpret_cast<const float4*>(a.R) + 2 * (size_t)e;
-        const float4 r0 = __ldg(rp), r1 = __ldg(rp + 1);
-        rad[0] = r0.x; rad[1] = r0.y; rad[2] = r0.z; rad[3] = r0.w;
-        rad[4] = r1.x; rad[5] = r1.y; rad[6] = r1.z; rad[7] = r1.w;
-      }
-      const int s = __ldg(a.src + e);
-      const bool in_range = (unsigned)s < (unsigned)a.N_src;  // an out-of-range sender adds nothing
-      const float* xrow = a.x + ((size_t)(in_range ? s : 0) * C + c) * NC;
-      if (!zero) {
-        {
-          // frame Q (columns t1, t2, n; Duff et al. 2017); level 1 is Q in
-          // (y, z, x) order, entry (i, j) = 3 i + j written by thread
-          // (3 i + j) mod C
+    for (int b0 = e0; b0 < e1; b0 += kBatch) {
+      const int nb = min(kBatch, e1 - b0);
+      __syncthreads();  // the previous batch's slots are no longer read
+      if (t < nb) {
+        const int e = b0 + t;
+        const float vx = __ldg(a.vec + 3 * (size_t)e), vy = __ldg(a.vec + 3 * (size_t)e + 1),
+                    vz = __ldg(a.vec + 3 * (size_t)e + 2);
+        const float r2 = fmaf(vx, vx, fmaf(vy, vy, vz * vz));
+        if (r2 >= 1e-30f) {
           const float inv = rsqrtf(r2);
-          const float x = vx * inv, y = vy * inv, z = vz * inv;
-          const float sg = z >= 0.0f ? 1.0f : -1.0f;
-          const float ia = -1.0f / (sg + z);
-          const float b = x * y * ia;
-          const float Q[3][3] = {{fmaf(sg * x * x, ia, 1.0f), b, x},
-                                 {sg * b, fmaf(y * y, ia, sg), y},
-                                 {-sg * x, -y, z}};
-          for (int ij = c; ij < 9; ij += C) {
-            const int i = ij / 3, j = ij % 3;
-            const int qi = i == 0 ? 1 : i == 1 ? 2 : 0, qj = j == 0 ? 1 : j == 1 ? 2 : 0;
-            float q = 0.0f;
+          hl_wigner<L>(vx * inv, vy * inv, vz * inv, slots + (size_t)t * K::DS);
+          flags[t] = 0.0f;
+        } else {
+          flags[t] = 1.0f;  // zero length: Y = (Y00, 0, ...)
+        }
+      }
+      __syncthreads();
+      for (int j = g; j < nb; j += G) {
+        const int e = b0 + j;
+        const float* D = slots + (size_t)j * K::DS;
+        const bool zero = flags[j] != 0.0f;
+        float rad[8];
+        if constexpr (RADIAL) {
+          const float4* rp = reinterpret_cast<const float4*>(a.R) + 2 * (size_t)e;
+          const float4 r0 = __ldg(rp), r1 = __ldg(rp + 1);
+          rad[0] = r0.x; rad[1] = r0.y; rad[2] = r0.z; rad[3] = r0.w;
+          rad[4] = r1.x; rad[5] = r1.y; rad[6] = r1.z; rad[7] = r1.w;
+          // W[p] = sum_k R[e,k] M[k, p C + c] for every path, into this
+          // thread's column (read only by this thread); eight paths at a time
+          const float* mc = a.M + c;
+          const size_t pc = (size_t)K::P * C;
+#pragma unroll 1
+          for (int p0 = 0; p0 < K::P; p0 += 8) {
+            float m[8][8];
 #pragma unroll
-            for (int u = 0; u < 3; ++u)
+            for (int q = 0; q < 8; ++q)
 #pragma unroll
-              for (int v = 0; v < 3; ++v) q = (u == qi && v == qj) ? Q[u][v] : q;
-            D[K::off(1) + i * K::stride(1) + j] = q;
+              for (int k = 0; k < 8; ++k)
+                m[q][k] = p0 + q < K::P ? __ldg(mc + k * pc + (size_t)(p0 + q) * C) : 0.0f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              float w = 0.0f;
+#pragma unroll
+              for (int k = 0; k < 8; ++k) w = fmaf(rad[k], m[q][k], w);
+              if (p0 + q < K::P) ws[(p0 + q) * kHlThreads + t] = w;
+            }
+          }
+        }
+        const int s = __ldg(a.src + e);
+        const bool in_range = (unsigned)s < (unsigned)a.N_src;  // an out-of-range sender adds nothing
+        // stage the sender's row (C * NC floats, contiguous) with coalesced float4s
+        {
+          const float4* src4 = reinterpret_cast<const float4*>(a.x + (size_t)(in_range ? s : 0) * C * NC);
+          float4* xs4 = reinterpret_cast<float4*>(xs);
+          const int n4 = C * NC / 4;
+#pragma unroll
+          for (int v = 0; v < K::XV; ++v) {
+            const int i = c + v * C;
+            if (i < n4) xs4[i] = __ldg(src4 + i);
           }
         }
         group_sync(C, g);
-#pragma unroll 1
-        for (int l = 2; l <= L; ++l) {
-          const int W = 2 * l + 1, n_ent = W * W;
-          const int st = (W + 3) / 4 * 4, stp = (W - 2 + 3) / 4 * 4;
-          int base = 0, basep = 0;
-          for (int j = 1; j < l; ++j) {
-            basep = base;
-            base += (2 * j + 1) * ((2 * j + 1 + 3) / 4 * 4);
-          }
-          for (int i = c; i < n_ent; i += C) {
-            const int m = i / W - l, n = i % W - l;
-            D[base + (m + l) * st + (n + l)] = ir_entry(l, m, n, D + K::off(1), D + basep, stp);
-          }
-          group_sync(C, g);
-        }
         if (in_range) {
-          float xr[NC];
-          xr[0] = __ldg(xrow);
-          rotate_in_all<L>(D, xrow, xr, std::make_integer_sequence<int, L>{});
-          all_blocks<L, RADIAL>(a, c, rad, D, xr, acc, std::make_integer_sequence<int, L + 1>{});
+          const float* xrs = xs + c * NC;
+          if (!zero) {
+            float xr[NC];
+            xr[0] = xrs[0];
+            rotate_in_all<L>(D, xrs, xr, std::make_integer_sequence<int, L>{});
+            all_blocks<L, RADIAL>(a, ws, c, rad, D, xr, acc, std::make_integer_sequence<int, L + 1>{});
+          } else {
+            zero_len_terms<L, RADIAL>(a, ws, c, rad, xrs, acc, std::make_integer_sequence<int, K::P>{});
+          }
         }
-      } else {
-        group_sync(C, g);  // keeps one barrier per step (see above)
-        if (in_range) zero_len_terms<L, RADIAL>(a, c, rad, xrow, acc, std::make_integer_sequence<int, K::P>{});
+        group_sync(C, g);  // the staged row (and radial weights) are rewritten next
       }
     }
     __syncthreads();
@@ -358,9 +414,9 @@ __global__ void __launch_bounds__(kHlThreads) k_hl(const HlArgs a) {
 template <int L, bool RADIAL>
 eqmp_status launch_hl(const HlArgs& a, cudaStream_t st, const DeviceInfo& dev) {
   auto kern = k_hl<L, RADIAL>;
-  const int smem = HlCfg<L>::smem(a.C);
+  const int smem = HlCfg<L>::smem(a.C, RADIAL);
   static unsigned long long attr_done = 0;
-  if (ensure_smem_attr(kern, HlCfg<L>::SMEM, &attr_done) != cudaSuccess) return EQMP_ERR_CUDA;
+  if (ensure_smem_attr(kern, 227 * 1024, &attr_done) != cudaSuccess) return EQMP_ERR_CUDA;
   int occ = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kHlThreads, smem) != cudaSuccess || occ < 1)
     return EQMP_ERR_CUDA;

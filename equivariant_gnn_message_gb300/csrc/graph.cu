@@ -7,7 +7,9 @@
 // rounded on its own (no contraction into FMA):
 //     d_a = p_j[a] - p_i[a];  d2 = (d_x*d_x + d_y*d_y) + d_z*d_z;  edge iff d2 < r_c*r_c.
 //
-// Pipeline (all on the caller's stream, no host synchronisation):
+// Pipeline (all on the caller's stream, no host synchronisation; one
+// cooperative launch of k_graph_coop runs every phase with grid barriers in
+// between, or, where cooperative launches are unavailable, one kernel each):
 //   k_clear    zero the bucket counters
 //   k_bin      cell of each atom (cell side = r_c (1 + 2^-10)), hashed into
 //              H = 2^k >= 2N buckets; count atoms per bucket
@@ -27,6 +29,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include "common.cuh"
 #include "eqmp.h"
 #include "launch.h"
 
@@ -41,6 +44,9 @@ constexpr int kSortWarps = 8;
 constexpr int kSortCap = 512;          // row length sorted in shared memory
 constexpr float kCellRange = 4096.0f;  // |p| / cell side must stay below this
 constexpr long long kGraphMaxAtoms = 1ll << 30;  // keeps the bucket count <= 2^31
+constexpr int kCoopMaxBlocks = 2048;              // cooperative grid cap (block totals it can hold)
+constexpr long long kCoopMaxAtoms = 16384;        // the single launch is used up to this many atoms
+constexpr unsigned long long kGridWaitNs = 4000000000ull;
 
 // Cell coordinates hashed as in Teschner et al. 2003 (optimised spatial
 // hashing: XOR of coordinates times three large primes), then mixed by the
@@ -168,10 +174,9 @@ __global__ void k_clear(int32_t* __restrict__ a, long long n, int* __restrict__ 
   if (blockIdx.x == 0 && threadIdx.x == 0) *bad = 0;
 }
 
-__global__ void k_bin(const float* __restrict__ pos, int N, float inv, uint32_t mask, int32_t* __restrict__ atom_bucket,
-                      int32_t* __restrict__ count, int* __restrict__ bad) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= N) return;
+__device__ __forceinline__ void bin_one(int i, const float* __restrict__ pos, float inv, uint32_t mask,
+                                        int32_t* __restrict__ atom_bucket, int32_t* __restrict__ count,
+                                        int* __restrict__ bad) {
   const float3 p = load_pos(pos, i);
   const float qx = __fmul_rn(p.x, inv), qy = __fmul_rn(p.y, inv), qz = __fmul_rn(p.z, inv);
   // false for NaN as well as for out-of-range coordinates
@@ -182,18 +187,29 @@ __global__ void k_bin(const float* __restrict__ pos, int N, float inv, uint32_t 
   atomicAdd(count + h, 1);
 }
 
+__global__ void k_bin(const float* __restrict__ pos, int N, float inv, uint32_t mask, int32_t* __restrict__ atom_bucket,
+                      int32_t* __restrict__ count, int* __restrict__ bad) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < N) bin_one(i, pos, inv, mask, atom_bucket, count, bad);
+}
+
 // Atoms listed bucket by bucket, with a copy of their positions in the same
 // order, so that the neighbour walk reads candidates' positions contiguously.
-__global__ void k_scatter(const float* __restrict__ pos, int N, const int32_t* __restrict__ atom_bucket,
-                          const int32_t* __restrict__ start, int32_t* __restrict__ fill,
-                          int32_t* __restrict__ bucket_atoms, float4* __restrict__ bucket_pos) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= N) return;
+__device__ __forceinline__ void scatter_one(int i, const float* __restrict__ pos, const int32_t* __restrict__ atom_bucket,
+                                            const int32_t* __restrict__ start, int32_t* __restrict__ fill,
+                                            int32_t* __restrict__ bucket_atoms, float4* __restrict__ bucket_pos) {
   const int h = atom_bucket[i];
   const int slot = start[h] + atomicAdd(fill + h, 1);
   bucket_atoms[slot] = i;
   const float3 p = load_pos(pos, i);
   bucket_pos[slot] = make_float4(p.x, p.y, p.z, 0.0f);
+}
+
+__global__ void k_scatter(const float* __restrict__ pos, int N, const int32_t* __restrict__ atom_bucket,
+                          const int32_t* __restrict__ start, int32_t* __restrict__ fill,
+                          int32_t* __restrict__ bucket_atoms, float4* __restrict__ bucket_pos) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < N) scatter_one(i, pos, atom_bucket, start, fill, bucket_atoms, bucket_pos);
 }
 
 // ------------------------------------------------------------ neighbour walk
@@ -206,15 +222,11 @@ __global__ void k_scatter(const float* __restrict__ pos, int N, const int32_t* _
 // FILL = false: row_offsets[i] = degree of i (row_offsets[N] = 0).
 // FILL = true:  senders of i written, unsorted, to src[off[i] .. off[i+1]).
 template <bool FILL>
-__global__ void __launch_bounds__(kNeighThreads) k_neigh(const float4* __restrict__ bucket_pos, int N, float inv,
-                                                         float rc2, uint32_t mask, const int32_t* __restrict__ start,
-                                                         const int32_t* __restrict__ bucket_atoms,
-                                                         int32_t* __restrict__ row_offsets,
-                                                         int32_t* __restrict__ src, long long e_cap) {
-  const int lane = threadIdx.x & 31;
-  const long long wg = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (!FILL && wg == 0 && lane == 0) row_offsets[N] = 0;
-  if (wg >= N) return;  // warp-uniform
+__device__ __forceinline__ void neigh_row(long long wg, int lane, const float4* __restrict__ bucket_pos, float inv,
+                                          float rc2, uint32_t mask, const int32_t* __restrict__ start,
+                                          const int32_t* __restrict__ bucket_atoms,
+                                          int32_t* __restrict__ row_offsets, int32_t* __restrict__ src,
+                                          long long e_cap) {
   const int i = bucket_atoms[wg];  // the receiver sits at slot wg of the bucket order
   const float4 pw = bucket_pos[wg];
   const float3 pi = make_float3(pw.x, pw.y, pw.z);
@@ -269,27 +281,33 @@ __global__ void __launch_bounds__(kNeighThreads) k_neigh(const float4* __restric
   if (!FILL && lane == 0) row_offsets[i] = count;
 }
 
+template <bool FILL>
+__global__ void __launch_bounds__(kNeighThreads) k_neigh(const float4* __restrict__ bucket_pos, int N, float inv,
+                                                         float rc2, uint32_t mask, const int32_t* __restrict__ start,
+                                                         const int32_t* __restrict__ bucket_atoms,
+                                                         int32_t* __restrict__ row_offsets,
+                                                         int32_t* __restrict__ src, long long e_cap) {
+  const int lane = threadIdx.x & 31;
+  const long long wg = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (!FILL && wg == 0 && lane == 0) row_offsets[N] = 0;
+  if (wg < N) neigh_row<FILL>(wg, lane, bucket_pos, inv, rc2, mask, start, bucket_atoms, row_offsets, src, e_cap);
+}
+
 // ------------------------------------------------------------ row sort
 // One warp per receiver.  Senders in a row are distinct, so the rank of a
 // sender (the number of smaller ones) is its sorted position.  Rows up to
 // kSortCap are ranked from shared memory; longer rows are staged in the
 // row's own vec storage (3 words per edge, so it holds the row) and ranked
 // from there before vec is written.
-__global__ void __launch_bounds__(kSortWarps * 32) k_sort(const float* __restrict__ pos, int N,
-                                                          const int32_t* __restrict__ row_offsets,
-                                                          int32_t* __restrict__ src, float* __restrict__ vec,
-                                                          int32_t* __restrict__ dst, long long e_cap) {
-  __shared__ int32_t rows[kSortWarps][kSortCap];
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int i = blockIdx.x * kSortWarps + wid;
-  if (i >= N) return;
+__device__ __forceinline__ void sort_row(int i, int lane, int32_t* sm, const float* __restrict__ pos,
+                                         const int32_t* __restrict__ row_offsets, int32_t* __restrict__ src,
+                                         float* __restrict__ vec, int32_t* __restrict__ dst, long long e_cap) {
   const long long beg = row_offsets[i], end = row_offsets[i + 1];
   if (beg < 0 || end > e_cap || end < beg) return;
   const int k = (int)(end - beg);
   const float3 pi = load_pos(pos, i);
   int32_t* row = src + beg;
   if (k <= kSortCap) {
-    int32_t* sm = rows[wid];
     for (int a = lane; a < k; a += 32) sm[a] = row[a];
     __syncwarp();
     for (int a = lane; a < k; a += 32) {
@@ -326,13 +344,20 @@ __global__ void __launch_bounds__(kSortWarps * 32) k_sort(const float* __restric
   }
 }
 
+__global__ void __launch_bounds__(kSortWarps * 32) k_sort(const float* __restrict__ pos, int N,
+                                                          const int32_t* __restrict__ row_offsets,
+                                                          int32_t* __restrict__ src, float* __restrict__ vec,
+                                                          int32_t* __restrict__ dst, long long e_cap) {
+  __shared__ int32_t rows[kSortWarps][kSortCap];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int i = blockIdx.x * kSortWarps + wid;
+  if (i < N) sort_row(i, lane, rows[wid], pos, row_offsets, src, vec, dst, e_cap);
+}
+
 // rev[e] for e = (i <- j): the position of (j <- i) in row j (binary search;
 // the relation is symmetric, so it exists).
-__global__ void k_rev(int N, const int32_t* __restrict__ row_offsets, const int32_t* __restrict__ src,
-                      int32_t* __restrict__ rev, long long e_cap) {
-  const int lane = threadIdx.x & 31;
-  const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (i >= N) return;
+__device__ __forceinline__ void rev_row(int i, int lane, const int32_t* __restrict__ row_offsets,
+                                        const int32_t* __restrict__ src, int32_t* __restrict__ rev, long long e_cap) {
   const long long beg = row_offsets[i], end = row_offsets[i + 1];
   if (beg < 0 || end > e_cap || end < beg) return;
   for (long long e = beg + lane; e < end; e += 32) {
@@ -351,10 +376,153 @@ __global__ void k_rev(int N, const int32_t* __restrict__ row_offsets, const int3
   }
 }
 
+__global__ void k_rev(int N, const int32_t* __restrict__ row_offsets, const int32_t* __restrict__ src,
+                      int32_t* __restrict__ rev, long long e_cap) {
+  const int lane = threadIdx.x & 31;
+  const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (i < N) rev_row(i, lane, row_offsets, src, rev, e_cap);
+}
+
+// ------------------------------------------------------------ one launch
+// The whole pipeline in one cooperative launch (every CTA resident), the
+// phases separated by grid barriers: for small systems the twelve launches
+// of the multi-kernel path cost more than their work.
+struct CoopArgs {
+  const float* pos;
+  int N;
+  float inv, rc2;
+  uint32_t mask;
+  long long H, n_clear, e_cap;
+  int32_t *atom_bucket, *start, *fill, *bucket_atoms;
+  float4* bucket_pos;
+  int* bad;
+  long long* sums;     // [gridDim.x] block totals
+  unsigned* bar;       // [2]: arrivals, completed generations (zeroed before the launch)
+  int32_t *row_offsets, *src, *dst, *rev;
+  float* vec;
+  long long* e_total;
+  int* watchdog;
+};
+
+// Grid barrier with a bounded wait: false (and the watchdog set) if the
+// other CTAs did not all arrive within kGridWaitNs.
+__device__ __forceinline__ bool grid_sync(unsigned* bar, unsigned& gen, int* watchdog) {
+  __shared__ int ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    ++gen;
+    ok = 1;
+    __threadfence();
+    const unsigned arrived = atomicAdd(bar, 1u) + 1u;
+    if (arrived == gen * gridDim.x) {
+      __threadfence();
+      atomicExch(bar + 1, gen);
+    } else {
+      const unsigned long long t0 = global_ns();
+      while (*reinterpret_cast<volatile unsigned*>(bar + 1) < gen) {
+        if (global_ns() - t0 > kGridWaitNs) {
+          watchdog_trip(watchdog, 4);
+          ok = 0;
+          break;
+        }
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+  return ok != 0;
+}
+
+// Exclusive scan of data[0..n) across the grid: each CTA scans a contiguous
+// chunk (tiles of 1024 with a running carry), a barrier, then each CTA adds
+// the totals of the CTAs before it.  64-bit totals; *total_out (if given) =
+// the grand total, reported as for the multi-kernel path.
+__device__ bool grid_scan(int32_t* data, long long n, long long* sums, unsigned* bar, unsigned& gen, int* watchdog,
+                          const int* bad, long long* total_out) {
+  __shared__ long long warp_tot[32];
+  __shared__ long long total;
+  const long long chunk = (n + gridDim.x - 1) / gridDim.x;
+  const long long lo = min(n, (long long)blockIdx.x * chunk), hi = min(n, lo + chunk);
+  long long carry = 0;
+  for (long long base = lo; base < hi; base += 4 * blockDim.x) {
+    const long long i0 = base + 4 * threadIdx.x;
+    int v[4];
+    long long s = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      v[k] = i0 + k < hi ? data[i0 + k] : 0;
+      s += v[k];
+    }
+    long long run = carry + block_exclusive(s, warp_tot, &total);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (i0 + k < hi) data[i0 + k] = (int32_t)run;
+      run += v[k];
+    }
+    carry += total;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) sums[blockIdx.x] = carry;
+  if (!grid_sync(bar, gen, watchdog)) return false;
+  long long before = 0, all = 0;
+  for (unsigned b = threadIdx.x; b < gridDim.x; b += blockDim.x) {
+    const long long t = sums[b];
+    all += t;
+    if (b < blockIdx.x) before += t;
+  }
+  // block sums of `before` and `all` (fixed-order tree: integers, exact)
+  before = block_exclusive(before, warp_tot, &total), before = total;
+  __syncthreads();
+  all = block_exclusive(all, warp_tot, &total), all = total;
+  for (long long i = lo + threadIdx.x; i < hi; i += blockDim.x) data[i] += (int32_t)before;
+  if (total_out && blockIdx.x == 0 && threadIdx.x == 0) {
+    long long e = all;
+    if (e > INT32_MAX) e = -2;
+    if (*bad) e = -1;
+    *total_out = e;
+  }
+  return grid_sync(bar, gen, watchdog);
+}
+
+__global__ void __launch_bounds__(kSortWarps * 32) k_graph_coop(const CoopArgs g) {
+  __shared__ int32_t rows[kSortWarps][kSortCap];
+  unsigned gen = 0;
+  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long nthreads = (long long)gridDim.x * blockDim.x;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const long long warp0 = (long long)blockIdx.x * kSortWarps + wid, nwarps = (long long)gridDim.x * kSortWarps;
+  for (long long i = tid; i < g.n_clear; i += nthreads) g.start[i] = 0;
+  if (tid == 0) *g.bad = 0;
+  if (!grid_sync(g.bar, gen, g.watchdog)) return;
+  for (long long i = tid; i < g.N; i += nthreads) bin_one((int)i, g.pos, g.inv, g.mask, g.atom_bucket, g.start, g.bad);
+  if (!grid_sync(g.bar, gen, g.watchdog)) return;
+  if (!grid_scan(g.start, g.H + 1, g.sums, g.bar, gen, g.watchdog, g.bad, nullptr)) return;
+  for (long long i = tid; i < g.N; i += nthreads)
+    scatter_one((int)i, g.pos, g.atom_bucket, g.start, g.fill, g.bucket_atoms, g.bucket_pos);
+  if (!grid_sync(g.bar, gen, g.watchdog)) return;
+  if (tid == 0) g.row_offsets[g.N] = 0;
+  for (long long w = warp0; w < g.N; w += nwarps)
+    neigh_row<false>(w, lane, g.bucket_pos, g.inv, g.rc2, g.mask, g.start, g.bucket_atoms, g.row_offsets, nullptr,
+                     g.e_cap);
+  if (!grid_sync(g.bar, gen, g.watchdog)) return;
+  if (!grid_scan(g.row_offsets, (long long)g.N + 1, g.sums, g.bar, gen, g.watchdog, g.bad, g.e_total)) return;
+  if (g.e_cap <= 0) return;
+  for (long long w = warp0; w < g.N; w += nwarps)
+    neigh_row<true>(w, lane, g.bucket_pos, g.inv, g.rc2, g.mask, g.start, g.bucket_atoms, g.row_offsets, g.src,
+                    g.e_cap);
+  if (!grid_sync(g.bar, gen, g.watchdog)) return;
+  for (long long i = warp0; i < g.N; i += nwarps)
+    sort_row((int)i, lane, rows[wid], g.pos, g.row_offsets, g.src, g.vec, g.dst, g.e_cap);
+  if (!g.rev) return;
+  if (!grid_sync(g.bar, gen, g.watchdog)) return;
+  for (long long i = warp0; i < g.N; i += nwarps) rev_row((int)i, lane, g.row_offsets, g.src, g.rev, g.e_cap);
+}
+
 // ------------------------------------------------------------ workspace
 struct GraphWs {
   long long H = 0;
-  size_t atom_bucket = 0, start = 0, fill = 0, bucket_atoms = 0, bucket_pos = 0, sums = 0, bad = 0, bytes = 0;
+  size_t atom_bucket = 0, start = 0, fill = 0, bucket_atoms = 0, bucket_pos = 0, sums = 0, bad = 0, coop = 0,
+         bytes = 0;
 };
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -374,6 +542,7 @@ GraphWs graph_ws(long long N) {
   w.bucket_pos = o;  o = align256(o + 16 * (size_t)N);
   w.sums = o;        o = align256(o + 8 * (size_t)nb);
   w.bad = o;         o = align256(o + 4);
+  w.coop = o;        o = align256(o + 8 * (size_t)kCoopMaxBlocks + 16);  // block totals + barrier words
   w.bytes = o;
   return w;
 }
@@ -419,6 +588,48 @@ eqmp_status eqmp_radius_graph(const float* pos, int64_t N, float cutoff, int32_t
   const float rc2 = cutoff * cutoff;
   const uint32_t mask = (uint32_t)(w.H - 1);
   const int nblk = (int)((N + kNeighThreads - 1) / kNeighThreads);
+
+  // One cooperative launch when the device allows it (grid sized to the
+  // work: one warp per receiver, at most what is resident at once).
+  {
+    static int occ_cache[64] = {0};
+    int d = 0;
+    cudaGetDevice(&d);
+    int occ = __atomic_load_n(&occ_cache[d & 63], __ATOMIC_RELAXED);
+    if (occ == 0) {
+      int coop = 0;
+      if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, d) != cudaSuccess) return EQMP_ERR_CUDA;
+      if (!coop || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_graph_coop, kSortWarps * 32, 0) !=
+                       cudaSuccess || occ < 1)
+        occ = -1;  // multi-kernel path only
+      __atomic_store_n(&occ_cache[d & 63], occ, __ATOMIC_RELAXED);
+    }
+    DeviceInfo dev;
+    // measured: one launch wins while the launches dominate (up to ~10k
+    // atoms); above that the per-phase launch shapes of the multi-kernel
+    // path are faster
+    if (occ > 0 && N <= kCoopMaxAtoms && device_info(&dev) == EQMP_OK) {
+      long long grid = (long long)dev.sms * occ;
+      const long long want = (N + kSortWarps - 1) / kSortWarps;
+      if (grid > want) grid = want > 0 ? want : 1;
+      if (grid > kCoopMaxBlocks) grid = kCoopMaxBlocks;
+      CoopArgs g{};
+      g.pos = pos; g.N = (int)N; g.inv = inv; g.rc2 = rc2; g.mask = mask; g.H = w.H; g.n_clear = n_clear;
+      g.e_cap = E_cap; g.atom_bucket = atom_bucket; g.start = start; g.fill = fill; g.bucket_atoms = bucket_atoms;
+      g.bucket_pos = bucket_pos; g.bad = bad;
+      g.sums = reinterpret_cast<long long*>(base + w.coop);
+      g.bar = reinterpret_cast<unsigned*>(base + w.coop + 8 * (size_t)kCoopMaxBlocks);
+      g.row_offsets = row_offsets; g.src = src; g.dst = dst; g.rev = rev; g.vec = vec;
+      g.e_total = reinterpret_cast<long long*>(E_total);
+      g.watchdog = dev.watchdog;
+      if (cudaMemsetAsync(g.bar, 0, 2 * sizeof(unsigned), st) != cudaSuccess) return EQMP_ERR_CUDA;
+      void* params[] = {&g};
+      const cudaError_t err = cudaLaunchCooperativeKernel((const void*)k_graph_coop, dim3((unsigned)grid),
+                                                          dim3(kSortWarps * 32), params, 0, st);
+      if (err == cudaSuccess) return EQMP_OK;
+      (void)cudaGetLastError();  // fall through to the multi-kernel path
+    }
+  }
 
   k_clear<<<256, 256, 0, st>>>(start, n_clear, bad);
   if (N > 0) {

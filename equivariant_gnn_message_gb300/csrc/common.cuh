@@ -23,7 +23,8 @@ namespace eqmp {
 // The watchdog word lives in device memory owned by the library (one per
 // device); kernels receive its address.  It becomes nonzero once any
 // bounded wait has given up and is read and cleared by eqmp_device_error().
-// Codes: 1 consumer full-wait, 2 producer empty-wait, 3 producer drain.
+// Codes: 1 consumer full-wait, 2 producer empty-wait, 3 producer drain,
+// 4 grid barrier of the single-launch radius graph.
 
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s
 

@@ -291,7 +291,9 @@ eqmp_status eqmp_validate_graph(const int32_t* row_offsets, const int32_t* src, 
 /*
  * Reads and clears the current device's watchdog word (synchronises the
  * device).  *code = 0 when no bounded wait has given up since the last
- * call; otherwise a nonzero code naming the wait.  A nonzero code means the
+ * call; otherwise a nonzero code naming the wait: 1 a consumer waiting for
+ * a gathered row, 2 a producer waiting for a free slot, 3 a producer
+ * draining its last slots, 4 a grid barrier of eqmp_radius_graph.  A nonzero code means the
  * outputs of the kernels since the last call are unspecified.  Returns
  * EQMP_ERR_DEVICE_TIMEOUT when *code != 0.
  */

@@ -28,7 +28,7 @@ __all__ = [
     "EqmpError", "load_library", "library_path", "eqmp_num_paths", "eqmp_path_table",
     "eqmp_status_string", "eqmp_sh", "eqmp_tp_scatter", "eqmp_fused", "eqmp_fused_so2", "eqmp_validate_graph",
     "eqmp_device_error", "eqmp_fused_backward", "eqmp_fused_backward_noalloc", "eqmp_radius_graph", "eqmp_fused_lmax",
-    "eqmp_num_paths_lmax", "sender_view", "EQMP_OK", "EQMP_ERR_INVALID_ARG", "EQMP_ERR_UNSUPPORTED",
+    "eqmp_num_paths_lmax", "eqmp_watchdog_selftest", "sender_view", "EQMP_OK", "EQMP_ERR_INVALID_ARG", "EQMP_ERR_UNSUPPORTED",
     "EQMP_ERR_CUDA", "EQMP_ERR_DEVICE_TIMEOUT", "EQMP_ERR_GRAPH",
 ]
 
@@ -89,6 +89,8 @@ def load_library():
     lib.eqmp_fused_backward.argtypes = [vp, vp, i64, vp, vp, vp, vp, vp, i64, i64, i64, i32, Weights,
                                         vp, vp, vp, vp, vp, vp, vp, i64, vp]
     lib.eqmp_fused_backward.restype = i32
+    lib.eqmp_watchdog_selftest.argtypes = [i32, vp]
+    lib.eqmp_watchdog_selftest.restype = i32
     lib.eqmp_num_paths_lmax.argtypes = [i32]
     lib.eqmp_num_paths_lmax.restype = i32
     lib.eqmp_fused_lmax.argtypes = [i32, vp, vp, i64, vp, vp, i64, i64, i32, Weights, vp, vp]
@@ -246,6 +248,11 @@ def eqmp_device_error():
     if st not in (EQMP_OK, EQMP_ERR_DEVICE_TIMEOUT):
         _check(st, "eqmp_device_error")
     return int(code.value)
+
+
+def eqmp_watchdog_selftest(wait_ms=20, stream=None):
+    """Launch the watchdog self-test (a wait that must give up); read the code with eqmp_device_error()."""
+    _check(load_library().eqmp_watchdog_selftest(int(wait_ms), _stream(stream)), "eqmp_watchdog_selftest")
 
 
 def eqmp_num_paths_lmax(l_max):

@@ -62,6 +62,27 @@ __global__ void k_validate(const int32_t* __restrict__ off, const int32_t* __res
   }
 }
 
+// ------------------------------------------------------------ watchdog self-test
+// One thread waits on an mbarrier that nothing will ever complete, with a
+// limit of limit_ns; when the wait gives up it records code 5 in the
+// watchdog word and the kernel ends.  Shows on a live GPU that an expired
+// wait is reported to the host and leaves the context usable, without any
+// fault or hang.
+__global__ void k_wait_selftest(unsigned long long limit_ns, int* watchdog) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  fence_mbar_init();
+  const unsigned long long t0 = global_ns();
+  while (!mbar_test_wait(b, 0)) {
+    if (global_ns() - t0 > limit_ns) {
+      watchdog_trip(watchdog, 5);
+      break;
+    }
+  }
+}
+
 // ------------------------------------------------------------ device state
 eqmp_status device_info(DeviceInfo* out) {
   static std::once_flag once[64];
@@ -242,6 +263,16 @@ eqmp_status eqmp_validate_graph(const int32_t* row_offsets, const int32_t* src, 
     return EQMP_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return EQMP_ERR_CUDA;
   return h ? EQMP_ERR_GRAPH : EQMP_OK;
+}
+
+eqmp_status eqmp_watchdog_selftest(int32_t wait_ms, eqmp_stream_t stream) {
+  if (wait_ms < 1 || wait_ms > 1000) return EQMP_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  eqmp_status s = device_info(&dev);
+  if (s != EQMP_OK) return s;
+  k_wait_selftest<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      (unsigned long long)wait_ms * 1000000ull, dev.watchdog);
+  return cuda_status(cudaGetLastError());
 }
 
 eqmp_status eqmp_device_error(int32_t* code) {

@@ -293,11 +293,21 @@ eqmp_status eqmp_validate_graph(const int32_t* row_offsets, const int32_t* src, 
  * device).  *code = 0 when no bounded wait has given up since the last
  * call; otherwise a nonzero code naming the wait: 1 a consumer waiting for
  * a gathered row, 2 a producer waiting for a free slot, 3 a producer
- * draining its last slots, 4 a grid barrier of eqmp_radius_graph.  A nonzero code means the
+ * draining its last slots, 4 a grid barrier of eqmp_radius_graph, 5 the
+ * self-test below.  A nonzero code means the
  * outputs of the kernels since the last call are unspecified.  Returns
  * EQMP_ERR_DEVICE_TIMEOUT when *code != 0.
  */
 eqmp_status eqmp_device_error(int32_t* code);
+
+/*
+ * Self-test of the failure reporting above: launches one thread that waits
+ * on a barrier nothing completes, with a limit of wait_ms milliseconds
+ * (1..1000, else EQMP_ERR_INVALID_ARG).  The wait gives up and records
+ * code 5; the next eqmp_device_error returns EQMP_ERR_DEVICE_TIMEOUT with
+ * *code = 5, and the device stays usable.  Nothing faults or hangs.
+ */
+eqmp_status eqmp_watchdog_selftest(int32_t wait_ms, eqmp_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -129,7 +129,9 @@ eqmp_status eqmp_tp_scatter(const float* Y, const void* x, int64_t N_src, eqmp_d
  * The fused layer: SH in registers + CG tensor product + receiver sum in one
  * kernel, each edge vector read once and each output row written once
  * (Batmobile blog, section "3. 操作融合").  Arguments as eqmp_tp_scatter,
- * with vec [E][3] fp32 (4-byte aligned) in place of Y.
+ * with vec [E][3] fp32 (4-byte aligned) in place of Y.  With radial
+ * weights it runs the aligned-frame schedule of eqmp_fused_so2 (the same
+ * result; fewer FMAs when the weights change per edge).
  */
 eqmp_status eqmp_fused(const float* vec, const void* x, int64_t N_src, eqmp_dtype x_dtype,
                        const int32_t* row_offsets, const int32_t* src, int64_t N, int64_t E,

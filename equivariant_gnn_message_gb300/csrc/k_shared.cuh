@@ -111,7 +111,7 @@ struct SharedCfg {
   static_assert(ROW_BYTES % 128 == 0, "row must be whole 128-byte lines");
 };
 
-// Consumers read ahead this many edges (the producer pads as many empty
+// The backward kernel's consumers read ahead this many edges (its producer pads as many empty
 // edges after the last real one).
 constexpr uint32_t kLookAhead = 2;
 
@@ -275,8 +275,9 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
   float4* ys = reinterpret_cast<float4*>(smem + K::OFF_Y);
   float* red = reinterpret_cast<float*>(smem + K::OFF_RED);
   float* ws = reinterpret_cast<float*>(smem + K::OFF_W);
+  constexpr int SP = S / 2;  // slot pairs: ordinals 2p and 2p+1 share one full and one empty barrier
   const uint32_t full0 = smem_u32(smem + K::OFF_BAR);
-  const uint32_t empty0 = full0 + 8 * S;
+  const uint32_t empty0 = full0 + 8 * SP;
   const int tid = threadIdx.x;
 
   // Contiguous receiver range of this CTA, balanced on edges + 3 per
@@ -285,9 +286,9 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
   const int2 rr = balanced_range(a.off, a.N, gridDim.x, blockIdx.x, kReceiverCost);
   const int r_begin = rr.x, r_end = rr.y;
 
-  if (tid < S) {
-    mbar_init(full0 + 8 * tid, 1);
-    mbar_init(empty0 + 8 * tid, K::NCONS);  // every consumer thread releases
+  if (tid < SP) {
+    mbar_init(full0 + 8 * tid, 1);          // the even ordinal's arrive (+ the rows' bytes)
+    mbar_init(empty0 + 8 * tid, K::NCONS);  // every consumer thread releases the pair
     fence_mbar_init();
   }
   __syncthreads();  // barriers initialised; the producer starts at once
@@ -315,8 +316,14 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
     // this round the warp issued its previous 32 edges (up to 32 NP ordinals
     // back), whose empty-waits proved every ordinal up to that point minus S
     // released; YR >= 32 NP + S.  Each lane's arrive publishes its own SH.
+    // Slots come in pairs (ordinals 2p, 2p+1, one full and one empty barrier
+    // per pair): CH is even, so a pair always falls to one warp, on lanes
+    // 2i and 2i+1 of the same batch, and the even lane (which runs first)
+    // waits for the pair to be free, arms its full barrier with the bytes
+    // of both rows (one row if the odd ordinal is past the end), and the odd
+    // lane only adds its copy.
     constexpr int CH = S / K::NP;
-    static_assert(CH >= 1 && 32 % CH == 0 && K::YR >= 32 * K::NP + S, "producer layout");
+    static_assert(CH >= 2 && CH % 2 == 0 && 32 % CH == 0 && K::YR >= 32 * K::NP + S, "producer layout");
     const int pw = K::WS ? tid >> 5 : 0;  // producer warp index (the non-specialised CTA has one)
     if (pw >= K::NP) return;              // warpgroup 0 has 4 warps; NP of them produce
     const int lane = tid & 31;
@@ -349,7 +356,7 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
     int node_nx;
     float vx_nx, vy_nx, vz_nx;
     load_edge(ordinal(0), node_nx, vx_nx, vy_nx, vz_nx);
-    uint32_t last = 0;  // this warp's last issued ordinal + 1 (0: none)
+    uint32_t lastp = 0;  // this warp's last issued pair + 1 (0: none)
     for (int g = 0; ok; ++g) {
       const uint32_t n = ordinal(g);
       const uint32_t cnt = (uint32_t)__popc(__ballot_sync(0xffffffffu, n < (uint32_t)total));
@@ -368,46 +375,50 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
       for (uint32_t j = 0; j < cnt; ++j) {
         int good = 1;
         if ((uint32_t)lane == j) {
-          const uint32_t s = n % S, par = ((n / S) & 1u) ^ 1u;
-          if (mbar_try_wait(empty0 + 8 * s, par) || mbar_wait(empty0 + 8 * s, par, a.watchdog, 2)) {
-            mbar_arrive_expect_tx(full0 + 8 * s, TX);
-            tma_load_2d(smem_u32(smem + K::OFF_X + s * K::SLOT), &tmap, 0, node * K::ROWS,
-                        full0 + 8 * s);
+          const uint32_t pr = n >> 1, sp = pr % SP, par = ((pr / SP) & 1u) ^ 1u;
+          const uint32_t fb = full0 + 8 * sp;
+          bool go = true;
+          if ((n & 1u) == 0) {
+            go = mbar_try_wait(empty0 + 8 * sp, par) || mbar_wait(empty0 + 8 * sp, par, a.watchdog, 2);
+            if (go) mbar_arrive_expect_tx(fb, n + 1 < (uint32_t)total ? 2 * TX : TX);
+          }
+          if (go) {
+            tma_load_2d(smem_u32(smem + K::OFF_X + (n % S) * K::SLOT), &tmap, 0, node * K::ROWS, fb);
             if constexpr (!FROM_VEC)
-              bulk_load(smem_u32(yd), a.Y + 16 * (size_t)(e_begin + (int)n), 64, full0 + 8 * s);
+              bulk_load(smem_u32(yd), a.Y + 16 * (size_t)(e_begin + (int)n), 64, fb);
           } else {
             good = 0;
           }
         }
         if (!__all_sync(0xffffffffu, good)) { ok = false; break; }
       }
-      if (ok) last = __shfl_sync(0xffffffffu, n, (int)cnt - 1) + 1;
+      if (ok) lastp = (__shfl_sync(0xffffffffu, n, (int)cnt - 1) >> 1) + 1;
     }
-    // Tail: empty edges at ordinals total and total+1 (phase completed by a
-    // plain arrive, no data), each issued by the warp that owns its slot
-    // after all its real edges, so the consumers' two-edge look-ahead never
-    // waits on a slot that is not coming.
-#pragma unroll
-    for (uint32_t t = 0; t < kLookAhead; ++t) {
-      const uint32_t n = (uint32_t)total + t;
-      if (ok && pw == (int)((n / CH) % K::NP)) {
+    // Tail: one empty pair after the last pair holding a real edge (phase
+    // completed by a plain arrive, no data), issued by the warp that owns it
+    // after all its real edges, so the consumers' one-pair look-ahead never
+    // waits on a pair that is not coming.
+    {
+      const uint32_t pr = ((uint32_t)total + 1) >> 1;
+      if (ok && pw == (int)((2 * pr / CH) % K::NP)) {
         if (lane == 0) {
-          const uint32_t s = n % S, par = ((n / S) & 1u) ^ 1u;
-          if (mbar_try_wait(empty0 + 8 * s, par) || mbar_wait(empty0 + 8 * s, par, a.watchdog, 2))
-            mbar_arrive(full0 + 8 * s);
+          const uint32_t sp = pr % SP, par = ((pr / SP) & 1u) ^ 1u;
+          if (mbar_try_wait(empty0 + 8 * sp, par) || mbar_wait(empty0 + 8 * sp, par, a.watchdog, 2))
+            mbar_arrive(full0 + 8 * sp);
         }
-        last = n + 1;  // the tail is this warp's latest ordinal on its slot
+        lastp = pr + 1;  // the tail is this warp's latest pair on its barriers
       }
     }
-    // Drain: wait until this warp's loads among the last S ordinals have
+    // Drain: wait until this warp's loads among the last SP pairs have
     // landed, so no bulk copy of this warp is in flight when it leaves.  The
-    // window [last - S, last) holds exactly the latest ordinal of each slot,
-    // so every phase waited for is the current or the one just completed.
-    if (lane == 0 && last > 0) {
-      const uint32_t first = last > (uint32_t)S ? last - S : 0;
-      for (uint32_t i = first; i < last; ++i)
-        if ((i / CH) % K::NP == (uint32_t)pw)
-          if (!mbar_wait(full0 + 8 * (i % S), (i / S) & 1u, a.watchdog, 3)) break;
+    // window [lastp - SP, lastp) holds exactly the latest pair of each
+    // barrier, so every phase waited for is the current or the one just
+    // completed.
+    if (lane == 0 && lastp > 0) {
+      const uint32_t first = lastp > (uint32_t)SP ? lastp - SP : 0;
+      for (uint32_t i = first; i < lastp; ++i)
+        if ((2 * i / CH) % K::NP == (uint32_t)pw)
+          if (!mbar_wait(full0 + 8 * (i % SP), (i / SP) & 1u, a.watchdog, 3)) break;
     }
     return;
   }
@@ -447,19 +458,20 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
   uint32_t n = 0;  // ordinal of the CTA's next edge
   int buf = 0;
   bool failed = false;
-  // Edge m lives in slot m % S, phase (m / S) & 1, with its SH in ring entry
-  // m % YR.  A cursor holds these for one ordinal (full barrier address,
-  // parity, byte offsets of the slot and of the SH entry) and steps to the
-  // next ordinal with a few warp-uniform adds and selects, so the edge loop
-  // never recomputes them from the ordinal.
+  // Edge m lives in slot m % S with its SH in ring entry m % YR; edges 2p
+  // and 2p+1 share the barriers of pair p (index p % SP, phase (p / SP) & 1).
+  // A cursor holds these for one pair (full barrier address, parity, byte
+  // offsets of the even edge's slot and SH entry; the odd edge's are one
+  // slot and one entry further) and steps to the next pair with a few
+  // warp-uniform adds and selects.
   struct Cursor {
     uint32_t bar, par, xs, ys;
   };
   auto advance = [&](Cursor& u) {
     u.bar += 8;
-    u.xs += K::SLOT;
-    u.ys += 64;
-    if (u.bar == full0 + 8 * S) {
+    u.xs += 2 * K::SLOT;
+    u.ys += 128;
+    if (u.bar == full0 + 8 * SP) {
       u.bar = full0;
       u.xs = K::OFF_X;
       u.par ^= 1u;
@@ -470,43 +482,34 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
     if (!mbar_try_wait(u.bar, u.par))
       if (!mbar_wait_slow(u.bar, u.par, a.watchdog, 1, failed)) failed = true;
   };
-  auto load_cur = [&](const Cursor& u, float2 (&yv)[8], float (&xv)[KQ]) {
-    const float4* yp = reinterpret_cast<const float4*>(smem + u.ys);
+  // Registers of one edge of the pair at the cursor (h = 0 even, 1 odd).
+  auto load_half = [&](const Cursor& u, int h, float2 (&yv)[8], float (&xv)[KQ]) {
+    const float4* yp = reinterpret_cast<const float4*>(smem + u.ys + 64 * h);
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      const float4 t = yp[h];
-      yv[2 * h] = make_float2(t.x, t.y);
-      yv[2 * h + 1] = make_float2(t.z, t.w);
+    for (int k = 0; k < 4; ++k) {
+      const float4 t = yp[k];
+      yv[2 * k] = make_float2(t.x, t.y);
+      yv[2 * k + 1] = make_float2(t.z, t.w);
     }
-    load_x<XT, KQ>(smem + u.xs, xo, xv);
+    load_x<XT, KQ>(smem + u.xs + K::SLOT * h, xo, xv);
   };
-  // The look-ahead cursor `la` is two ordinals past the edge being summed.
-  // One edge: test (non-blocking) that the look-ahead edge has landed, run
-  // the FMAs of the edge held in (yv, xv) from registers, release its slot
-  // (every consumer thread arrives on its empty barrier, 8 S bytes past the
-  // full one), then (waiting only if the early test failed) load the
-  // look-ahead edge into the registers just freed and step the cursor.
+  // Registers A hold the even edge of the current pair, B the odd one; `la`
+  // is the next pair (the look-ahead).  A whole pair: test (non-blocking)
+  // that the next pair has landed, run A's FMAs, (waiting only if the test
+  // failed) load the next even edge into A, run B's FMAs, release the pair
+  // (every consumer thread arrives on its empty barrier, 8 SP bytes past the
+  // full one), load the next odd edge into B, step the cursor.  A receiver
+  // that starts or ends inside a pair runs the half of it that is its own;
+  // the pair is released once both halves are summed.
   Cursor la = {full0, 0u, (uint32_t)K::OFF_X, (uint32_t)K::OFF_Y};
-  auto step = [&](float2 (&acc)[KQ][8], float2 (&yv)[8], float (&xv)[KQ], uint32_t& bar) {
-    const bool ready = mbar_test_wait(la.bar, la.par);
-    fma_edge(acc, yv, xv);
-    mbar_arrive(bar + 8 * S);
-    if (!ready) wait_cur(la);
-    load_cur(la, yv, xv);
-    bar = la.bar;
-    advance(la);
-  };
   float2 yA[8], yB[8];
   float xA[KQ], xB[KQ];
-  uint32_t barA, barB;
   wait_cur(la);
-  load_cur(la, yA, xA);
-  barA = la.bar;
+  load_half(la, 0, yA, xA);
+  load_half(la, 1, yB, xB);
+  uint32_t barP = la.bar;
   advance(la);
-  wait_cur(la);
-  load_cur(la, yB, xB);
-  barB = la.bar;
-  advance(la);
+  bool half = false;  // the next edge is the odd one of the loaded pair
   for (int r = r_begin; r < r_end; ++r) {
     if (r - chunk == 32) {
       chunk += 32;
@@ -525,28 +528,35 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
 #pragma unroll
       for (int k = 0; k < 8; ++k) acc[i][k] = make_float2(0.0f, 0.0f);
 
-    // Two edges per trip; registers A hold edge n, B edge n+1.  The
-    // look-ahead may reach the producer's empty tail edges (never used).
     int j = 0;
-    for (; j + 2 <= deg; j += 2, n += 2) {
-      step(acc, yA, xA, barA);
-      step(acc, yB, xB, barB);
+    if (half && deg > 0) {  // the receiver starts on the odd edge: finish that pair
+      const bool ready = mbar_test_wait(la.bar, la.par);
+      fma_edge(acc, yB, xB);
+      mbar_arrive(barP + 8 * SP);
+      if (!ready) wait_cur(la);
+      load_half(la, 0, yA, xA);
+      load_half(la, 1, yB, xB);
+      barP = la.bar;
+      advance(la);
+      half = false;
+      j = 1;
     }
-    if (j < deg) {  // odd degree: edge n from A, then A takes n+1 and B loads n+2
+    for (; j + 2 <= deg; j += 2) {
       const bool ready = mbar_test_wait(la.bar, la.par);
       fma_edge(acc, yA, xA);
-      mbar_arrive(barA + 8 * S);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) yA[k] = yB[k];
-#pragma unroll
-      for (int i = 0; i < KQ; ++i) xA[i] = xB[i];
-      barA = barB;
       if (!ready) wait_cur(la);
-      load_cur(la, yB, xB);
-      barB = la.bar;
+      load_half(la, 0, yA, xA);
+      fma_edge(acc, yB, xB);
+      mbar_arrive(barP + 8 * SP);
+      load_half(la, 1, yB, xB);
+      barP = la.bar;
       advance(la);
-      ++n;
     }
+    if (j < deg) {  // the receiver ends on an even edge: the odd one is the next receiver's
+      fma_edge(acc, yA, xA);
+      half = true;
+    }
+    n += (uint32_t)deg;
 
     float part[16];
 #pragma unroll

@@ -44,9 +44,9 @@ FLUSH_BYTES = 256 << 20
 # tag, which makes its entry missing (traffic null) until re-captured.
 KERNEL_VERSION = {"shared": "k_shared-pairs-v3", "radial": "k_so2-v2"}
 NCU_TRAFFIC = {
-    ("pages_1k_c32", "k_shared-cursor-v2"): 2360576 + 0,
-    ("scale_100k_c64", "k_shared-cursor-v2"): 6206180352 + 406954496,
-    ("dense_10k_c128_bf16", "k_shared-cursor-v2"): 48816128 + 12697088,
+    ("pages_1k_c32", "k_shared-pairs-v3"): 2360000 + 7940,
+    ("scale_100k_c64", "k_shared-pairs-v3"): 6213447000 + 407233792,
+    ("dense_10k_c128_bf16", "k_shared-pairs-v3"): 48790000 + 11480000,
     ("radial_1k_c32", "k_radial-v1"): 2883584 + 0,
 }
 

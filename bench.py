@@ -42,7 +42,7 @@ FLUSH_BYTES = 256 << 20
 # profiles/ (None until captured for the current kernel version).
 # Keyed by (workload, kernel version); a changed kernel gets a new version
 # tag, which makes its entry missing (traffic null) until re-captured.
-KERNEL_VERSION = {"shared": "k_shared-pairs-v3", "radial": "k_so2-v2"}
+KERNEL_VERSION = {"shared": "k_shared-pairs-v4", "radial": "k_so2-v3"}
 NCU_TRAFFIC = {
     ("pages_1k_c32", "k_shared-pairs-v3"): 2360000 + 7940,
     ("scale_100k_c64", "k_shared-pairs-v3"): 6213447000 + 407233792,

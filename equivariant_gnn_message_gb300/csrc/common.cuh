@@ -102,6 +102,16 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The dynamic shared-memory array advanced to the next multiple of A bytes.
+// The result is the array plus an offset (not a pointer rebuilt from an
+// integer), so the compiler still knows it points into shared memory and
+// addresses it with 32-bit shared loads and stores.
+template <uint32_t A>
+__device__ __forceinline__ uint8_t* smem_align(uint8_t* raw) {
+  const uint32_t base = smem_u32(raw);
+  return raw + (((base + (A - 1)) & ~(A - 1)) - base);
+}
+
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }

@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(BwdSwCfg<C>::NTHREADS, BwdSwCfg<C>::MIN_BLOCKS
   using K = BwdSwCfg<C>;
   constexpr int S = K::S, KQ = 4;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align<1024>(smem_raw);
   float4* ys = reinterpret_cast<float4*>(smem + K::OFF_Y);
   float* dyr = reinterpret_cast<float*>(smem + K::OFF_DY);  // [S][NCW][16]
   float* dwq = reinterpret_cast<float*>(smem + K::OFF_DW);  // [NQ][34][C]

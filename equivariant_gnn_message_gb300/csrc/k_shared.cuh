@@ -270,8 +270,7 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
   using K = SharedCfg<C, KQ, XT, FROM_VEC>;
   constexpr int S = K::S;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align<1024>(smem_raw);
   float4* ys = reinterpret_cast<float4*>(smem + K::OFF_Y);
   float* red = reinterpret_cast<float*>(smem + K::OFF_RED);
   float* ws = reinterpret_cast<float*>(smem + K::OFF_W);

@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(So2Cfg<C, XT, RADIAL>::NTHREADS, So2Cfg<C, XT,
   using K = So2Cfg<C, XT, RADIAL>;
   constexpr int S = K::S;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align<1024>(smem_raw);
   float* ering = reinterpret_cast<float*>(smem + K::OFF_E);
   float* red = reinterpret_cast<float*>(smem + K::OFF_RED);
   float2* Ms = reinterpret_cast<float2*>(smem + K::OFF_M);

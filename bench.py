@@ -44,10 +44,10 @@ FLUSH_BYTES = 256 << 20
 # tag, which makes its entry missing (traffic null) until re-captured.
 KERNEL_VERSION = {"shared": "k_shared-pairs-v4", "radial": "k_so2-v3"}
 NCU_TRAFFIC = {
-    ("pages_1k_c32", "k_shared-pairs-v3"): 2360000 + 7940,
-    ("scale_100k_c64", "k_shared-pairs-v3"): 6213447000 + 407233792,
-    ("dense_10k_c128_bf16", "k_shared-pairs-v3"): 48790000 + 11480000,
-    ("radial_1k_c32", "k_radial-v1"): 2883584 + 0,
+    ("pages_1k_c32", "k_shared-pairs-v4"): 2357248 + 0,
+    ("scale_100k_c64", "k_shared-pairs-v4"): 6209806592 + 406970112,
+    ("dense_10k_c128_bf16", "k_shared-pairs-v4"): 48810496 + 11308544,
+    ("radial_1k_c32", "k_so2-v3"): 2888960 + 0,
 }
 
 

@@ -61,7 +61,10 @@ struct HlCfg {
     for (int j = 1; j < l; ++j) o += (2 * j + 1) * stride(j);
     return o;
   }
-  static constexpr int DS = (off(L + 1) + 31) / 32 * 32;  // floats per edge slot (D_1..D_L)
+  // Floats per edge slot (D_1..D_L): a multiple of 4 (rows are read as
+  // float4s) that is 4 more than a multiple of 32, so the builders of a batch
+  // (thread j writes slot j) spread over the banks (2-way, not 16-way).
+  static constexpr int DS = (off(L + 1) + 31) / 32 * 32 + 4;
   static constexpr int XV = (NC + 3) / 4;                  // float4s of a staged row per thread
   // floats: a batch of kBatch edge slots (+ zero-length flags), the
   // accumulators of every thread [NC][128], the staged sender rows

@@ -42,7 +42,7 @@ FLUSH_BYTES = 256 << 20
 # profiles/ (None until captured for the current kernel version).
 # Keyed by (workload, kernel version); a changed kernel gets a new version
 # tag, which makes its entry missing (traffic null) until re-captured.
-KERNEL_VERSION = {"shared": "k_shared-pairs-v4", "radial": "k_so2-v3"}
+KERNEL_VERSION = {"shared": "k_shared-pairs-v5", "radial": "k_so2-v4"}
 NCU_TRAFFIC = {
     ("pages_1k_c32", "k_shared-pairs-v4"): 2357248 + 0,
     ("scale_100k_c64", "k_shared-pairs-v4"): 6209806592 + 406970112,

@@ -55,7 +55,10 @@ __device__ __forceinline__ int split_probe(int lo, int hi, int lane) {
   return lo + (int)(((lane + 1) * d + 31) / 32) - 1;
 }
 
-__device__ __forceinline__ int2 balanced_range(const int* __restrict__ off, int N, int G, int b, int alpha) {
+// Returns (x, y, off[x], off[y]); the offsets are as loaded, unclamped.  The
+// search has loaded them already, so the caller's edge range costs no
+// further dependent load.
+__device__ __forceinline__ int4 balanced_range_off(const int* __restrict__ off, int N, int G, int b, int alpha) {
   const int lane = threadIdx.x & 31;
   // round 1: the probes of both bounds coincide; off[0] and off[N] load with them
   const int p1 = split_probe(0, N, lane);
@@ -63,18 +66,19 @@ __device__ __forceinline__ int2 balanced_range(const int* __restrict__ off, int 
   const int o0 = __ldg(off), oN = __ldg(off + N);
   const long long total = (long long)max(oN - o0, 0) + (long long)alpha * N;
   const long long tgt[2] = {total * b / G, total * (b + 1) / G};
-  int lo[2], hi[2];
+  int lo[2], hi[2], ohi[2];
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     const long long w = (long long)(o_p1 - o0) + (long long)alpha * p1;
     const unsigned ge = __ballot_sync(0xffffffffu, p1 == N || w >= tgt[k]);
     const int f = __ffs(ge) - 1;
     hi[k] = __shfl_sync(0xffffffffu, p1, f);
+    ohi[k] = __shfl_sync(0xffffffffu, o_p1, f);
     const int prev = __shfl_sync(0xffffffffu, p1, f > 0 ? f - 1 : 0);
     lo[k] = f == 0 ? 0 : prev + 1;
   }
-  if (b == 0) lo[0] = hi[0] = 0;
-  if (b == G - 1) lo[1] = hi[1] = N;
+  if (b == 0) { lo[0] = hi[0] = 0; ohi[0] = o0; }
+  if (b == G - 1) { lo[1] = hi[1] = N; ohi[1] = oN; }
   while (lo[0] < hi[0] || lo[1] < hi[1]) {
     int p[2], o[2];
 #pragma unroll
@@ -89,12 +93,15 @@ __device__ __forceinline__ int2 balanced_range(const int* __restrict__ off, int 
       const unsigned ge = __ballot_sync(0xffffffffu, p[k] == hi[k] || w >= tgt[k]);
       const int f = __ffs(ge) - 1;
       const int nh = __shfl_sync(0xffffffffu, p[k], f);
+      const int of = __shfl_sync(0xffffffffu, o[k], f);
       const int prev = __shfl_sync(0xffffffffu, p[k], f > 0 ? f - 1 : 0);
       lo[k] = f == 0 ? lo[k] : prev + 1;
+      if (nh != hi[k]) ohi[k] = of;  // a probe below hi was loaded; hi itself keeps its value
       hi[k] = nh;
     }
   }
-  return make_int2(hi[0], max(hi[1], hi[0]));
+  const bool up = hi[1] >= hi[0];
+  return make_int4(hi[0], up ? hi[1] : hi[0], ohi[0], up ? ohi[1] : ohi[0]);
 }
 
 // ---------------------------------------------------------------- mbarrier

@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(BwdSwCfg<C>::NTHREADS, BwdSwCfg<C>::MIN_BLOCKS
   const uint32_t empty0 = full0 + 8 * S;
   const int tid = threadIdx.x;
 
-  const int2 rr = balanced_range(a.off, a.N, gridDim.x, blockIdx.x, kReceiverCost);
+  const int4 rr = balanced_range_off(a.off, a.N, gridDim.x, blockIdx.x, kReceiverCost);
   const int r_begin = rr.x, r_end = rr.y;
   if (tid < S) {
     mbar_init(full0 + 8 * tid, 1);
@@ -166,8 +166,8 @@ __global__ void __launch_bounds__(BwdSwCfg<C>::NTHREADS, BwdSwCfg<C>::MIN_BLOCKS
     fence_mbar_init();
   }
   __syncthreads();
-  const int e_begin = min(max(__ldg(a.off + r_begin), 0), a.E);
-  const int e_end = max(e_begin, min(max(__ldg(a.off + r_end), 0), a.E));
+  const int e_begin = min(max(rr.z, 0), a.E);
+  const int e_end = max(e_begin, min(max(rr.w, 0), a.E));
   const int total = e_end - e_begin;
 
   if (tid < K::CONS0) {

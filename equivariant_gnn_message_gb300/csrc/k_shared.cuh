@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
   // Contiguous receiver range of this CTA, balanced on edges + 3 per
   // receiver (the contraction and store of a receiver cost about three
   // edges' accumulation).
-  const int2 rr = balanced_range(a.off, a.N, gridDim.x, blockIdx.x, kReceiverCost);
+  const int4 rr = balanced_range_off(a.off, a.N, gridDim.x, blockIdx.x, kReceiverCost);
   const int r_begin = rr.x, r_end = rr.y;
 
   if (tid < SP) {
@@ -294,8 +294,8 @@ __global__ void __launch_bounds__(SharedCfg<C, KQ, XT, FROM_VEC>::NTHREADS,
 
   // Edge range, clamped into [0, E]: a malformed CSR cannot send a load
   // out of bounds, and producer and consumers agree on the count.
-  const int e_begin = min(max(__ldg(a.off + r_begin), 0), a.E);
-  const int e_end = max(e_begin, min(max(__ldg(a.off + r_end), 0), a.E));
+  const int e_begin = min(max(rr.z, 0), a.E);
+  const int e_end = max(e_begin, min(max(rr.w, 0), a.E));
   const int total = e_end - e_begin;
 
   if (K::WS ? tid < K::CONS0 : tid >= K::NCONS) {

@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(So2Cfg<C, XT, RADIAL>::NTHREADS, So2Cfg<C, XT,
   const int tid = threadIdx.x;
   // Contiguous receiver range, balanced on edges (a receiver's group sum and
   // store cost about one edge here).
-  const int2 rr = balanced_range(a.off, a.N, gridDim.x, blockIdx.x, 1);
+  const int4 rr = balanced_range_off(a.off, a.N, gridDim.x, blockIdx.x, 1);
   const int r_begin = rr.x, r_end = rr.y;
   if (tid < S) {
     mbar_init(full0 + 8 * tid, 1);
@@ -287,8 +287,8 @@ __global__ void __launch_bounds__(So2Cfg<C, XT, RADIAL>::NTHREADS, So2Cfg<C, XT,
     for (int i = tid; i < 34 * C; i += K::NTHREADS) ws[i] = __ldg(a.w + i);
   }
   __syncthreads();
-  const int e_begin = min(max(__ldg(a.off + r_begin), 0), a.E);
-  const int e_end = max(e_begin, min(max(__ldg(a.off + r_end), 0), a.E));
+  const int e_begin = min(max(rr.z, 0), a.E);
+  const int e_end = max(e_begin, min(max(rr.w, 0), a.E));
   const int total = e_end - e_begin;
 
   if (tid >= K::NCONS) {

@@ -44,10 +44,10 @@ FLUSH_BYTES = 256 << 20
 # tag, which makes its entry missing (traffic null) until re-captured.
 KERNEL_VERSION = {"shared": "k_shared-pairs-v5", "radial": "k_so2-v4"}
 NCU_TRAFFIC = {
-    ("pages_1k_c32", "k_shared-pairs-v4"): 2357248 + 0,
-    ("scale_100k_c64", "k_shared-pairs-v4"): 6209806592 + 406970112,
-    ("dense_10k_c128_bf16", "k_shared-pairs-v4"): 48810496 + 11308544,
-    ("radial_1k_c32", "k_so2-v3"): 2888960 + 0,
+    ("pages_1k_c32", "k_shared-pairs-v5"): 2357504 + 0,
+    ("scale_100k_c64", "k_shared-pairs-v5"): 6207318016 + 407371008,
+    ("dense_10k_c128_bf16", "k_shared-pairs-v5"): 48796160 + 11876864,
+    ("radial_1k_c32", "k_so2-v4"): 2888704 + 0,
 }
 
 

@@ -8,17 +8,20 @@
 // and channel), then contracted once per receiver with the 611 CG terms and
 // the 34 path weights.  The result is the same sum in another order.
 //
-// Organisation of one CTA (persistent; owns a contiguous receiver range):
-//   * producer warp: for its edges, in CSR order, computes the 16 SH in
-//     registers (or reads them, for the unfused tp_scatter entry point),
-//     stores them in the slot's Y area and issues ONE TMA tensor load of the
-//     sender's feature row x[src] (C*16 elements) into the slot, with
-//     128-byte swizzle; ring of S slots with full/empty mbarriers.
+// Organisation of one CTA (persistent; owns a contiguous receiver range,
+// balanced on edges plus a per-receiver cost):
+//   * producer warps: for their edges, in CSR order, compute the 16 SH in
+//     registers (or read them, for the unfused tp_scatter entry point),
+//     store them in an SH ring and issue ONE TMA tensor load of the sender's
+//     feature row x[src] (C*16 elements) per edge into a ring slot, with
+//     128-byte swizzle.  The ring's slots come in pairs, each pair with one
+//     full and one empty mbarrier.
 //   * consumer warps: thread (c, q) holds A[c, q*KQ .. q*KQ+KQ-1, 0..15] in
-//     registers.  Per edge: wait full, 4 broadcast LDS.128 of Y, one
-//     conflict-free swizzled LDS of x, KQ*16 FFMAs, release the slot.  At the
-//     end of a receiver: contraction with compile-time CG constants, partial
-//     sums over the NQ quads through shared memory, one store per output.
+//     registers.  Per edge: 4 broadcast LDS.128 of Y, conflict-free swizzled
+//     LDS of x, KQ*8 paired FFMAs; per pair of edges: one wait, one release.
+//     At the end of a receiver: contraction with compile-time CG constants,
+//     partial sums over the NQ quads through shared memory, one store per
+//     output.
 //   * the receiver sum is in CSR order, deterministic, with no atomics.
 #pragma once
 

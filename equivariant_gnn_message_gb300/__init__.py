@@ -28,7 +28,7 @@ __all__ = [
     "EqmpError", "load_library", "library_path", "eqmp_num_paths", "eqmp_path_table",
     "eqmp_status_string", "eqmp_sh", "eqmp_tp_scatter", "eqmp_fused", "eqmp_fused_so2", "eqmp_validate_graph",
     "eqmp_device_error", "eqmp_fused_backward", "eqmp_fused_backward_noalloc", "eqmp_radius_graph", "eqmp_fused_lmax",
-    "eqmp_num_paths_lmax", "eqmp_watchdog_selftest", "sender_view", "EQMP_OK", "EQMP_ERR_INVALID_ARG", "EQMP_ERR_UNSUPPORTED",
+    "eqmp_num_paths_lmax", "eqmp_watchdog_selftest", "eqmp_fp32_peak_probe", "sender_view", "EQMP_OK", "EQMP_ERR_INVALID_ARG", "EQMP_ERR_UNSUPPORTED",
     "EQMP_ERR_CUDA", "EQMP_ERR_DEVICE_TIMEOUT", "EQMP_ERR_GRAPH",
 ]
 
@@ -91,6 +91,8 @@ def load_library():
     lib.eqmp_fused_backward.restype = i32
     lib.eqmp_watchdog_selftest.argtypes = [i32, vp]
     lib.eqmp_watchdog_selftest.restype = i32
+    lib.eqmp_fp32_peak_probe.argtypes = [i32, i32, vp, ctypes.POINTER(ctypes.c_double), vp]
+    lib.eqmp_fp32_peak_probe.restype = i32
     lib.eqmp_num_paths_lmax.argtypes = [i32]
     lib.eqmp_num_paths_lmax.restype = i32
     lib.eqmp_fused_lmax.argtypes = [i32, vp, vp, i64, vp, vp, i64, i64, i32, Weights, vp, vp]
@@ -253,6 +255,14 @@ def eqmp_device_error():
 def eqmp_watchdog_selftest(wait_ms=20, stream=None):
     """Launch the watchdog self-test (a wait that must give up); read the code with eqmp_device_error()."""
     _check(load_library().eqmp_watchdog_selftest(int(wait_ms), _stream(stream)), "eqmp_watchdog_selftest")
+
+
+def eqmp_fp32_peak_probe(iters, out, blocks_per_sm=4, stream=None):
+    """Launch the FP32 throughput probe (out: one-float CUDA tensor); returns its flop count."""
+    flops = ctypes.c_double(0.0)
+    _check(load_library().eqmp_fp32_peak_probe(int(iters), int(blocks_per_sm), _ptr(out), ctypes.byref(flops),
+                                                _stream(stream)), "eqmp_fp32_peak_probe")
+    return flops.value
 
 
 def eqmp_num_paths_lmax(l_max):

@@ -83,6 +83,24 @@ __global__ void k_wait_selftest(unsigned long long limit_ns, int* watchdog) {
   }
 }
 
+// Eight independent paired-FMA chains per thread: enough independent work
+// to keep the FMA pipe busy from any resident warp.
+__global__ void __launch_bounds__(256) k_fp32_peak(int iters, float* out) {
+  const float t = (float)threadIdx.x * 1e-7f;
+  float2 v[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) v[k] = make_float2(t + (float)k * 1e-3f, t - (float)k * 1e-3f);
+  const float2 m = make_float2(0.999999f, 1.000001f), c = make_float2(1e-7f, -1e-7f);
+  for (int i = 0; i < iters; ++i) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = __ffma2_rn(v[k], m, c);
+  }
+  float s = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) s += v[k].x + v[k].y;
+  if (s == 1234567.0f) *out = s;
+}
+
 // ------------------------------------------------------------ device state
 eqmp_status device_info(DeviceInfo* out) {
   static std::once_flag once[64];
@@ -278,6 +296,18 @@ eqmp_status eqmp_watchdog_selftest(int32_t wait_ms, eqmp_stream_t stream) {
   if (s != EQMP_OK) return s;
   k_wait_selftest<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
       (unsigned long long)wait_ms * 1000000ull, dev.watchdog);
+  return cuda_status(cudaGetLastError());
+}
+
+eqmp_status eqmp_fp32_peak_probe(int32_t iters, int32_t blocks_per_sm, float* out, double* flops,
+                                 eqmp_stream_t stream) {
+  if (!out || !flops || iters < 1 || blocks_per_sm < 1 || blocks_per_sm > 8) return EQMP_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  eqmp_status s = device_info(&dev);
+  if (s != EQMP_OK) return s;
+  const int grid = dev.sms * blocks_per_sm;
+  *flops = (double)grid * 256.0 * 32.0 * (double)iters;
+  k_fp32_peak<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(iters, out);
   return cuda_status(cudaGetLastError());
 }
 

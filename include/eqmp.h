@@ -311,6 +311,19 @@ eqmp_status eqmp_device_error(int32_t* code);
  */
 eqmp_status eqmp_watchdog_selftest(int32_t wait_ms, eqmp_stream_t stream);
 
+/* FP32 throughput probe: the denominator of the layer kernels' roofline.
+ * Launches `blocks_per_sm` x (SM count) CTAs of 256 threads; each thread runs
+ * `iters` rounds of 8 independent paired FP32 FMAs (fma.rn.f32x2), i.e.
+ * 32 * iters flops per thread, nothing else but a final conditional store.
+ * The caller times the launch (CUDA events on `stream`) and divides.
+ * `out`: device pointer to one float; written only if the sums reach a value
+ * they never reach (it keeps the arithmetic from being removed).
+ * Writes the launch's flop count to *flops (host pointer).
+ * Errors: EQMP_ERR_INVALID_ARG for a null pointer, iters < 1 or
+ * blocks_per_sm outside [1, 8]; EQMP_ERR_CUDA for a failed launch. */
+eqmp_status eqmp_fp32_peak_probe(int32_t iters, int32_t blocks_per_sm, float* out, double* flops,
+                                 eqmp_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

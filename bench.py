@@ -14,8 +14,9 @@ Prints ONE JSON line (rank 0):
   e2e          the same metric through the public API with pinned host
                buffers: H2D of the step's inputs, the layer, D2H of out;
   roofline     FP32-ALU bound of the layer kernel (FMA count of the
-               lowest-FMA exact schedule at the SM count x 128 lanes x 2
-               flops x max SM clock);
+               lowest-FMA exact schedule against the higher of the derived
+               peak, SM count x 128 lanes x 2 flops x max SM clock, and the
+               measured one from eqmp_fp32_peak_probe; both are reported);
   cpu_baseline the CPU oracle (numpy, fp64) on a bounded sample of the same
                workload on this host's cores.
 --impl reference times the CPU oracle alone (the reference arm).

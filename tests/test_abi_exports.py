@@ -49,6 +49,19 @@ def test_host_only_functions(lib):
     assert lib.eqmp_path_table(None) == eq.EQMP_ERR_INVALID_ARG
 
 
+def test_fp32_probe_rejects_bad_arguments_before_any_launch(lib):
+    """The probe's argument checks come before any CUDA call (no GPU needed)."""
+    import equivariant_gnn_message_gb300 as eq
+
+    flops = ctypes.c_double(-1.0)
+    out = ctypes.c_void_p(16)  # never dereferenced: every call below fails its checks first
+    for iters, bps, o, f in ((0, 4, out, ctypes.byref(flops)), (64, 0, out, ctypes.byref(flops)),
+                             (64, 9, out, ctypes.byref(flops)), (64, 4, None, ctypes.byref(flops)),
+                             (64, 4, out, None)):
+        assert lib.eqmp_fp32_peak_probe(iters, bps, o, f, None) == eq.EQMP_ERR_INVALID_ARG
+    assert flops.value == -1.0
+
+
 def test_product_path_has_no_oracle_dependency():
     """The package and its sources never import or mention the oracle."""
     pkg = os.path.join(ROOT, "equivariant_gnn_message_gb300")

@@ -3,22 +3,30 @@
 
 One step = one eqmp_fused call (the whole hot path: CSR walk, SH in
 registers, sender-row gather, CG tensor product, receiver sum, store) over
-one seeded synthetic graph.  Default workload: 1000 atoms, 32 channels,
-~16.5 neighbours per atom, shared per-path weights, fp32 - the workload
-the Batmobile blog quotes (1000 atoms, 32 channels, about 20 neighbours).
+one seeded synthetic graph.  Headline workload: 1000 atoms, 32 channels,
+~16.5 neighbours per atom, shared per-path weights, fp32 - the workload the
+Batmobile blog quotes (1000 atoms, 32 channels, about 20 neighbours).
 
 Prints ONE JSON line (rank 0):
   value        edges/s over all ranks, inputs resident in HBM, L2 flushed
                (256 MB write) before every timed step, device time of the
-               layer kernel from CUDA events on the launching stream;
+               layer kernel from CUDA events on the launching stream (the
+               host queues each group of steps behind a short GPU spin, so
+               host-side enqueue jitter never shows up as device time);
   e2e          the same metric through the public API with pinned host
                buffers: H2D of the step's inputs, the layer, D2H of out;
-  roofline     FP32-ALU bound of the layer kernel (FMA count of the
-               lowest-FMA exact schedule against the higher of the derived
-               peak, SM count x 128 lanes x 2 flops x max SM clock, and the
-               measured one from eqmp_fp32_peak_probe; both are reported);
+  roofline     t_roof = max(FMA count / FP32 peak, compulsory bytes / HBM
+               peak); frac = t_roof / measured time, bound = the larger
+               term.  FMA count of the lowest-FMA exact schedule (shared
+               weights: accumulate x (x) Y, contract once per receiver;
+               radial weights: the aligned-frame schedule), FP32 peak = the
+               higher of the derived one (SM count x 128 lanes x 2 flops x
+               max SM clock) and the measured one (eqmp_fp32_peak_probe);
+  workloads    the same measurement (time, roofline, clocks) for the
+               100k-atom, the dense bf16 and the radial-weight workloads;
   cpu_baseline the CPU oracle (numpy, fp64) on a bounded sample of the same
-               workload on this host's cores.
+               workload on this host's cores, plus one-thread runs of the
+               tiny, pages and radial workloads.
 --impl reference times the CPU oracle alone (the reference arm).
 Multi-GPU: independent replicas (weak scaling), no collective on the data
 path; barrier + max over ranks for timing.
@@ -39,6 +47,12 @@ sys.path.insert(0, ROOT)
 METRIC = "edges/s fused SH+CG-TP+scatter (1k atoms, C=32, ~20 nbrs); % of roofline"
 METRIC_GRAPH = "edges/s radius graph (CSR by receiver, edge vectors)"
 FLUSH_BYTES = 256 << 20
+HEADLINE = "pages_1k_c32"
+# Measured beside the headline in the default run (the other full-size configurations).
+EXTRA_WORKLOADS = ("scale_100k_c64", "dense_10k_c128_bf16", "radial_1k_c32")
+# One-thread oracle runs (the small configurations).
+SINGLE_THREAD_WORKLOADS = ("tiny_64", "pages_1k_c32", "radial_1k_c32")
+GROUP = 32  # timed steps queued behind one GPU spin
 # DRAM bytes per launch of the layer kernel from the ncu capture recorded in
 # profiles/ (None until captured for the current kernel version).
 # Keyed by (workload, kernel version); a changed kernel gets a new version
@@ -51,11 +65,15 @@ NCU_TRAFFIC = {
     ("radial_1k_c32", "k_so2-v4"): 2888704 + 0,
 }
 
+# aligned-frame terms per degree (one per output order and path with m2 = 0)
+ALIGNED_TERMS = {3: 111, 4: 272, 5: 565, 6: 1036}
+
 
 def fma_count(wl):
-    """FMAs of the lowest-FMA exact schedule of the layer (per launch).
+    """FMAs of the dense schedules of the l <= 3 layer (per launch).
 
     shared weights: 256*C per edge (A += x (x) Y) + (611 + 156)*C per receiver
+    (the lowest-FMA exact schedule for shared weights);
     radial weights: (611 + 156 + 272)*C + 611 per edge (W = R.M per path and
     channel, CG terms, weighted sum; the Y-side products shared by channels).
     """
@@ -70,27 +88,63 @@ def sum_rot(l_max):
     return sum((2 * l + 1) ** 2 for l in range(1, l_max + 1))
 
 
-def aligned_fma_count(wl, l_max, n_terms):
+def aligned_fma_count(wl, l_max):
     """FMAs of the aligned-frame schedule at degree l_max (per launch):
     rotate in and out (2 sum (2l+1)^2), one FMA per aligned term, and for
-    radial weights 8 per path; per edge and channel."""
+    radial weights 8 per path; per edge and channel.  At l_max = 3 with
+    radial weights this is 549 per edge and channel, the lowest-FMA exact
+    schedule for per-edge weights (the dense one needs 1039)."""
     from equivariant_gnn_message_gb300.inputs import n_paths
 
-    per = 2 * sum_rot(l_max) + n_terms + (8 * n_paths(l_max) if wl.w is None else 0)
+    per = 2 * sum_rot(l_max) + ALIGNED_TERMS[l_max] + (8 * n_paths(l_max) if wl.w is None else 0)
     return per * wl.channels * wl.n_edges
 
 
-# aligned-frame terms per degree (one per output order and path with m2 = 0)
-ALIGNED_TERMS = {4: 272, 5: 565, 6: 1036}
-
-
 def compulsory_bytes(wl):
+    """x read once, vec, src, offsets, weights (or R and M), out written once."""
     s = 2 if wl.storage == "bf16" else 4
     C, E, N = wl.channels, wl.n_edges, wl.n_atoms
     nc = wl.x.shape[2]
     b = N * C * nc * s + 12 * E + 4 * E + 4 * (N + 1) + N * C * nc * s
     b += 4 * 34 * C if wl.w is not None else 32 * E + 4 * 8 * 34 * C
     return b
+
+
+def layer_flops(wl, which, l_max):
+    """(algorithmic flops per launch, basis name, extra) for the roofline."""
+    if which == "backward":
+        # three forward-sized contractions (dx, the weight gradient, dY) of
+        # the dense schedule plus the SH Jacobian (48 FMA per edge)
+        return 2.0 * (3 * fma_count(wl) + 48 * wl.n_edges), "backward: 3 x forward schedule + SH Jacobian", {}
+    if l_max != 3 or wl.w is None:
+        f = 2.0 * aligned_fma_count(wl, l_max)
+        extra = {}
+        if l_max == 3:
+            extra["flops_dense_basis"] = 2.0 * fma_count(wl)
+        return f, f"aligned frame (2*rot + {ALIGNED_TERMS[l_max]} terms" + \
+            (" + 8 per path" if wl.w is None else "") + " per edge and channel)", extra
+    return 2.0 * fma_count(wl), "accumulate-then-contract (256*C per edge + 767*C per receiver)", {}
+
+
+def roofline(flops, nbytes, ms, fp32_peak, hbm_peak, kernel, traffic, basis, extra=None):
+    """t_roof = max(flops / FP32 peak, bytes / HBM peak); frac = t_roof / t."""
+    t = ms * 1e-3
+    t_alu = flops / (fp32_peak * 1e12)
+    t_hbm = nbytes / (hbm_peak * 1e9)
+    if t_alu >= t_hbm:
+        r = {"bound": "alu", "achieved": flops / t / 1e12, "peak": fp32_peak, "unit": "TFLOP/s"}
+    else:
+        r = {"bound": "hbm", "achieved": nbytes / t / 1e9, "peak": hbm_peak, "unit": "GB/s"}
+    r.update({"frac": max(t_alu, t_hbm) / t, "traffic": traffic, "traffic_unit": "bytes/launch",
+              "kernel": kernel, "flops": flops, "compulsory_bytes": nbytes, "fma_basis": basis,
+              "t_alu_us": t_alu * 1e6, "t_hbm_us": t_hbm * 1e6,
+              "hbm_gbs_compulsory": nbytes / t / 1e9})
+    for k, v in (extra or {}).items():
+        if k == "flops_dense_basis":
+            r["frac_dense_basis"] = v / (fp32_peak * 1e12) / t
+        else:
+            r[k] = v
+    return r
 
 
 class ClockSampler:
@@ -132,10 +186,11 @@ class ClockSampler:
         if self._t is not None:
             self._t.join(timeout=2)
 
-    def summary(self, t0, t1):
-        win = [s for (t, s) in self.samples if t0 - 0.3 <= t <= t1 + 0.3] or [s for _, s in self.samples]
+    def summary(self, t0, t1, pad=0.3):
+        win = [s for (t, s) in self.samples if t0 - pad <= t <= t1 + pad] or [s for _, s in self.samples]
         if not win:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+
         def num(v):
             try:
                 return float(v)
@@ -143,24 +198,28 @@ class ClockSampler:
                 return None
         sm = [num(s[1]) for s in win if num(s[1]) is not None]
         mx = [num(s[2]) for s in win if num(s[2]) is not None]
+        pw = [num(s[3]) for s in win if len(s) > 3 and num(s[3]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for s in win for i in range(4) if len(s) > 5 + i and s[5 + i] == "Active"})
         return {"sm_mhz": float(np.median(sm)) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(win)}
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(win),
+                "power_w_max": max(pw) if pw else None}
 
 
+# ---------------------------------------------------------------- CPU oracle
 def _oracle_chunk(args):
     """Child-process worker: oracle on a receiver subset, `reps` times
-    (single-threaded BLAS)."""
+    (single-threaded BLAS); returns the wall time of the oracle calls."""
     name, receivers, l_max, reps = args
     from equivariant_gnn_message_gb300.inputs import make_workload
     from oracle import layer
 
     wl = make_workload(name, l_max=l_max)
     kw = dict(w=wl.w) if wl.w is not None else dict(R=wl.R, M=wl.M)
+    receivers = np.arange(wl.n_atoms) if receivers is None else np.asarray(receivers)
     t = time.perf_counter()
     for _ in range(reps):
-        layer.message_pass(wl.vec, wl.x, wl.off, wl.src, receivers=np.asarray(receivers), **kw)
+        layer.message_pass(wl.vec, wl.x, wl.off, wl.src, receivers=receivers, **kw)
     return time.perf_counter() - t
 
 
@@ -218,6 +277,23 @@ def cpu_oracle_rate(name, wl, seconds_target=12.0, pool=None, cores=1):
             f"receivers 0..{n_recv - 1} ({edges} edges of {wl.n_edges}) x {reps}, {wall:.1f} s wall")
 
 
+def single_thread_rates(pool, names, seconds=2.5):
+    """One worker of the pool (one thread) runs the oracle over every
+    receiver of each small workload, repeated to about `seconds`."""
+    from equivariant_gnn_message_gb300.inputs import make_workload
+
+    res = []
+    for name in names:
+        E = make_workload(name).n_edges
+        t1 = pool.apply(_oracle_chunk, ((name, None, 3, 1),))
+        reps = max(1, int(round(seconds / max(t1, 1e-3))))
+        wall = pool.apply(_oracle_chunk, ((name, None, 3, reps),))
+        res.append({"workload": name, "value": E * reps / wall, "unit": "edges/s", "cores": 1,
+                    "ms_per_layer": 1e3 * wall / reps,
+                    "sample": f"all {E} edges x {reps}, {wall:.2f} s wall"})
+    return res
+
+
 def run_reference(args, wl):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -242,9 +318,7 @@ def run_reference(args, wl):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * wl.n_edges / value, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "n_atoms": wl.n_atoms, "n_edges": wl.n_edges,
-                   "channels": wl.channels, "storage": wl.storage,
-                   "weights": "shared" if wl.w is not None else "radial"},
+        "config": workload_config(args.workload, wl, args.entry, 1),
         "cpu_baseline": {"value": value, "unit": "edges/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "edges/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -253,14 +327,110 @@ def run_reference(args, wl):
     print(json.dumps(line), flush=True)
 
 
+def workload_config(name, wl, entry, world):
+    return {"workload": name, "n_atoms": wl.n_atoms, "n_edges": wl.n_edges,
+            "channels": wl.channels, "storage": wl.storage,
+            "weights": "shared" if wl.w is not None else "radial", "entry": entry,
+            "l2": "flushed (256 MB write) before every timed step",
+            "parallelism": f"replicas x{world}"}
+
+
+# ---------------------------------------------------------------- GPU timing
+class Timer:
+    """CUDA-event timing of `step` on `stream`, L2 flushed before each step.
+
+    The host queues GROUP steps (flush, start event, step, end event) behind
+    one GPU spin long enough to cover their enqueue time, so every step runs
+    back to back on the device and the events hold device time only.
+    """
+
+    def __init__(self, torch, stream, flush):
+        self.torch = torch
+        self.stream = stream
+        self.flush = flush
+        self.host_s = 60e-6  # host enqueue time per step; refined by warm()
+
+    def warm(self, step, n):
+        torch = self.torch
+        torch.cuda.synchronize()
+        t = time.perf_counter()
+        for _ in range(n):
+            self.flush.zero_()
+            step()
+        self.host_s = max(self.host_s, (time.perf_counter() - t) / max(1, n))
+        torch.cuda.synchronize()
+
+    def _spin(self, n_steps):
+        sleep = getattr(self.torch.cuda, "_sleep", None)
+        if sleep is not None:
+            seconds = min(0.05, 3.0 * n_steps * self.host_s + 2e-4)
+            sleep(int(seconds * 2.2e9))  # cycles at up to 2.2 GHz
+
+    def run(self, step, steps):
+        torch = self.torch
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        i = 0
+        while i < steps:
+            n = min(GROUP, steps - i)
+            self._spin(n)
+            for _ in range(n):
+                self.flush.zero_()  # evict L2 between timed steps
+                starts[i].record(self.stream)
+                step()
+                ends[i].record(self.stream)
+                i += 1
+        torch.cuda.synchronize()
+        return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def device_inputs(torch, wl, dev):
+    t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    d = dict(vec=t(wl.vec), off=t(wl.off), src=t(wl.src), w=t(wl.w), R=t(wl.R), M=t(wl.M))
+    if wl.storage == "bf16":
+        d["x"] = torch.from_numpy(wl.x_bf16_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    else:
+        d["x"] = t(wl.x)
+    return d
+
+
+def layer_step(eq, entry, l_max, d, out, Yb=None):
+    wkw = dict(w=d["w"]) if d["w"] is not None else dict(R=d["R"], M=d["M"])
+    if l_max != 3:
+        return lambda: eq.eqmp_fused_lmax(l_max, d["vec"], d["x"], d["off"], d["src"], out=out, **wkw)
+    if entry == "fused":
+        return lambda: eq.eqmp_fused(d["vec"], d["x"], d["off"], d["src"], out=out, **wkw)
+    if entry == "so2":
+        return lambda: eq.eqmp_fused_so2(d["vec"], d["x"], d["off"], d["src"], out=out, **wkw)
+
+    def two():
+        eq.eqmp_sh(d["vec"], Yb)
+        eq.eqmp_tp_scatter(Yb, d["x"], d["off"], d["src"], out=out, **wkw)
+    return two
+
+
+def kernel_version(wl, which, l_max, entry):
+    if which == "backward":
+        return "k_bwd-v1"
+    if l_max != 3:
+        return f"k_hl<{l_max}>-v1"
+    if entry == "tp_scatter":
+        return "k_sh+" + ("k_shared-tp" if wl.w is not None else "k_radial")
+    if entry == "so2":
+        return KERNEL_VERSION["radial"]
+    return KERNEL_VERSION["shared" if wl.w is not None else "radial"]
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="pages_1k_c32")
+    ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="time the chosen workload only (no scale / dense / radial entries)")
     ap.add_argument("--entry", default="fused", choices=["fused", "tp_scatter", "so2"])
     ap.add_argument("--lmax", type=int, default=3,
                     help="4..6: the higher-degree layer (eqmp_fused_lmax) on the workload's graph")
@@ -309,29 +479,30 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
-    t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-    vec, off, src, w, R, M = t(wl.vec), t(wl.off), t(wl.src), t(wl.w), t(wl.R), t(wl.M)
-    if wl.storage == "bf16":
-        x = torch.from_numpy(wl.x_bf16_bits.view(np.int16)).to(dev).view(torch.bfloat16)
-    else:
-        x = t(wl.x)
-    out = torch.empty((wl.n_atoms, wl.channels, 16), dtype=x.dtype, device=dev)
-    Yb = torch.empty((wl.n_edges, 16), dtype=torch.float32, device=dev)
-    wkw = dict(w=w) if w is not None else dict(R=R, M=M)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
+    timer = Timer(torch, stream, flush)
+    sampler = ClockSampler(local)
+    sampler.start()
 
-    bwd_args = None
+    d = device_inputs(torch, wl, dev)
+    t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    out = torch.empty((wl.n_atoms, wl.channels, (args.lmax + 1) ** 2), dtype=d["x"].dtype, device=dev)
+    Yb = torch.empty((wl.n_edges, 16), dtype=torch.float32, device=dev) if args.entry == "tp_scatter" else None
+    wkw = dict(w=d["w"]) if d["w"] is not None else dict(R=d["R"], M=d["M"])
+    n_edges = wl.n_edges
+
     if args.which == "backward":
         if wl.storage != "f32":
             raise SystemExit("the backward pass takes fp32 features")
         so, se = eq.sender_view(wl.src, wl.n_atoms)
-        gout = torch.randn((wl.n_atoms, wl.channels, 16), device=dev, generator=torch.Generator(device=dev).manual_seed(0))
-        need = ("x", "vec", "w") if w is not None else ("x", "vec", "R", "M")
-        bwd_args = ((vec, x, off, src, t(wl.dst), t(so), t(se), gout), dict(need=need, **wkw))
-
-    graph_args = None
-    if args.which == "graph":
+        gout = torch.randn((wl.n_atoms, wl.channels, 16), device=dev,
+                           generator=torch.Generator(device=dev).manual_seed(0))
+        need = ("x", "vec", "w") if d["w"] is not None else ("x", "vec", "R", "M")
+        bargs = (d["vec"], d["x"], d["off"], d["src"], t(wl.dst), t(so), t(se), gout)
+        step = lambda: eq.eqmp_fused_backward(*bargs, need=need, **wkw)
+        launches_per_step = 3
+    elif args.which == "graph":
         import ctypes
 
         lib = eq.load_library()
@@ -340,118 +511,84 @@ def main():
         g_ws = torch.empty(lib.eqmp_radius_graph_workspace_size(N), dtype=torch.uint8, device=dev)
         g_E = torch.empty(1, dtype=torch.int64, device=dev)
         g_out, E_graph = eq.eqmp_radius_graph(g_pos, wl.cutoff)
-        g_cap = E_graph
         g_off, g_src, g_vec = g_out["off"], g_out["src"], g_out["vec"]
         graph_args = (g_pos.data_ptr(), N, ctypes.c_float(wl.cutoff), g_off.data_ptr(), g_src.data_ptr(),
-                      g_vec.data_ptr(), None, None, g_cap, g_E.data_ptr(), g_ws.data_ptr(), g_ws.numel(),
+                      g_vec.data_ptr(), None, None, E_graph, g_E.data_ptr(), g_ws.data_ptr(), g_ws.numel(),
                       stream.cuda_stream)
+        step = lambda: lib.eqmp_radius_graph(*graph_args)
+        coop = N <= 16384  # the library's single cooperative launch covers up to 16,384 atoms
+        launches_per_step = 1 if coop else 12
+        n_edges = E_graph
+    else:
+        step = layer_step(eq, args.entry, args.lmax, d, out, Yb)
+        launches_per_step = 2 if args.entry == "tp_scatter" else 1
 
-    if args.lmax != 3:
-        out = torch.empty((wl.n_atoms, wl.channels, (args.lmax + 1) ** 2), dtype=torch.float32, device=dev)
-
-    def step():
-        if args.lmax != 3:
-            eq.eqmp_fused_lmax(args.lmax, vec, x, off, src, out=out, **wkw)
-        elif graph_args is not None:
-            lib.eqmp_radius_graph(*graph_args)
-        elif bwd_args is not None:
-            eq.eqmp_fused_backward(*bwd_args[0], **bwd_args[1])
-        elif args.entry == "fused":
-            eq.eqmp_fused(vec, x, off, src, out=out, **wkw)
-        elif args.entry == "so2":
-            eq.eqmp_fused_so2(vec, x, off, src, out=out, **wkw)
-        else:
-            eq.eqmp_sh(vec, Yb)
-            eq.eqmp_tp_scatter(Yb, x, off, src, out=out, **wkw)
-
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
+    timer.warm(step, args.warmup)
     barrier()
     if eq.eqmp_device_error() != 0:
         raise RuntimeError("device watchdog tripped during warm-up")
-
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier()
     t0 = time.time()
-    for i in range(args.steps):
-        flush.zero_()                 # evict L2 between timed steps
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
+    kernel_ms = timer.run(step, args.steps)
     barrier()
     t1 = time.time()
-    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = max_over_ranks(float(np.mean(kernel_ms)))
 
     # ---- e2e through the public API with pinned host buffers.  The step's
     # inputs sit in one pinned host block (each array 256-byte aligned) and
     # go over in one host->device copy; the result comes back in one copy.
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
-    parts = {"vec": wl.vec, "off": wl.off, "src": wl.src,
-             "x": wl.x_bf16_bits.view(np.int16) if wl.storage == "bf16" else wl.x}
-    for k in ("w", "R", "M"):
-        if getattr(wl, k) is not None:
-            parts[k] = getattr(wl, k)
-    layout, nbytes = {}, 0
-    for k, a in parts.items():
-        a = np.ascontiguousarray(a)
-        layout[k] = (nbytes, a.dtype, a.shape)
-        nbytes = (nbytes + a.nbytes + 255) // 256 * 256
-    h_pack = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
-    hp = h_pack.numpy()
-    for k, a in parts.items():
-        o, dt, shp = layout[k]
-        a = np.ascontiguousarray(a)
-        hp[o:o + a.nbytes] = a.view(np.uint8).reshape(-1)
-    d_pack = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-    tdt = {np.dtype(np.float32): torch.float32, np.dtype(np.int32): torch.int32, np.dtype(np.int16): torch.int16}
+    e2e_ms, h2d, d2h = None, 0, 0
+    if args.which == "forward":
+        parts = {"vec": wl.vec, "off": wl.off, "src": wl.src,
+                 "x": wl.x_bf16_bits.view(np.int16) if wl.storage == "bf16" else wl.x}
+        for k in ("w", "R", "M"):
+            if getattr(wl, k) is not None:
+                parts[k] = getattr(wl, k)
+        layout, nbytes = {}, 0
+        for k, a in parts.items():
+            a = np.ascontiguousarray(a)
+            layout[k] = (nbytes, a.dtype, a.shape)
+            nbytes = (nbytes + a.nbytes + 255) // 256 * 256
+        h_pack = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+        hp = h_pack.numpy()
+        for k, a in parts.items():
+            o, dt, shp = layout[k]
+            a = np.ascontiguousarray(a)
+            hp[o:o + a.nbytes] = a.view(np.uint8).reshape(-1)
+        d_pack = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        tdt = {np.dtype(np.float32): torch.float32, np.dtype(np.int32): torch.int32,
+               np.dtype(np.int16): torch.int16}
 
-    def dview(k):
-        o, dt, shp = layout[k]
-        n = int(np.prod(shp)) * dt.itemsize
-        return d_pack[o:o + n].view(tdt[dt]).view(shp)
+        def dview(k):
+            o, dt, shp = layout[k]
+            n = int(np.prod(shp)) * dt.itemsize
+            return d_pack[o:o + n].view(tdt[dt]).view(shp)
 
-    d_in = {k: dview(k) for k in parts}
-    h_in = {"packed": h_pack}
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(np.ascontiguousarray(a).nbytes for a in parts.values())
-    d2h = h_out.numel() * h_out.element_size()
-
-    def e2e_step():
-        d_pack.copy_(h_pack, non_blocking=True)
-        xd = d_in["x"].view(torch.bfloat16) if wl.storage == "bf16" else d_in["x"]
-        kw = dict(w=d_in["w"]) if "w" in d_in else dict(R=d_in["R"], M=d_in["M"])
-        if args.lmax != 3:
-            eq.eqmp_fused_lmax(args.lmax, d_in["vec"], xd, d_in["off"], d_in["src"], out=out, **kw)
-        elif args.entry == "so2":
-            eq.eqmp_fused_so2(d_in["vec"], xd, d_in["off"], d_in["src"], out=out, **kw)
-        elif args.entry == "tp_scatter":
-            eq.eqmp_sh(d_in["vec"], Yb)
-            eq.eqmp_tp_scatter(Yb, xd, d_in["off"], d_in["src"], out=out, **kw)
-        else:
-            eq.eqmp_fused(d_in["vec"], xd, d_in["off"], d_in["src"], out=out, **kw)
-        h_out.copy_(out, non_blocking=True)
-
-    if graph_args is not None:
-        h_in = {"pos": pin(wl.pos)}
-        d_in = {"pos": g_pos}
-        h_out = [torch.empty(a.shape, dtype=a.dtype).pin_memory() for a in (g_off, g_src, g_vec)]
-        h2d = h_in["pos"].numel() * 4
-        d2h = sum(a.numel() * a.element_size() for a in h_out)
+        d_in = {k: dview(k) for k in parts}
+        d_in["x"] = d_in["x"].view(torch.bfloat16) if wl.storage == "bf16" else d_in["x"]
+        for k in ("w", "R", "M"):
+            d_in.setdefault(k, None)
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = sum(np.ascontiguousarray(a).nbytes for a in parts.values())
+        d2h = h_out.numel() * h_out.element_size()
+        layer_e2e = layer_step(eq, args.entry, args.lmax, d_in, out, Yb)
 
         def e2e_step():
-            d_in["pos"].copy_(h_in["pos"], non_blocking=True)
-            lib.eqmp_radius_graph(*graph_args)
-            for h, d in zip(h_out, (g_off, g_src, g_vec)):
-                h.copy_(d, non_blocking=True)
+            d_pack.copy_(h_pack, non_blocking=True)
+            layer_e2e()
+            h_out.copy_(out, non_blocking=True)
+    elif args.which == "graph":
+        h_pos = torch.from_numpy(np.ascontiguousarray(wl.pos)).pin_memory()
+        h_outs = [torch.empty(a.shape, dtype=a.dtype).pin_memory() for a in (g_off, g_src, g_vec)]
+        h2d = h_pos.numel() * 4
+        d2h = sum(a.numel() * a.element_size() for a in h_outs)
 
-    e2e_ms = None
-    if bwd_args is None:  # the end-to-end figure is the forward layer's
+        def e2e_step():
+            g_pos.copy_(h_pos, non_blocking=True)
+            lib.eqmp_radius_graph(*graph_args)
+            for h, dd in zip(h_outs, (g_off, g_src, g_vec)):
+                h.copy_(dd, non_blocking=True)
+    if args.which != "backward":
         for _ in range(3):
             e2e_step()
         barrier()
@@ -464,21 +601,50 @@ def main():
             e_e[i].record(stream)
         barrier()
         e2e_ms = max_over_ranks(float(np.mean([s.elapsed_time(e) for s, e in zip(e_s, e_e)])))
-    sampler.stop()
-    # FP32 throughput probe (paired FMAs only), outside the timed region:
-    # the measured counterpart of the derived FP32 peak.
+
+    # ---- the other full-size workloads, same timing, one entry each
+    extra = []
+    run_extra = (args.workload == HEADLINE and args.which == "forward" and args.lmax == 3
+                 and args.entry == "fused" and not args.no_workloads)
+    extra_launches = 0
+    if run_extra:
+        del d
+        for name in EXTRA_WORKLOADS:
+            xw = make_workload(name)
+            xd = device_inputs(torch, xw, dev)
+            xo = torch.empty((xw.n_atoms, xw.channels, 16), dtype=xd["x"].dtype, device=dev)
+            xs = layer_step(eq, "fused", 3, xd, xo)
+            timer.warm(xs, args.warmup)
+            barrier()
+            ta = time.time()
+            xk = timer.run(xs, args.steps)
+            barrier()
+            tb = time.time()
+            xms = max_over_ranks(float(np.mean(xk)))
+            extra.append(dict(name=name, wl=xw, ms=xms, kernel_ms=xk, t=(ta, tb)))
+            extra_launches += args.steps
+            del xd, xo
+            torch.cuda.empty_cache()
+
+    # ---- FP32 throughput probe (paired FMAs only), outside every timed
+    # region but inside the clock sampler's window: the measured
+    # counterpart of the derived FP32 peak, with the SM clock it ran at.
     probe_buf = torch.zeros(1, device=dev)
     probe_ms = []
-    for i in range(7):
+    pt0 = time.time()
+    while time.time() - pt0 < 0.8 or len(probe_ms) < 8:
         ps, pe = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ps.record(stream)
         probe_flops = eq.eqmp_fp32_peak_probe(65536, probe_buf, stream=stream)
         pe.record(stream)
         torch.cuda.synchronize()
-        if i >= 2:
-            probe_ms.append(ps.elapsed_time(pe))
+        probe_ms.append(ps.elapsed_time(pe))
+    pt1 = time.time()
+    probe_ms = probe_ms[2:]
     fp32_measured = probe_flops / (float(np.median(probe_ms)) * 1e-3) / 1e12
     wd = eq.eqmp_device_error()
+    time.sleep(0.25)
+    sampler.stop()
 
     if rank != 0:
         if dist is not None:
@@ -487,42 +653,59 @@ def main():
 
     props = torch.cuda.get_device_properties(dev)
     clocks = sampler.summary(t0, t1)
+    probe_clocks = sampler.summary(pt0, pt1, pad=0.05)
     peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     peaks = json.load(open(peaks_path)) if os.path.exists(peaks_path) else {}
     max_mhz = clocks.get("sm_max_mhz") or peaks.get("sm_max_mhz") or 2070.0
     derived_tflops = props.multi_processor_count * 128 * 2 * max_mhz * 1e6 / 1e12
     # graded against the higher of the derived and the measured FP32 peak
-    peak_tflops = max(derived_tflops, fp32_measured)
+    fp32_peak = max(derived_tflops, fp32_measured)
+    hbm_peak = float(peaks.get("hbm_gbs", 6793.1))
     peak_basis = (f"{props.multi_processor_count} SMs x 128 FP32 lanes x 2 x {max_mhz:.0f} MHz (derived)"
                   if derived_tflops >= fp32_measured else "eqmp_fp32_peak_probe (measured, paired FMAs)")
-    # backward: three forward-sized contractions (dx, the weight gradient,
-    # dY) of the lowest-FMA schedule plus the SH Jacobian (48 FMA per edge)
-    flops = 2.0 * fma_count(wl) if bwd_args is None else 2.0 * (3 * fma_count(wl) + 48 * wl.n_edges)
-    if args.lmax != 3:
-        flops = 2.0 * aligned_fma_count(wl, args.lmax, ALIGNED_TERMS[args.lmax])
-    achieved = flops / (ms * 1e-3) / 1e12
-    version = KERNEL_VERSION["shared" if wl.w is not None else "radial"] if bwd_args is None else "k_bwd-v1"
-    if args.lmax != 3:
-        version = f"k_hl<{args.lmax}>-v1"
-    traffic = NCU_TRAFFIC.get((args.workload, version)) if args.entry == "fused" else None
-    n_edges = wl.n_edges if graph_args is None else E_graph
-    value = n_edges * world / (ms * 1e-3)
-    roofline = {"bound": "alu", "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
-                "frac": achieved / peak_tflops, "traffic": traffic, "traffic_unit": "bytes/launch",
-                "kernel": version,
-                "peak_basis": peak_basis, "fp32_derived": derived_tflops, "fp32_measured": fp32_measured,
-                "hbm_gbs_compulsory": compulsory_bytes(wl) / (ms * 1e-3) / 1e9}
-    if graph_args is not None:
+    fp32_info = {"peak_basis": peak_basis, "fp32_derived": derived_tflops, "fp32_measured": fp32_measured,
+                 "fp32_probe_sm_mhz": probe_clocks.get("sm_mhz"),
+                 "hbm_peak_basis": "MEASURED_PEAKS.json hbm_gbs (measured copy)"}
+    if probe_clocks.get("sm_mhz"):
+        # the probe's throughput scaled to the maximum SM clock
+        fp32_info["fp32_measured_at_max_clock"] = fp32_measured * max_mhz / probe_clocks["sm_mhz"]
+
+    def layer_roof(w_, ms_, version, which, l_max, entry):
+        flops, basis, xtra = layer_flops(w_, which, l_max)
+        traffic = NCU_TRAFFIC.get((w_.name, version)) if entry == "fused" else None
+        r = roofline(flops, compulsory_bytes(w_), ms_, fp32_peak, hbm_peak, version, traffic, basis, xtra)
+        r.update(fp32_info)
+        return r
+
+    version = kernel_version(wl, args.which, args.lmax, args.entry)
+    if args.which == "graph":
         # positions in; offsets, senders and edge vectors out
         gbytes = 12 * wl.n_atoms + 4 * (wl.n_atoms + 1) + 16 * E_graph
-        hbm = float(peaks.get("hbm_gbs", 6787.2))
-        gach = gbytes / (ms * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "achieved": gach, "peak": hbm, "unit": "GB/s", "frac": gach / hbm,
-                    "traffic": None, "kernel": "radius-graph-v1 (12 launches)",
-                    "algorithmic_bytes": gbytes, "peak_basis": "MEASURED_PEAKS.json hbm_gbs (measured copy)"}
+        label = ("radius-graph cooperative single launch" if coop else
+                 "radius-graph multi-kernel (12 launches)")
+        roof = roofline(0.0, gbytes, ms, fp32_peak, hbm_peak, label, None,
+                        "compulsory bytes: positions, offsets, senders, edge vectors")
+        roof["algorithmic_bytes"] = gbytes
+    else:
+        roof = layer_roof(wl, ms, version, args.which, args.lmax, args.entry)
+
+    workloads = []
+    for x in extra:
+        xw = x["wl"]
+        xv = kernel_version(xw, "forward", 3, "fused")
+        workloads.append({
+            "workload": x["name"], "n_atoms": xw.n_atoms, "n_edges": xw.n_edges, "channels": xw.channels,
+            "storage": xw.storage, "weights": "shared" if xw.w is not None else "radial",
+            "ms_per_step": x["ms"], "value": xw.n_edges * world / (x["ms"] * 1e-3), "unit": "edges/s",
+            "steps": args.steps, "gpu_launches": args.steps,
+            "kernel_ms": {"min": float(np.min(x["kernel_ms"])), "median": float(np.median(x["kernel_ms"])),
+                          "max": float(np.max(x["kernel_ms"]))},
+            "roofline": layer_roof(xw, x["ms"], xv, "forward", 3, "fused"),
+            "clocks": sampler.summary(*x["t"]),
+        })
 
     cpu = None
-    if pool is not None and graph_args is not None:
+    if pool is not None and args.which == "graph":
         from oracle import graph as oracle_graph
 
         pool.terminate()
@@ -533,30 +716,31 @@ def main():
                "sample": f"whole workload ({wl.n_atoms} atoms, {E_cpu} edges), k-d tree candidates + float32 test, {wall:.2f} s"}
     elif pool is not None:
         rate, sample = cpu_oracle_rate(args.workload, wl, pool=pool, cores=cores)
-        pool.terminate()
         cpu = {"value": rate, "unit": "edges/s", "cores": cores, "kind": "oracle", "sample": sample}
+        if args.which == "forward" and args.lmax == 3:
+            cpu["single_thread"] = single_thread_rates(pool, SINGLE_THREAD_WORKLOADS)
+        pool.terminate()
 
+    value = n_edges * world / (ms * 1e-3)
     line = {
-        "metric": METRIC if graph_args is None else METRIC_GRAPH, "value": value, "unit": "edges/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "metric": METRIC if args.which != "graph" else METRIC_GRAPH, "value": value, "unit": "edges/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32" if wl.storage == "f32" else "bf16-storage/f32-compute", "data": "synthetic",
-        "config": {"workload": args.workload, "n_atoms": wl.n_atoms, "n_edges": wl.n_edges,
-                   "channels": wl.channels, "storage": wl.storage,
-                   "weights": "shared" if wl.w is not None else "radial", "entry": args.entry,
-                   "l2": "flushed (256 MB write) before every timed step",
-                   "parallelism": f"replicas x{world}"},
-        "roofline": roofline,
+        "config": workload_config(args.workload, wl, args.entry, world),
+        "roofline": roof,
         "e2e": None if e2e_ms is None else {
             "value": n_edges * world / (e2e_ms * 1e-3), "unit": "edges/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "pass": args.which,
         "l_max": args.lmax,
-        "graph_edges": None if graph_args is None else E_graph,
-        "gpu_launches": args.steps * (1 if args.lmax != 3 else 12 if graph_args is not None else
-                                      (2 if args.entry == "tp_scatter" else 1) if bwd_args is None else 3),
+        "graph_edges": None if args.which != "graph" else E_graph,
+        "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks,
-        "kernel_ms": {"min": float(np.min(kernel_ms)), "median": float(np.median(kernel_ms))},
+        "kernel_ms": {"min": float(np.min(kernel_ms)), "median": float(np.median(kernel_ms)),
+                      "max": float(np.max(kernel_ms))},
+        "workloads": workloads,
+        "fp32_probe": {"tflops": fp32_measured, "clocks": probe_clocks, "launches": len(probe_ms) + 2},
         "watchdog": wd,
         "cpu_baseline": cpu,
     }

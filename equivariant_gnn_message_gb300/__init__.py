@@ -89,6 +89,10 @@ def load_library():
     lib.eqmp_fused_backward.argtypes = [vp, vp, i64, vp, vp, vp, vp, vp, i64, i64, i64, i32, Weights,
                                         vp, vp, vp, vp, vp, vp, vp, i64, vp]
     lib.eqmp_fused_backward.restype = i32
+    lib.eqmp_fused_backward_noalloc.argtypes = [vp, vp, i64, vp, vp, vp, vp, vp, i64, i64, i64, i32, Weights,
+                                                vp, vp, vp, vp, vp, vp, vp]
+    lib.eqmp_fused_backward_noalloc.restype = i32
+    lib.eqmp_fused_backward_noalloc_max_bytes.restype = i64
     lib.eqmp_watchdog_selftest.argtypes = [i32, vp]
     lib.eqmp_watchdog_selftest.restype = i32
     lib.eqmp_fp32_peak_probe.argtypes = [i32, i32, vp, ctypes.POINTER(ctypes.c_double), vp]
@@ -136,10 +140,10 @@ def _require(t, name, dtype=None, cuda=True):
         return
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if cuda and not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
     if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
         raise TypeError(f"{name} has dtype {t.dtype}")
+    if cuda and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
 
@@ -356,17 +360,21 @@ def sender_view(src, n_src):
     return offs, order
 
 
-def eqmp_fused_backward(vec, x, row_offsets, src, dst, send_offsets, send_edges, grad_out,
-                        w=None, R=None, M=None, need=("x", "w", "vec"), stream=None):
-    """Gradients of the fused layer; returns {"x", "w" | "R", "M", "vec"} as requested."""
+def _backward_prepare(vec, x, row_offsets, src, dst, send_offsets, send_edges, grad_out, w, R, M, need):
+    """Checks of the backward's inputs and its requested output tensors."""
     import torch
 
-    for name, t, dt in (("vec", vec, torch.float32), ("x", x, torch.float32),
-                        ("row_offsets", row_offsets, torch.int32), ("src", src, torch.int32),
-                        ("dst", dst, torch.int32), ("send_offsets", send_offsets, torch.int32),
-                        ("send_edges", send_edges, torch.int32), ("grad_out", grad_out, torch.float32),
-                        ("w", w, torch.float32), ("R", R, torch.float32), ("M", M, torch.float32)):
+    spec = (("vec", vec, torch.float32), ("x", x, torch.float32),
+            ("row_offsets", row_offsets, torch.int32), ("src", src, torch.int32),
+            ("dst", dst, torch.int32), ("send_offsets", send_offsets, torch.int32),
+            ("send_edges", send_edges, torch.int32), ("grad_out", grad_out, torch.float32),
+            ("w", w, torch.float32), ("R", R, torch.float32), ("M", M, torch.float32))
+    for name, t, dt in spec:  # every dtype first, then placement and layout
+        _require(t, name, dt, cuda=False)
+    for name, t, dt in spec:
         _require(t, name, dt)
+    if (w is None) == (R is None or M is None):
+        raise ValueError("give exactly one of w or (R, M)")
     n_src, C = x.shape[0], x.shape[1]
     N = row_offsets.shape[0] - 1
     E = vec.shape[0]
@@ -384,19 +392,27 @@ def eqmp_fused_backward(vec, x, row_offsets, src, dst, send_offsets, send_edges,
             out["M"] = torch.empty((8, 34 * C), dtype=torch.float32, device=dev)
     elif "w" in need:
         out["w"] = torch.empty((34, C), dtype=torch.float32, device=dev)
+    wt = (Weights(ctypes.c_void_p(w.data_ptr()), None, None, 0) if not radial else
+          Weights(None, ctypes.c_void_p(R.data_ptr()), ctypes.c_void_p(M.data_ptr()), R.shape[1]))
+    head = (_ptr(vec), _ptr(x), n_src, _ptr(row_offsets), _ptr(src), _ptr(dst), _ptr(send_offsets),
+            _ptr(send_edges), send_edges.shape[0], N, E, C, wt, _ptr(grad_out), _ptr(out.get("x")),
+            _ptr(out.get("w")), _ptr(out.get("R")), _ptr(out.get("M")), _ptr(out.get("vec")))
+    return out, head, (N, E, C, radial)
+
+
+def eqmp_fused_backward(vec, x, row_offsets, src, dst, send_offsets, send_edges, grad_out,
+                        w=None, R=None, M=None, need=("x", "w", "vec"), stream=None):
+    """Gradients of the fused layer; returns {"x", "w" | "R", "M", "vec"} as requested."""
+    import torch
+
+    out, head, (N, E, C, radial) = _backward_prepare(vec, x, row_offsets, src, dst, send_offsets,
+                                                     send_edges, grad_out, w, R, M, need)
     lib = load_library()
     nbytes = int(lib.eqmp_fused_backward_workspace_size(N, E, C, 1 if radial else 0))
     if nbytes < 0:
         raise EqmpError(EQMP_ERR_CUDA, "eqmp_fused_backward_workspace_size")
-    ws = torch.empty(max(nbytes // 4, 4), dtype=torch.float32, device=dev)
-    wt = (Weights(ctypes.c_void_p(w.data_ptr()), None, None, 0) if not radial else
-          Weights(None, ctypes.c_void_p(R.data_ptr()), ctypes.c_void_p(M.data_ptr()), R.shape[1]))
-    st = lib.eqmp_fused_backward(
-        _ptr(vec), _ptr(x), n_src, _ptr(row_offsets), _ptr(src), _ptr(dst), _ptr(send_offsets),
-        _ptr(send_edges), send_edges.shape[0], N, E, C, wt, _ptr(grad_out), _ptr(out.get("x")),
-        _ptr(out.get("w")), _ptr(out.get("R")), _ptr(out.get("M")), _ptr(out.get("vec")),
-        _ptr(ws), ws.numel() * 4, _stream(stream))
-    _check(st, "eqmp_fused_backward")
+    ws = torch.empty(max(nbytes // 4, 4), dtype=torch.float32, device=x.device)
+    _check(lib.eqmp_fused_backward(*head, _ptr(ws), ws.numel() * 4, _stream(stream)), "eqmp_fused_backward")
     return out
 
 
@@ -405,36 +421,7 @@ def eqmp_fused_backward_noalloc(vec, x, row_offsets, src, dst, send_offsets, sen
     """eqmp_fused_backward with the library's static scratch instead of a
     workspace (the C entry point allocates no device memory; this wrapper
     only allocates the requested output tensors through torch)."""
-    import torch
-
-    lib = load_library()
-    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
-    fn = lib.eqmp_fused_backward_noalloc
-    fn.argtypes = [vp, vp, i64, vp, vp, vp, vp, vp, i64, i64, i64, i32, Weights,
-                   vp, vp, vp, vp, vp, vp, vp]
-    fn.restype = i32
-    n_src, C = x.shape[0], x.shape[1]
-    N = row_offsets.shape[0] - 1
-    E = vec.shape[0]
-    radial = w is None
-    dev = x.device
-    out = {}
-    if "x" in need:
-        out["x"] = torch.empty((n_src, C, 16), dtype=torch.float32, device=dev)
-    if "vec" in need:
-        out["vec"] = torch.zeros((E, 3), dtype=torch.float32, device=dev)
-    if radial:
-        if "R" in need:
-            out["R"] = torch.zeros((E, 8), dtype=torch.float32, device=dev)
-        if "M" in need:
-            out["M"] = torch.empty((8, 34 * C), dtype=torch.float32, device=dev)
-    elif "w" in need:
-        out["w"] = torch.empty((34, C), dtype=torch.float32, device=dev)
-    wt = (Weights(ctypes.c_void_p(w.data_ptr()), None, None, 0) if not radial else
-          Weights(None, ctypes.c_void_p(R.data_ptr()), ctypes.c_void_p(M.data_ptr()), R.shape[1]))
-    st = fn(_ptr(vec), _ptr(x), n_src, _ptr(row_offsets), _ptr(src), _ptr(dst), _ptr(send_offsets),
-            _ptr(send_edges), send_edges.shape[0], N, E, C, wt, _ptr(grad_out), _ptr(out.get("x")),
-            _ptr(out.get("w")), _ptr(out.get("R")), _ptr(out.get("M")), _ptr(out.get("vec")),
-            _stream(stream))
-    _check(st, "eqmp_fused_backward_noalloc")
+    out, head, _ = _backward_prepare(vec, x, row_offsets, src, dst, send_offsets, send_edges, grad_out,
+                                     w, R, M, need)
+    _check(load_library().eqmp_fused_backward_noalloc(*head, _stream(stream)), "eqmp_fused_backward_noalloc")
     return out

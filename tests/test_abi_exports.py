@@ -107,3 +107,27 @@ def test_generated_tables_match_oracle():
             assert np.allclose(poly * pw.real, Y[:, l * l + l + m], atol=1e-14)
             if m:
                 assert np.allclose(poly * pw.imag, Y[:, l * l + l - m], atol=1e-14)
+
+
+@pytest.mark.parametrize("entry", ["eqmp_fused_backward", "eqmp_fused_backward_noalloc"])
+def test_backward_wrappers_reject_a_wrong_dtype_before_any_call(lib, entry):
+    """A float64 x (or int64 index array) never reaches the C entry point as
+    a raw pointer: the binding raises TypeError first (no GPU needed)."""
+    import torch
+
+    import equivariant_gnn_message_gb300 as eq
+
+    f32, i32 = torch.float32, torch.int32
+    args = dict(vec=torch.zeros(6, 3, dtype=f32), x=torch.zeros(3, 8, 16, dtype=f32),
+                row_offsets=torch.zeros(4, dtype=i32), src=torch.zeros(6, dtype=i32),
+                dst=torch.zeros(6, dtype=i32), send_offsets=torch.zeros(4, dtype=i32),
+                send_edges=torch.zeros(6, dtype=i32), grad_out=torch.zeros(3, 8, 16, dtype=f32))
+    fn = getattr(eq, entry)
+    for name, bad in (("x", torch.zeros(3, 8, 16, dtype=torch.float64)),
+                      ("src", torch.zeros(6, dtype=torch.int64)),
+                      ("grad_out", torch.zeros(3, 8, 16, dtype=torch.float64))):
+        kw = dict(args, **{name: bad})
+        with pytest.raises(TypeError, match=name):
+            fn(**kw, w=torch.zeros(34, 8, dtype=f32))
+    with pytest.raises(ValueError, match="CUDA"):  # right dtypes, host memory
+        fn(**args, w=torch.zeros(34, 8, dtype=f32))

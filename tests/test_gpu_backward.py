@@ -60,6 +60,24 @@ def test_backward_workloads(eq, name):
         assert rel_err(got[k], want[k]) <= TOL, k
 
 
+@pytest.mark.parametrize("mode", ["shared", "radial"])
+def test_backward_10k_atoms_every_gradient(eq, mode):
+    """A 10,000-atom graph (about 190k edges, C = 32) in full: every row of
+    dx, dvec (and dR) and every entry of dw (dM) against the oracle, which
+    runs on all host cores (per receiver range, partial gradients summed)."""
+    from tests import oracle_pool
+
+    wl = make_workload(n_atoms=10_000, cutoff=5.0, channels=32, weights=mode, storage="f32", seed=210)
+    g = np.random.default_rng(3).standard_normal((wl.n_atoms, 32, 16)).astype(np.float32)
+    need = ("x", "vec", "w") if mode == "shared" else ("x", "vec", "R", "M")
+    got = _run(eq, wl, g, need)
+    want = oracle_pool.layer_backward_all(wl, g)
+    for k in need:
+        err = rel_err(got[k], want[k])
+        print(f"backward 10k {mode} grad {k}: E={wl.n_edges} rel err {err:.3e}")
+        assert err <= TOL, f"grad {k}: rel err {err:.3e}"
+
+
 def test_backward_deterministic_and_skips(eq):
     wl = make_workload(n_atoms=200, cutoff=5.0, channels=32, weights="shared", storage="f32", seed=5)
     g = np.random.default_rng(2).standard_normal((wl.n_atoms, 32, 16)).astype(np.float32)

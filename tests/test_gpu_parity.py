@@ -45,6 +45,7 @@ def _check_full(eq, wl, entry="fused"):
     got = host(_run(eq, d, entry, wl))
     want = layer.message_pass(wl.vec, wl.x, wl.off, wl.src, **oracle_kw(wl))
     err = rel_err(got, want)
+    print(f"{wl.name} {entry}: E={wl.n_edges} rel err {err:.3e}")
     assert err <= TOL[wl.storage], f"{wl.name} {entry}: rel err {err:.3e}"
     assert eq.eqmp_device_error() == 0
     return err
@@ -83,23 +84,27 @@ def test_workload_full_parity(eq, name, entry):
     _check_full(eq, make_workload(name), entry)
 
 
-@pytest.mark.parametrize("name,n_sample", [("scale_100k_c64", 256), ("dense_10k_c128_bf16", 96)])
-def test_workload_full_size_sampled(eq, name, n_sample):
-    """Full-size graphs in the launch configuration the benchmark times;
-    the oracle checks a sample of receivers (first, last, highest degree,
-    random)."""
+@pytest.mark.parametrize("name", ["scale_100k_c64", "dense_10k_c128_bf16"])
+def test_workload_full_size_every_receiver(eq, name):
+    """The two largest workloads in the launch configuration the benchmark
+    times, compared element by element on every receiver (100,000 and
+    10,000 rows) with the oracle, which runs on all host cores."""
+    from tests import oracle_pool
+
     wl = make_workload(name)
     d = to_device(wl)
     got = host(_run(eq, d, "fused", wl))
-    deg = np.diff(wl.off)
-    rng = np.random.default_rng(0)
-    pick = np.unique(np.concatenate([[0, wl.n_atoms - 1, int(np.argmax(deg)), int(np.argmin(deg))],
-                                     rng.choice(wl.n_atoms, n_sample, replace=False)]))
-    want = layer.message_pass(wl.vec, wl.x, wl.off, wl.src, receivers=pick, **oracle_kw(wl))
-    err = rel_err(got[pick], want)
-    assert err <= TOL[wl.storage], f"{name}: rel err {err:.3e}"
-    assert np.all(np.isfinite(got))
     assert eq.eqmp_device_error() == 0
+    want = oracle_pool.message_pass_all(wl)
+    assert got.shape == want.shape
+    assert np.all(np.isfinite(got))
+    err = rel_err(got, want)
+    assert err <= TOL[wl.storage], f"{name}: rel err {err:.3e}"
+    # the CTA-boundary receivers (a receiver whose edges start on an odd
+    # ring ordinal takes the kernel's half-pair path) are among the rows
+    # checked; record the error at the worst receiver for the report
+    row = np.max(np.abs(got - want), axis=(1, 2))
+    print(f"{name}: E={wl.n_edges} rel err {err:.3e}, worst receiver {int(np.argmax(row))}")
 
 
 # ---------------------------------------------------------------- C x dtype x mode

@@ -5,14 +5,15 @@ device memory (a plugin inside a framework that owns the memory pool, a
 simulation loop that must not allocate every step).  Its scratch is a
 static device array shared by all calls.  This test calls it through the C
 ABI twice in a row (the second call starts from the first call's leftover
-scratch) and compares every gradient with eqmp_fused_backward, within the
-parity tolerance of the GPU tests.  It runs last so a failure here leaves
-the rest of the suite already run.
+scratch) and compares every gradient with eqmp_fused_backward and with the
+CPU oracle's gradients, within the parity tolerance of the GPU tests.  It
+runs last so a failure here leaves the rest of the suite already run.
 """
 import numpy as np
 import pytest
 
 from equivariant_gnn_message_gb300.inputs import make_workload
+from oracle import backward
 
 pytestmark = pytest.mark.gpu
 
@@ -26,7 +27,8 @@ def _rel(a, b):
     return float(np.max(np.abs(a - b)) / scale) if scale > 0 else float(np.max(np.abs(a)))
 
 
-@pytest.mark.parametrize("mode,C,n_atoms", [("shared", 32, 400), ("shared", 128, 600), ("radial", 8, 40)])
+@pytest.mark.parametrize("mode,C,n_atoms", [("shared", 32, 400), ("shared", 64, 500), ("shared", 128, 600),
+                                             ("radial", 8, 40)])
 def test_noalloc_backward_matches_workspace_backward(mode, C, n_atoms):
     import torch
 
@@ -47,9 +49,13 @@ def test_noalloc_backward_matches_workspace_backward(mode, C, n_atoms):
         ref = eq.eqmp_fused_backward(*args, **kw)
         got = eq.eqmp_fused_backward_noalloc(*args, **kw)
         torch.cuda.synchronize()
+        okw = dict(w=wl.w) if mode == "shared" else dict(R=wl.R, M=wl.M)
+        want = backward.layer_backward(wl.vec, wl.x, wl.off, wl.src, g.cpu().numpy(), **okw)
         for k in need:
             err = _rel(got[k], ref[k])
-            assert err <= TOL, f"call {call}, grad {k}: rel err {err:.3e}"
+            assert err <= TOL, f"call {call}, grad {k}: rel err {err:.3e} against the workspace entry"
+            err = _rel(got[k], torch.from_numpy(want[k]))
+            assert err <= TOL, f"call {call}, grad {k}: rel err {err:.3e} against the oracle"
     assert eq.eqmp_device_error() == 0
     assert eq.load_library().eqmp_fused_backward_noalloc_max_bytes() == 8 << 20
 

@@ -17,7 +17,9 @@ Modules
   backward  the chain rule of that layer: gradients of x, w (or R and M)
          and of the edge vectors through the harmonics.
   graph  the radius graph (ordered pairs closer than the cutoff, CSR by
-         receiver), with the cutoff decision taken in float32.
+         receiver), with the cutoff decision taken in float32; open
+         boundaries, or a periodic orthorhombic box (every image within
+         one box length per direction).
 
 sh, cg and layer take the degree as a parameter (l_max = 3 by default, the
 Batmobile layer; l_max = 4..6 for the higher-degree variant the blog lists

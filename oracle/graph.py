@@ -29,6 +29,28 @@ Two routes to the same set:
   radius_graph             candidate pairs from scipy's k-d tree at a
                            slightly larger radius (a library primitive used
                            as a step), then the float32 test above.
+
+Periodic boundaries.  E2Former-V2 (section 4.2) handles periodic systems by
+expanding the cells, one image per direction.  Reading: an orthorhombic box
+of sides L = (L_x, L_y, L_z), positions inside it (0 <= p_a < L_a), and the
+directed edges
+
+    (sender j, image s) -> receiver i   for every s in {-1, 0, 1}^3 and every
+                                        j with |p_j + s L - p_i| < r_c,
+                                        except j = i with s = 0,
+
+with d_a = (p_j[a] - p_i[a]) + s_a L_a (two float32 operations, s_a L_a
+exact), d2 and the test as above, vec = d.  One image per direction is all
+there is when r_c <= min(L) (a shift of 2 puts every image at least L away),
+which is required.  Several images of one sender can be edges of the same
+receiver (r_c > L/2); each is its own edge.  Rows are sorted by sender,
+then by the image index sigma = (s_x + 1) + 3 (s_y + 1) + 9 (s_z + 1).  With
+s = 0 the arithmetic is the open-boundary one, bit for bit.
+  radius_graph_pbc_bruteforce  every (pair, image), chunked (small N);
+  radius_graph_pbc             candidate pairs from scipy's periodic k-d
+                               tree (minimum-image distance, a library
+                               primitive) at a slightly larger radius, then
+                               every image of each candidate pair tested.
 """
 import numpy as np
 
@@ -99,3 +121,88 @@ def radius_graph(pos, cutoff):
     keep = _d2(pos[i], pos[j]) < rc2
     off, src, dst = _csr(i[keep], j[keep], n)
     return _finish(pos, off, src, dst)
+
+
+# ---------------------------------------------------------------- periodic
+# image shifts in index order sigma = (s_x + 1) + 3 (s_y + 1) + 9 (s_z + 1)
+SHIFTS = np.array([(sx, sy, sz) for sz in (-1, 0, 1) for sy in (-1, 0, 1) for sx in (-1, 0, 1)],
+                  dtype=np.int64)
+SELF_IMAGE = 13  # sigma of s = (0, 0, 0)
+
+
+def _box(pos, cutoff, box):
+    box = np.asarray(box, dtype=_F32).reshape(3)
+    if not np.all(np.isfinite(box)) or np.any(box <= 0):
+        raise ValueError("box sides must be positive")
+    if _F32(cutoff) > np.min(box):
+        raise ValueError("the cutoff must not exceed the smallest box side")
+    if len(pos) and (np.any(pos < 0) or np.any(pos >= box[None, :])):
+        raise ValueError("positions must lie inside the box, 0 <= p < L")
+    return box
+
+
+def _image_vec(pi, pj, sL):
+    """float32 d = (p_j - p_i) + s L, each operation rounded on its own."""
+    return ((pj - pi).astype(_F32) + sL).astype(_F32)
+
+
+def _d2v(d):
+    return (d[..., 0] * d[..., 0] + d[..., 1] * d[..., 1]) + d[..., 2] * d[..., 2]
+
+
+def _csr_pbc(dst, src, img, n, pos, box):
+    order = np.lexsort((img, src, dst))
+    dst, src, img = dst[order], src[order], img[order]
+    off = np.searchsorted(dst, np.arange(n + 1), side="left").astype(np.int64)
+    sL = (SHIFTS[img].astype(_F32) * box[None, :]).astype(_F32)
+    vec = _image_vec(pos[dst], pos[src], sL)
+    return dict(off=off, src=src.astype(np.int64), dst=dst.astype(np.int64), img=img.astype(np.int64), vec=vec)
+
+
+def radius_graph_pbc_bruteforce(pos, cutoff, box, chunk=128):
+    """Every (receiver, sender, image) tested; dict(off, src, dst, img, vec)."""
+    pos = np.ascontiguousarray(pos, dtype=_F32).reshape(-1, 3)
+    n = len(pos)
+    box = _box(pos, cutoff, box)
+    rc2 = _rc2(cutoff)
+    dsts, srcs, imgs = [], [], []
+    for k, s in enumerate(SHIFTS):
+        sL = (s.astype(_F32) * box).astype(_F32)
+        for a in range(0, n, chunk):
+            d = _image_vec(pos[a:a + chunk, None, :], pos[None, :, :], sL)
+            ii, jj = np.nonzero(_d2v(d) < rc2)
+            ii = ii + a
+            keep = (ii != jj) | (k != SELF_IMAGE)
+            dsts.append(ii[keep])
+            srcs.append(jj[keep])
+            imgs.append(np.full(int(keep.sum()), k, np.int64))
+    cat = lambda x: np.concatenate(x) if x else np.zeros(0, np.int64)
+    return _csr_pbc(cat(dsts), cat(srcs), cat(imgs), n, pos, box)
+
+
+def radius_graph_pbc(pos, cutoff, box):
+    """Same set as radius_graph_pbc_bruteforce, candidate pairs from a
+    periodic k-d tree: a pair with any image inside the cutoff has its
+    minimum-image distance inside it too."""
+    from scipy.spatial import cKDTree
+
+    pos = np.ascontiguousarray(pos, dtype=_F32).reshape(-1, 3)
+    n = len(pos)
+    box = _box(pos, cutoff, box)
+    rc2 = _rc2(cutoff)
+    if n == 0:
+        z = np.zeros(0, np.int64)
+        return _csr_pbc(z, z, z, 0, pos, box)
+    r_search = float(cutoff) * (1.0 + 1e-3) + 1e-3 + 1e-5 * float(np.max(box))
+    tree = cKDTree(pos.astype(np.float64), boxsize=box.astype(np.float64))
+    pairs = tree.query_pairs(r_search, output_type="ndarray").reshape(-1, 2).astype(np.int64)
+    i = np.concatenate([pairs[:, 0], pairs[:, 1]])
+    j = np.concatenate([pairs[:, 1], pairs[:, 0]])
+    dsts, srcs, imgs = [], [], []
+    for k, s in enumerate(SHIFTS):  # a sender is never its own image: r_c <= min(L)
+        sL = (s.astype(_F32) * box).astype(_F32)
+        keep = _d2v(_image_vec(pos[i], pos[j], sL)) < rc2
+        dsts.append(i[keep])
+        srcs.append(j[keep])
+        imgs.append(np.full(int(keep.sum()), k, np.int64))
+    return _csr_pbc(np.concatenate(dsts), np.concatenate(srcs), np.concatenate(imgs), n, pos, box)

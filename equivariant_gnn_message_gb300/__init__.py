@@ -17,7 +17,7 @@ Entry points (same names as the C ABI):
   eqmp_fused_backward(vec, x, row_offsets, src, dst, send_offsets, send_edges, grad_out, ...)
                                                 -> dict of gradients
   eqmp_fused_backward_noalloc(...)              -> the same, no workspace
-  eqmp_radius_graph(pos, cutoff)                -> (dict(off, src, vec[, dst, rev]), E)
+  eqmp_radius_graph(pos, cutoff, box=None)      -> (dict(off, src, vec[, img, dst, rev]), E)
   eqmp_fused_lmax(l_max, vec, x, row_offsets, src, ...) -> out, degree 4..6
   eqmp_path_table()                             -> list of (l1, l2, l3)
 """
@@ -106,6 +106,9 @@ def load_library():
     lib.eqmp_radius_graph.argtypes = [vp, i64, ctypes.c_float, vp, vp, vp, vp, vp, i64, vp, vp,
                                       ctypes.c_size_t, vp]
     lib.eqmp_radius_graph.restype = i32
+    lib.eqmp_radius_graph_pbc.argtypes = [vp, i64, ctypes.c_float, ctypes.POINTER(ctypes.c_float), vp, vp, vp, vp,
+                                          vp, vp, i64, vp, vp, ctypes.c_size_t, vp]
+    lib.eqmp_radius_graph_pbc.restype = i32
     _lib = lib
     return lib
 
@@ -304,13 +307,16 @@ def eqmp_fused_lmax(l_max, vec, x, row_offsets, src, w=None, R=None, M=None, out
     return out
 
 
-def eqmp_radius_graph(pos, cutoff, e_cap=None, dst=False, rev=False, stream=None):
-    """Radius graph of pos [N, 3] fp32 (CUDA): dict(off, src, vec[, dst][, rev]), E.
+def eqmp_radius_graph(pos, cutoff, e_cap=None, dst=False, rev=False, stream=None, box=None):
+    """Radius graph of pos [N, 3] fp32 (CUDA): dict(off, src, vec[, img][, dst][, rev]), E.
 
     Edges j -> i for i != j with the float32 squared distance below
-    cutoff^2, CSR by receiver with senders ascending.  When the edge count
-    exceeds the capacity (e_cap, default 64 N), the call is repeated once
-    with the exact count, which costs one device-to-host read of E.
+    cutoff^2, CSR by receiver with senders ascending.  With box = (Lx, Ly, Lz)
+    the boundaries are periodic (eqmp_radius_graph_pbc): positions inside the
+    box, every image within one box length per direction, and "img" holds
+    each edge's image index.  When the edge count exceeds the capacity
+    (e_cap, default 64 N), the call is repeated once with the exact count,
+    which costs one device-to-host read of E.
     """
     import torch
 
@@ -332,17 +338,26 @@ def eqmp_radius_graph(pos, cutoff, e_cap=None, dst=False, rev=False, stream=None
             out["dst"] = torch.empty(cap, dtype=torch.int32, device=dev)
         if rev:
             out["rev"] = torch.empty(cap, dtype=torch.int32, device=dev)
-        _check(lib.eqmp_radius_graph(_ptr(pos), N, float(cutoff), _ptr(off), _ptr(out["src"]),
-                                     _ptr(out["vec"]), _ptr(out.get("dst")), _ptr(out.get("rev")), cap,
-                                     _ptr(e_total), _ptr(ws), ws.numel(), st), "eqmp_radius_graph")
+        if box is None:
+            _check(lib.eqmp_radius_graph(_ptr(pos), N, float(cutoff), _ptr(off), _ptr(out["src"]),
+                                         _ptr(out["vec"]), _ptr(out.get("dst")), _ptr(out.get("rev")), cap,
+                                         _ptr(e_total), _ptr(ws), ws.numel(), st), "eqmp_radius_graph")
+        else:
+            out["img"] = torch.empty(cap, dtype=torch.int32, device=dev)
+            lengths = (ctypes.c_float * 3)(*[float(v) for v in box])
+            _check(lib.eqmp_radius_graph_pbc(_ptr(pos), N, float(cutoff), lengths, _ptr(off), _ptr(out["src"]),
+                                             _ptr(out["vec"]), _ptr(out["img"]), _ptr(out.get("dst")),
+                                             _ptr(out.get("rev")), cap, _ptr(e_total), _ptr(ws), ws.numel(), st),
+                   "eqmp_radius_graph_pbc")
         E = int(e_total.item())
         if E < 0:
             raise EqmpError(EQMP_ERR_INVALID_ARG, "eqmp_radius_graph: positions non-finite or out of range"
+                            " (outside the box, with periodic boundaries)"
                             if E == -1 else "eqmp_radius_graph: 2^31 edges or more")
         if E <= cap:
             break
         cap = E
-    for k in ("src", "vec", "dst", "rev"):
+    for k in ("src", "vec", "img", "dst", "rev"):
         if k in out:
             out[k] = out[k][:E]
     return out, E

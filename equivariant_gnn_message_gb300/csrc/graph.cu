@@ -26,6 +26,19 @@
 // Bucket order and fill order depend on atomics; the output does not: the
 // degree is a count and each row is sorted, so the result is bitwise
 // deterministic.
+//
+// Periodic boundaries (eqmp_radius_graph_pbc; E2Former-V2 section 4.2:
+// periodic systems by expanded cells, one image per direction): positions
+// in an orthorhombic box [0, L), r_c <= min(L); edges (j, image s) -> i for
+// s in {-1, 0, 1}^3 with d_a = (p_j[a] - p_i[a]) + s_a L_a below the cutoff
+// (same test), except j = i with s = 0.  The cells tile the box (n_a per
+// axis, side >= r_c (1 + 2^-10)); an axis shorter than three cells is one
+// cell whose three images are walked explicitly.  Wrapped cells are hashed
+// into the same bucket table; the walk keys each of its 27 lanes by
+// (bucket, image), so one bucket visited under two images is walked twice
+// and under one image once.  The fill writes j * 27 + image; the row sort
+// ranks by that key (sender, then image index sigma = (s_x + 1) +
+// 3 (s_y + 1) + 9 (s_z + 1)) and writes src, img and vec.
 #include <math.h>
 #include <stdint.h>
 
@@ -44,6 +57,7 @@ constexpr int kSortWarps = 8;
 constexpr int kSortCap = 512;          // row length sorted in shared memory
 constexpr float kCellRange = 4096.0f;  // |p| / cell side must stay below this
 constexpr long long kGraphMaxAtoms = 1ll << 30;  // keeps the bucket count <= 2^31
+constexpr long long kGraphMaxAtomsPbc = 1ll << 26;  // keys sender * 27 + image stay below 2^31
 constexpr int kCoopMaxBlocks = 2048;              // cooperative grid cap (block totals it can hold)
 constexpr long long kCoopMaxAtoms = 16384;        // the single launch is used up to this many atoms
 constexpr unsigned long long kGridWaitNs = 4000000000ull;
@@ -64,6 +78,38 @@ __device__ __forceinline__ uint32_t cell_hash(int cx, int cy, int cz, uint32_t m
 __device__ __forceinline__ int cell_of(float p, float inv) {
   const float c = floorf(__fmul_rn(p, inv));
   return (int)fminf(fmaxf(c, -kCellRange - 2.0f), kCellRange + 2.0f);
+}
+
+// Periodic box: sides, cells per axis (1: one cell spanning the axis, its
+// images walked explicitly), cells per unit length.
+struct Box {
+  float L[3];
+  float inv[3];
+  int n[3];
+};
+constexpr int kImages = 27;
+constexpr int kSelfImage = 13;  // s = (0, 0, 0)
+
+__device__ __forceinline__ int pbc_cell(float p, float inv, int n) {
+  if (n == 1) return 0;
+  const int c = (int)floorf(__fmul_rn(p, inv));
+  return min(max(c, 0), n - 1);
+}
+
+// image shift of component a of image index sigma
+__device__ __forceinline__ int image_shift(int sigma, int a) {
+  return (a == 0 ? sigma : a == 1 ? sigma / 3 : sigma / 9) % 3 - 1;
+}
+
+// d_a = (p_j[a] - p_i[a]) + s_a L_a, each operation rounded on its own
+__device__ __forceinline__ float3 image_vec(float3 pi, float3 pj, int sigma, const Box& box) {
+  return make_float3(__fadd_rn(__fsub_rn(pj.x, pi.x), (float)image_shift(sigma, 0) * box.L[0]),
+                     __fadd_rn(__fsub_rn(pj.y, pi.y), (float)image_shift(sigma, 1) * box.L[1]),
+                     __fadd_rn(__fsub_rn(pj.z, pi.z), (float)image_shift(sigma, 2) * box.L[2]));
+}
+
+__device__ __forceinline__ float norm2(float3 d) {
+  return __fadd_rn(__fadd_rn(__fmul_rn(d.x, d.x), __fmul_rn(d.y, d.y)), __fmul_rn(d.z, d.z));
 }
 
 __device__ __forceinline__ float dist2(float3 a, float3 b) {
@@ -174,23 +220,34 @@ __global__ void k_clear(int32_t* __restrict__ a, long long n, int* __restrict__ 
   if (blockIdx.x == 0 && threadIdx.x == 0) *bad = 0;
 }
 
+template <bool PBC>
 __device__ __forceinline__ void bin_one(int i, const float* __restrict__ pos, float inv, uint32_t mask,
                                         int32_t* __restrict__ atom_bucket, int32_t* __restrict__ count,
-                                        int* __restrict__ bad) {
+                                        int* __restrict__ bad, const Box& box) {
   const float3 p = load_pos(pos, i);
-  const float qx = __fmul_rn(p.x, inv), qy = __fmul_rn(p.y, inv), qz = __fmul_rn(p.z, inv);
-  // false for NaN as well as for out-of-range coordinates
-  const bool ok = fabsf(qx) < kCellRange && fabsf(qy) < kCellRange && fabsf(qz) < kCellRange;
-  if (!ok) atomicOr(bad, 1);
-  const uint32_t h = cell_hash(cell_of(p.x, inv), cell_of(p.y, inv), cell_of(p.z, inv), mask);
+  uint32_t h;
+  if constexpr (PBC) {
+    // inside the box (false for NaN as well)
+    const bool ok = p.x >= 0.0f && p.x < box.L[0] && p.y >= 0.0f && p.y < box.L[1] && p.z >= 0.0f && p.z < box.L[2];
+    if (!ok) atomicOr(bad, 1);
+    h = cell_hash(pbc_cell(p.x, box.inv[0], box.n[0]), pbc_cell(p.y, box.inv[1], box.n[1]),
+                  pbc_cell(p.z, box.inv[2], box.n[2]), mask);
+  } else {
+    const float qx = __fmul_rn(p.x, inv), qy = __fmul_rn(p.y, inv), qz = __fmul_rn(p.z, inv);
+    // false for NaN as well as for out-of-range coordinates
+    const bool ok = fabsf(qx) < kCellRange && fabsf(qy) < kCellRange && fabsf(qz) < kCellRange;
+    if (!ok) atomicOr(bad, 1);
+    h = cell_hash(cell_of(p.x, inv), cell_of(p.y, inv), cell_of(p.z, inv), mask);
+  }
   atom_bucket[i] = (int32_t)h;
   atomicAdd(count + h, 1);
 }
 
+template <bool PBC>
 __global__ void k_bin(const float* __restrict__ pos, int N, float inv, uint32_t mask, int32_t* __restrict__ atom_bucket,
-                      int32_t* __restrict__ count, int* __restrict__ bad) {
+                      int32_t* __restrict__ count, int* __restrict__ bad, const Box box) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < N) bin_one(i, pos, inv, mask, atom_bucket, count, bad);
+  if (i < N) bin_one<PBC>(i, pos, inv, mask, atom_bucket, count, bad, box);
 }
 
 // Atoms listed bucket by bucket, with a copy of their positions in the same
@@ -221,12 +278,15 @@ __global__ void k_scatter(const float* __restrict__ pos, int N, const int32_t* _
 // binary search over the lanes' running sizes.
 // FILL = false: row_offsets[i] = degree of i (row_offsets[N] = 0).
 // FILL = true:  senders of i written, unsorted, to src[off[i] .. off[i+1]).
-template <bool FILL>
+// PBC: each lane names a (wrapped cell, image) pair; duplicates are merged
+// on (bucket, image); a candidate is tested with its lane's image shift and
+// the fill writes sender * 27 + image.
+template <bool FILL, bool PBC>
 __device__ __forceinline__ void neigh_row(long long wg, int lane, const float4* __restrict__ bucket_pos, float inv,
                                           float rc2, uint32_t mask, const int32_t* __restrict__ start,
                                           const int32_t* __restrict__ bucket_atoms,
                                           int32_t* __restrict__ row_offsets, int32_t* __restrict__ src,
-                                          long long e_cap) {
+                                          long long e_cap, const Box& box) {
   const int i = bucket_atoms[wg];  // the receiver sits at slot wg of the bucket order
   const float4 pw = bucket_pos[wg];
   const float3 pi = make_float3(pw.x, pw.y, pw.z);
@@ -236,10 +296,32 @@ __device__ __forceinline__ void neigh_row(long long wg, int lane, const float4* 
     w_end = row_offsets[i + 1];
     if (w < 0 || w_end > e_cap || w_end < w) return;  // row outside the caller's capacity
   }
-  const int cx = cell_of(pi.x, inv), cy = cell_of(pi.y, inv), cz = cell_of(pi.z, inv);
-  const uint32_t h = lane < 27 ? cell_hash(cx + lane % 3 - 1, cy + (lane / 3) % 3 - 1, cz + lane / 9 - 1, mask)
-                               : 0xffffffffu;
-  const unsigned same = __match_any_sync(0xffffffffu, h);
+  uint32_t h;
+  int sigma = kSelfImage;  // this lane's image (PBC)
+  unsigned same;
+  if constexpr (PBC) {
+    const int dc[3] = {lane % 3 - 1, (lane / 3) % 3 - 1, lane / 9 - 1};
+    const float pc[3] = {pi.x, pi.y, pi.z};
+    int wc[3], sh[3];
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+      if (box.n[a] == 1) {  // one cell: the neighbour "cells" are its images
+        wc[a] = 0;
+        sh[a] = dc[a];
+      } else {
+        const int t = pbc_cell(pc[a], box.inv[a], box.n[a]) + dc[a];
+        sh[a] = t < 0 ? -1 : (t >= box.n[a] ? 1 : 0);
+        wc[a] = t - sh[a] * box.n[a];
+      }
+    }
+    sigma = (sh[0] + 1) + 3 * (sh[1] + 1) + 9 * (sh[2] + 1);
+    h = lane < 27 ? cell_hash(wc[0], wc[1], wc[2], mask) : 0xffffffffu;
+    same = __match_any_sync(0xffffffffu, ((unsigned long long)h << 5) | (unsigned)sigma);
+  } else {
+    const int cx = cell_of(pi.x, inv), cy = cell_of(pi.y, inv), cz = cell_of(pi.z, inv);
+    h = lane < 27 ? cell_hash(cx + lane % 3 - 1, cy + (lane / 3) % 3 - 1, cz + lane / 9 - 1, mask) : 0xffffffffu;
+    same = __match_any_sync(0xffffffffu, h);
+  }
   const bool keep = lane < 27 && (same & ((1u << lane) - 1u)) == 0u;
   const int b0 = keep ? start[h] : 0;
   const int nb = keep ? start[h + 1] - b0 : 0;
@@ -263,16 +345,20 @@ __device__ __forceinline__ void neigh_row(long long wg, int lane, const float4* 
     L = min(L, 31);
     const int lb0 = __shfl_sync(0xffffffffu, b0, L);
     const int lex = __shfl_sync(0xffffffffu, incl - nb, L);
+    const int lsig = PBC ? __shfl_sync(0xffffffffu, sigma, L) : kSelfImage;
     bool hit = false;
     const int slot = lb0 + (t - lex);
     if (t < total) {
       const float4 q = bucket_pos[slot];
-      hit = slot != wg && dist2(pi, make_float3(q.x, q.y, q.z)) < rc2;
+      if constexpr (PBC)
+        hit = (slot != wg || lsig != kSelfImage) && norm2(image_vec(pi, make_float3(q.x, q.y, q.z), lsig, box)) < rc2;
+      else
+        hit = slot != wg && dist2(pi, make_float3(q.x, q.y, q.z)) < rc2;
     }
     const unsigned bal = __ballot_sync(0xffffffffu, hit);
     if (FILL) {
       const long long at = w + __popc(bal & ((1u << lane) - 1u));
-      if (hit && at < w_end) src[at] = bucket_atoms[slot];
+      if (hit && at < w_end) src[at] = PBC ? bucket_atoms[slot] * kImages + lsig : bucket_atoms[slot];
       w += __popc(bal);
     } else {
       count += __popc(bal);
@@ -281,16 +367,17 @@ __device__ __forceinline__ void neigh_row(long long wg, int lane, const float4* 
   if (!FILL && lane == 0) row_offsets[i] = count;
 }
 
-template <bool FILL>
+template <bool FILL, bool PBC>
 __global__ void __launch_bounds__(kNeighThreads) k_neigh(const float4* __restrict__ bucket_pos, int N, float inv,
                                                          float rc2, uint32_t mask, const int32_t* __restrict__ start,
                                                          const int32_t* __restrict__ bucket_atoms,
                                                          int32_t* __restrict__ row_offsets,
-                                                         int32_t* __restrict__ src, long long e_cap) {
+                                                         int32_t* __restrict__ src, long long e_cap, const Box box) {
   const int lane = threadIdx.x & 31;
   const long long wg = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (!FILL && wg == 0 && lane == 0) row_offsets[N] = 0;
-  if (wg < N) neigh_row<FILL>(wg, lane, bucket_pos, inv, rc2, mask, start, bucket_atoms, row_offsets, src, e_cap);
+  if (wg < N)
+    neigh_row<FILL, PBC>(wg, lane, bucket_pos, inv, rc2, mask, start, bucket_atoms, row_offsets, src, e_cap, box);
 }
 
 // ------------------------------------------------------------ row sort
@@ -299,9 +386,36 @@ __global__ void __launch_bounds__(kNeighThreads) k_neigh(const float4* __restric
 // kSortCap are ranked from shared memory; longer rows are staged in the
 // row's own vec storage (3 words per edge, so it holds the row) and ranked
 // from there before vec is written.
+// PBC: the row holds keys sender * 27 + image (distinct); ranked the same
+// way, then written as src (sender), img (image) and vec (the image's d).
+template <bool PBC>
+__device__ __forceinline__ void put_edge(long long e, int key, int i, float3 pi, const float* __restrict__ pos,
+                                         int32_t* __restrict__ src, int32_t* __restrict__ img,
+                                         float* __restrict__ vec, int32_t* __restrict__ dst, const Box& box) {
+  float* o = vec + 3 * e;
+  if constexpr (PBC) {
+    const int j = key / kImages, sigma = key - j * kImages;
+    const float3 d = image_vec(pi, load_pos(pos, j), sigma, box);
+    src[e] = j;
+    img[e] = sigma;
+    o[0] = d.x;
+    o[1] = d.y;
+    o[2] = d.z;
+  } else {
+    const float3 pj = load_pos(pos, key);
+    src[e] = key;
+    o[0] = __fsub_rn(pj.x, pi.x);
+    o[1] = __fsub_rn(pj.y, pi.y);
+    o[2] = __fsub_rn(pj.z, pi.z);
+  }
+  if (dst) dst[e] = i;
+}
+
+template <bool PBC>
 __device__ __forceinline__ void sort_row(int i, int lane, int32_t* sm, const float* __restrict__ pos,
                                          const int32_t* __restrict__ row_offsets, int32_t* __restrict__ src,
-                                         float* __restrict__ vec, int32_t* __restrict__ dst, long long e_cap) {
+                                         int32_t* __restrict__ img, float* __restrict__ vec,
+                                         int32_t* __restrict__ dst, long long e_cap, const Box& box) {
   const long long beg = row_offsets[i], end = row_offsets[i + 1];
   if (beg < 0 || end > e_cap || end < beg) return;
   const int k = (int)(end - beg);
@@ -314,13 +428,7 @@ __device__ __forceinline__ void sort_row(int i, int lane, int32_t* sm, const flo
       const int v = sm[a];
       int r = 0;
       for (int b = 0; b < k; ++b) r += sm[b] < v;
-      row[r] = v;
-      const float3 pj = load_pos(pos, v);
-      float* o = vec + 3 * (beg + r);
-      o[0] = __fsub_rn(pj.x, pi.x);
-      o[1] = __fsub_rn(pj.y, pi.y);
-      o[2] = __fsub_rn(pj.z, pi.z);
-      if (dst) dst[beg + r] = i;
+      put_edge<PBC>(beg + r, v, i, pi, pos, src, img, vec, dst, box);
     }
     return;
   }
@@ -334,30 +442,29 @@ __device__ __forceinline__ void sort_row(int i, int lane, int32_t* sm, const flo
     row[r] = v;
   }
   __syncwarp();
-  for (int a = lane; a < k; a += 32) {
-    const float3 pj = load_pos(pos, row[a]);
-    float* o = vec + 3 * (beg + a);
-    o[0] = __fsub_rn(pj.x, pi.x);
-    o[1] = __fsub_rn(pj.y, pi.y);
-    o[2] = __fsub_rn(pj.z, pi.z);
-    if (dst) dst[beg + a] = i;
-  }
+  for (int a = lane; a < k; a += 32) put_edge<PBC>(beg + a, row[a], i, pi, pos, src, img, vec, dst, box);
 }
 
+template <bool PBC>
 __global__ void __launch_bounds__(kSortWarps * 32) k_sort(const float* __restrict__ pos, int N,
                                                           const int32_t* __restrict__ row_offsets,
-                                                          int32_t* __restrict__ src, float* __restrict__ vec,
-                                                          int32_t* __restrict__ dst, long long e_cap) {
+                                                          int32_t* __restrict__ src, int32_t* __restrict__ img,
+                                                          float* __restrict__ vec, int32_t* __restrict__ dst,
+                                                          long long e_cap, const Box box) {
   __shared__ int32_t rows[kSortWarps][kSortCap];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int i = blockIdx.x * kSortWarps + wid;
-  if (i < N) sort_row(i, lane, rows[wid], pos, row_offsets, src, vec, dst, e_cap);
+  if (i < N) sort_row<PBC>(i, lane, rows[wid], pos, row_offsets, src, img, vec, dst, e_cap, box);
 }
 
 // rev[e] for e = (i <- j): the position of (j <- i) in row j (binary search;
 // the relation is symmetric, so it exists).
+// PBC: the reverse of (i <- j, image s) is (j <- i, image -s), i.e. the key
+// i * 27 + (26 - sigma) in row j.
+template <bool PBC>
 __device__ __forceinline__ void rev_row(int i, int lane, const int32_t* __restrict__ row_offsets,
-                                        const int32_t* __restrict__ src, int32_t* __restrict__ rev, long long e_cap) {
+                                        const int32_t* __restrict__ src, const int32_t* __restrict__ img,
+                                        int32_t* __restrict__ rev, long long e_cap) {
   const long long beg = row_offsets[i], end = row_offsets[i + 1];
   if (beg < 0 || end > e_cap || end < beg) return;
   for (long long e = beg + lane; e < end; e += 32) {
@@ -367,20 +474,24 @@ __device__ __forceinline__ void rev_row(int i, int lane, const int32_t* __restri
       rev[e] = -1;
       continue;
     }
+    const long long want = PBC ? (long long)i * kImages + (kImages - 1 - img[e]) : i;
     while (lo < hi) {
       const long long mid = (lo + hi) >> 1;
-      if (src[mid] < i) lo = mid + 1;
+      const long long key = PBC ? (long long)src[mid] * kImages + img[mid] : src[mid];
+      if (key < want) lo = mid + 1;
       else hi = mid;
     }
-    rev[e] = (lo < row_offsets[j + 1] && src[lo] == i) ? (int32_t)lo : -1;
+    const long long got = lo < row_offsets[j + 1] ? (PBC ? (long long)src[lo] * kImages + img[lo] : src[lo]) : -1;
+    rev[e] = got == want ? (int32_t)lo : -1;
   }
 }
 
+template <bool PBC>
 __global__ void k_rev(int N, const int32_t* __restrict__ row_offsets, const int32_t* __restrict__ src,
-                      int32_t* __restrict__ rev, long long e_cap) {
+                      const int32_t* __restrict__ img, int32_t* __restrict__ rev, long long e_cap) {
   const int lane = threadIdx.x & 31;
   const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (i < N) rev_row(i, lane, row_offsets, src, rev, e_cap);
+  if (i < N) rev_row<PBC>(i, lane, row_offsets, src, img, rev, e_cap);
 }
 
 // ------------------------------------------------------------ one launch
@@ -398,10 +509,11 @@ struct CoopArgs {
   int* bad;
   long long* sums;     // [gridDim.x] block totals
   unsigned* bar;       // [2]: arrivals, completed generations (zeroed before the launch)
-  int32_t *row_offsets, *src, *dst, *rev;
+  int32_t *row_offsets, *src, *dst, *rev, *img;
   float* vec;
   long long* e_total;
   int* watchdog;
+  Box box;  // periodic box (k_graph_coop<true>)
 };
 
 // Grid barrier with a bounded wait: false (and the watchdog set) if the
@@ -484,6 +596,7 @@ __device__ bool grid_scan(int32_t* data, long long n, long long* sums, unsigned*
   return grid_sync(bar, gen, watchdog);
 }
 
+template <bool PBC>
 __global__ void __launch_bounds__(kSortWarps * 32) k_graph_coop(const CoopArgs g) {
   __shared__ int32_t rows[kSortWarps][kSortCap];
   unsigned gen = 0;
@@ -494,7 +607,8 @@ __global__ void __launch_bounds__(kSortWarps * 32) k_graph_coop(const CoopArgs g
   for (long long i = tid; i < g.n_clear; i += nthreads) g.start[i] = 0;
   if (tid == 0) *g.bad = 0;
   if (!grid_sync(g.bar, gen, g.watchdog)) return;
-  for (long long i = tid; i < g.N; i += nthreads) bin_one((int)i, g.pos, g.inv, g.mask, g.atom_bucket, g.start, g.bad);
+  for (long long i = tid; i < g.N; i += nthreads)
+    bin_one<PBC>((int)i, g.pos, g.inv, g.mask, g.atom_bucket, g.start, g.bad, g.box);
   if (!grid_sync(g.bar, gen, g.watchdog)) return;
   if (!grid_scan(g.start, g.H + 1, g.sums, g.bar, gen, g.watchdog, g.bad, nullptr)) return;
   for (long long i = tid; i < g.N; i += nthreads)
@@ -502,20 +616,21 @@ __global__ void __launch_bounds__(kSortWarps * 32) k_graph_coop(const CoopArgs g
   if (!grid_sync(g.bar, gen, g.watchdog)) return;
   if (tid == 0) g.row_offsets[g.N] = 0;
   for (long long w = warp0; w < g.N; w += nwarps)
-    neigh_row<false>(w, lane, g.bucket_pos, g.inv, g.rc2, g.mask, g.start, g.bucket_atoms, g.row_offsets, nullptr,
-                     g.e_cap);
+    neigh_row<false, PBC>(w, lane, g.bucket_pos, g.inv, g.rc2, g.mask, g.start, g.bucket_atoms, g.row_offsets,
+                          nullptr, g.e_cap, g.box);
   if (!grid_sync(g.bar, gen, g.watchdog)) return;
   if (!grid_scan(g.row_offsets, (long long)g.N + 1, g.sums, g.bar, gen, g.watchdog, g.bad, g.e_total)) return;
   if (g.e_cap <= 0) return;
   for (long long w = warp0; w < g.N; w += nwarps)
-    neigh_row<true>(w, lane, g.bucket_pos, g.inv, g.rc2, g.mask, g.start, g.bucket_atoms, g.row_offsets, g.src,
-                    g.e_cap);
+    neigh_row<true, PBC>(w, lane, g.bucket_pos, g.inv, g.rc2, g.mask, g.start, g.bucket_atoms, g.row_offsets,
+                         g.src, g.e_cap, g.box);
   if (!grid_sync(g.bar, gen, g.watchdog)) return;
   for (long long i = warp0; i < g.N; i += nwarps)
-    sort_row((int)i, lane, rows[wid], g.pos, g.row_offsets, g.src, g.vec, g.dst, g.e_cap);
+    sort_row<PBC>((int)i, lane, rows[wid], g.pos, g.row_offsets, g.src, g.img, g.vec, g.dst, g.e_cap, g.box);
   if (!g.rev) return;
   if (!grid_sync(g.bar, gen, g.watchdog)) return;
-  for (long long i = warp0; i < g.N; i += nwarps) rev_row((int)i, lane, g.row_offsets, g.src, g.rev, g.e_cap);
+  for (long long i = warp0; i < g.N; i += nwarps)
+    rev_row<PBC>((int)i, lane, g.row_offsets, g.src, g.img, g.rev, g.e_cap);
 }
 
 // ------------------------------------------------------------ workspace
@@ -559,19 +674,19 @@ size_t eqmp_radius_graph_workspace_size(int64_t N) {
   return graph_ws(N).bytes;
 }
 
-eqmp_status eqmp_radius_graph(const float* pos, int64_t N, float cutoff, int32_t* row_offsets, int32_t* src,
-                              float* vec, int32_t* dst, int32_t* rev, int64_t E_cap, int64_t* E_total,
-                              void* workspace, size_t workspace_bytes, eqmp_stream_t stream) {
-  if (N < 0 || E_cap < 0) return EQMP_ERR_INVALID_ARG;
-  if (N > kGraphMaxAtoms) return EQMP_ERR_UNSUPPORTED;
-  if (!(cutoff > 0.0f) || !isfinite(cutoff)) return EQMP_ERR_INVALID_ARG;
-  if (!row_offsets || !E_total) return EQMP_ERR_INVALID_ARG;
-  if (N > 0 && !pos) return EQMP_ERR_INVALID_ARG;
-  if (E_cap > 0 && (!src || !vec)) return EQMP_ERR_INVALID_ARG;
+}  // extern "C"
+
+namespace eqmp {
+namespace {
+
+// Both entry points: argument checks done, box set up when PBC.
+template <bool PBC>
+eqmp_status radius_graph_run(const float* pos, int64_t N, float cutoff, const Box& box, int32_t* row_offsets,
+                             int32_t* src, float* vec, int32_t* img, int32_t* dst, int32_t* rev, int64_t E_cap,
+                             int64_t* E_total, void* workspace, size_t workspace_bytes, cudaStream_t st) {
   const GraphWs w = graph_ws(N);
   if (!workspace || workspace_bytes < w.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255))
     return EQMP_ERR_INVALID_ARG;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   char* base = static_cast<char*>(workspace);
   int32_t* atom_bucket = reinterpret_cast<int32_t*>(base + w.atom_bucket);
   int32_t* start = reinterpret_cast<int32_t*>(base + w.start);
@@ -599,7 +714,7 @@ eqmp_status eqmp_radius_graph(const float* pos, int64_t N, float cutoff, int32_t
     if (occ == 0) {
       int coop = 0;
       if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, d) != cudaSuccess) return EQMP_ERR_CUDA;
-      if (!coop || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_graph_coop, kSortWarps * 32, 0) !=
+      if (!coop || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_graph_coop<PBC>, kSortWarps * 32, 0) !=
                        cudaSuccess || occ < 1)
         occ = -1;  // multi-kernel path only
       __atomic_store_n(&occ_cache[d & 63], occ, __ATOMIC_RELAXED);
@@ -619,12 +734,13 @@ eqmp_status eqmp_radius_graph(const float* pos, int64_t N, float cutoff, int32_t
       g.bucket_pos = bucket_pos; g.bad = bad;
       g.sums = reinterpret_cast<long long*>(base + w.coop);
       g.bar = reinterpret_cast<unsigned*>(base + w.coop + 8 * (size_t)kCoopMaxBlocks);
-      g.row_offsets = row_offsets; g.src = src; g.dst = dst; g.rev = rev; g.vec = vec;
+      g.row_offsets = row_offsets; g.src = src; g.dst = dst; g.rev = rev; g.img = img; g.vec = vec;
       g.e_total = reinterpret_cast<long long*>(E_total);
       g.watchdog = dev.watchdog;
+      g.box = box;
       if (cudaMemsetAsync(g.bar, 0, 2 * sizeof(unsigned), st) != cudaSuccess) return EQMP_ERR_CUDA;
       void* params[] = {&g};
-      const cudaError_t err = cudaLaunchCooperativeKernel((const void*)k_graph_coop, dim3((unsigned)grid),
+      const cudaError_t err = cudaLaunchCooperativeKernel((const void*)k_graph_coop<PBC>, dim3((unsigned)grid),
                                                           dim3(kSortWarps * 32), params, 0, st);
       if (err == cudaSuccess) return EQMP_OK;
       (void)cudaGetLastError();  // fall through to the multi-kernel path
@@ -633,25 +749,75 @@ eqmp_status eqmp_radius_graph(const float* pos, int64_t N, float cutoff, int32_t
 
   k_clear<<<256, 256, 0, st>>>(start, n_clear, bad);
   if (N > 0) {
-    k_bin<<<nblk, kNeighThreads, 0, st>>>(pos, (int)N, inv, mask, atom_bucket, start, bad);
+    k_bin<PBC><<<nblk, kNeighThreads, 0, st>>>(pos, (int)N, inv, mask, atom_bucket, start, bad, box);
   }
   cudaError_t err = exclusive_scan(start, w.H + 1, sums, bad, nullptr, st);
   if (err != cudaSuccess) return EQMP_ERR_CUDA;
   if (N > 0)
     k_scatter<<<nblk, kNeighThreads, 0, st>>>(pos, (int)N, atom_bucket, start, fill, bucket_atoms, bucket_pos);
   const long long wblk = (N * 32 + kNeighThreads - 1) / kNeighThreads;  // one warp per receiver
-  k_neigh<false><<<(unsigned)(wblk > 0 ? wblk : 1), kNeighThreads, 0, st>>>(bucket_pos, (int)N, inv, rc2, mask, start,
-                                                                           bucket_atoms, row_offsets, nullptr, E_cap);
+  k_neigh<false, PBC><<<(unsigned)(wblk > 0 ? wblk : 1), kNeighThreads, 0, st>>>(
+      bucket_pos, (int)N, inv, rc2, mask, start, bucket_atoms, row_offsets, nullptr, E_cap, box);
   err = exclusive_scan(row_offsets, N + 1, sums, bad, reinterpret_cast<long long*>(E_total), st);
   if (err != cudaSuccess) return EQMP_ERR_CUDA;
   if (N > 0 && E_cap > 0) {
-    k_neigh<true><<<(unsigned)wblk, kNeighThreads, 0, st>>>(bucket_pos, (int)N, inv, rc2, mask, start, bucket_atoms,
-                                                            row_offsets, src, E_cap);
+    k_neigh<true, PBC><<<(unsigned)wblk, kNeighThreads, 0, st>>>(bucket_pos, (int)N, inv, rc2, mask, start,
+                                                                 bucket_atoms, row_offsets, src, E_cap, box);
     const int sblk = (int)((N + kSortWarps - 1) / kSortWarps);
-    k_sort<<<sblk, kSortWarps * 32, 0, st>>>(pos, (int)N, row_offsets, src, vec, dst, E_cap);
-    if (rev) k_rev<<<sblk, kSortWarps * 32, 0, st>>>((int)N, row_offsets, src, rev, E_cap);
+    k_sort<PBC><<<sblk, kSortWarps * 32, 0, st>>>(pos, (int)N, row_offsets, src, img, vec, dst, E_cap, box);
+    if (rev) k_rev<PBC><<<sblk, kSortWarps * 32, 0, st>>>((int)N, row_offsets, src, img, rev, E_cap);
   }
   return cuda_status(cudaGetLastError());
+}
+
+eqmp_status graph_args_ok(const float* pos, int64_t N, float cutoff, const int32_t* row_offsets, const int32_t* src,
+                          const float* vec, int64_t E_cap, const int64_t* E_total, int64_t n_max) {
+  if (N < 0 || E_cap < 0) return EQMP_ERR_INVALID_ARG;
+  if (N > n_max) return EQMP_ERR_UNSUPPORTED;
+  if (!(cutoff > 0.0f) || !isfinite(cutoff)) return EQMP_ERR_INVALID_ARG;
+  if (!row_offsets || !E_total) return EQMP_ERR_INVALID_ARG;
+  if (N > 0 && !pos) return EQMP_ERR_INVALID_ARG;
+  if (E_cap > 0 && (!src || !vec)) return EQMP_ERR_INVALID_ARG;
+  return EQMP_OK;
+}
+
+}  // namespace
+}  // namespace eqmp
+
+extern "C" {
+
+eqmp_status eqmp_radius_graph(const float* pos, int64_t N, float cutoff, int32_t* row_offsets, int32_t* src,
+                              float* vec, int32_t* dst, int32_t* rev, int64_t E_cap, int64_t* E_total,
+                              void* workspace, size_t workspace_bytes, eqmp_stream_t stream) {
+  const eqmp_status s = graph_args_ok(pos, N, cutoff, row_offsets, src, vec, E_cap, E_total, kGraphMaxAtoms);
+  if (s != EQMP_OK) return s;
+  return radius_graph_run<false>(pos, N, cutoff, Box{}, row_offsets, src, vec, nullptr, dst, rev, E_cap, E_total,
+                                 workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+eqmp_status eqmp_radius_graph_pbc(const float* pos, int64_t N, float cutoff, const float* box_lengths,
+                                  int32_t* row_offsets, int32_t* src, float* vec, int32_t* img, int32_t* dst,
+                                  int32_t* rev, int64_t E_cap, int64_t* E_total, void* workspace,
+                                  size_t workspace_bytes, eqmp_stream_t stream) {
+  const eqmp_status s = graph_args_ok(pos, N, cutoff, row_offsets, src, vec, E_cap, E_total, kGraphMaxAtomsPbc);
+  if (s != EQMP_OK) return s;
+  if (!box_lengths || (E_cap > 0 && !img)) return EQMP_ERR_INVALID_ARG;
+  Box box{};
+  for (int a = 0; a < 3; ++a) {
+    const float L = box_lengths[a];
+    if (!(L > 0.0f) || !isfinite(L)) return EQMP_ERR_INVALID_ARG;
+    if (cutoff > L) return EQMP_ERR_UNSUPPORTED;  // more than one image per direction
+    box.L[a] = L;
+    // cells of side >= r_c (1 + 2^-10) tile the axis; fewer than three
+    // become one cell whose images are walked; at most kCellRange per axis
+    // (the cell index of a coordinate is then exact to well within the margin)
+    double n = floor((double)L / ((double)cutoff * (1.0 + 1.0 / 1024.0)));
+    if (n > (double)kCellRange) n = (double)kCellRange;
+    box.n[a] = n < 3.0 ? 1 : (int)n;
+    box.inv[a] = (float)((double)box.n[a] / (double)L);
+  }
+  return radius_graph_run<true>(pos, N, cutoff, box, row_offsets, src, vec, img, dst, rev, E_cap, E_total,
+                                workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -281,6 +281,41 @@ eqmp_status eqmp_radius_graph(const float* pos, int64_t N, float cutoff, int32_t
                               eqmp_stream_t stream);
 
 /*
+ * Radius graph with periodic boundaries.  E2Former-V2 (section 4.2) treats
+ * periodic systems by expanding the cells, one image per direction.  The box
+ * is orthorhombic with sides box_lengths[0..2] (host memory, > 0, finite,
+ * else EQMP_ERR_INVALID_ARG), the atoms lie inside it, and the cutoff is at
+ * most the smallest side (EQMP_ERR_UNSUPPORTED otherwise), so that one image
+ * per direction holds every neighbour.
+ *
+ * Edges: (sender j, image s) -> receiver i for every s in {-1, 0, 1}^3 and
+ * every j with d2 < cutoff*cutoff, except j = i with s = 0, where, in
+ * float32 with each operation rounded on its own,
+ * d_a = (pos[j][a] - pos[i][a]) + s_a * box_lengths[a] (s_a * L_a is exact)
+ * and d2 = (d_x*d_x + d_y*d_y) + d_z*d_z.  A sender may appear in a row
+ * several times, once per image in reach (cutoff > L/2).  With s = 0 the
+ * arithmetic is that of eqmp_radius_graph, bit for bit.
+ *
+ *   pos          [N][3] fp32, device; 0 <= pos[i][a] < box_lengths[a], else
+ *                *E_total = -1 and the other outputs are unspecified.
+ *   img          [E_cap] int32, device, written (required when E_cap > 0):
+ *                image index sigma = (s_x+1) + 3 (s_y+1) + 9 (s_z+1) of
+ *                each edge (13 is s = 0).  Rows are sorted by sender, then
+ *                sigma.
+ *   vec          [E_cap][3] fp32, device, written: d above.
+ *   rev          [E_cap] int32 or NULL: index of the reverse edge, which is
+ *                (receiver <- sender) with the opposite image, 26 - sigma.
+ *   other arguments, E_total, the capacity protocol and the workspace
+ *                (eqmp_radius_graph_workspace_size(N) bytes): as
+ *                eqmp_radius_graph.
+ * N up to 2^26 (EQMP_ERR_UNSUPPORTED above).  Asynchronous on `stream`.
+ */
+eqmp_status eqmp_radius_graph_pbc(const float* pos, int64_t N, float cutoff, const float* box_lengths,
+                                  int32_t* row_offsets, int32_t* src, float* vec, int32_t* img,
+                                  int32_t* dst, int32_t* rev, int64_t E_cap, int64_t* E_total,
+                                  void* workspace, size_t workspace_bytes, eqmp_stream_t stream);
+
+/*
  * Synchronous check of the graph preconditions on device data:
  * 0 <= row_offsets[0] <= ... <= row_offsets[N] <= E and
  * 0 <= src[e] < N_src for every e in [row_offsets[0], row_offsets[N]).

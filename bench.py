@@ -437,13 +437,17 @@ def main():
     ap.add_argument("--pass", dest="which", default="forward", choices=["forward", "backward", "graph"],
                     help="backward: time eqmp_fused_backward (dx, dw or dR/dM, dvec) instead; "
                          "graph: time eqmp_radius_graph on the workload's atom positions")
+    ap.add_argument("--pbc", action="store_true",
+                    help="with --pass graph: periodic boundaries (eqmp_radius_graph_pbc) in the generator's cube")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
-    from equivariant_gnn_message_gb300.inputs import make_workload
+    from equivariant_gnn_message_gb300.inputs import DENSITY, make_workload
     from equivariant_gnn_message_gb300.sharding import max_over_ranks
 
     wl = make_workload(args.workload, l_max=args.lmax)
+    if args.pbc and args.which != "graph":
+        raise SystemExit("--pbc goes with --pass graph")
     if args.lmax != 3 and (args.which != "forward" or wl.storage != "f32"):
         raise SystemExit("--lmax: forward pass on fp32 workloads only")
     if args.impl == "reference":
@@ -507,15 +511,29 @@ def main():
 
         lib = eq.load_library()
         N = wl.n_atoms
-        g_pos = t(wl.pos)
+        box = None
+        pos_np = wl.pos
+        if args.pbc:  # the generator's cube as a periodic box; positions strictly inside it
+            side = float((N / DENSITY) ** (1.0 / 3.0))
+            box = (side, side, side)
+            pos_np = np.minimum(np.maximum(wl.pos, np.float32(0)), np.nextafter(np.float32(side), np.float32(0)))
+        g_pos = t(pos_np)
         g_ws = torch.empty(lib.eqmp_radius_graph_workspace_size(N), dtype=torch.uint8, device=dev)
         g_E = torch.empty(1, dtype=torch.int64, device=dev)
-        g_out, E_graph = eq.eqmp_radius_graph(g_pos, wl.cutoff)
+        g_out, E_graph = eq.eqmp_radius_graph(g_pos, wl.cutoff, box=box)
         g_off, g_src, g_vec = g_out["off"], g_out["src"], g_out["vec"]
-        graph_args = (g_pos.data_ptr(), N, ctypes.c_float(wl.cutoff), g_off.data_ptr(), g_src.data_ptr(),
-                      g_vec.data_ptr(), None, None, E_graph, g_E.data_ptr(), g_ws.data_ptr(), g_ws.numel(),
-                      stream.cuda_stream)
-        step = lambda: lib.eqmp_radius_graph(*graph_args)
+        if box is None:
+            graph_args = (g_pos.data_ptr(), N, ctypes.c_float(wl.cutoff), g_off.data_ptr(), g_src.data_ptr(),
+                          g_vec.data_ptr(), None, None, E_graph, g_E.data_ptr(), g_ws.data_ptr(), g_ws.numel(),
+                          stream.cuda_stream)
+            step = lambda: lib.eqmp_radius_graph(*graph_args)
+        else:
+            g_img = g_out["img"]
+            lengths = (ctypes.c_float * 3)(*box)
+            graph_args = (g_pos.data_ptr(), N, ctypes.c_float(wl.cutoff), lengths, g_off.data_ptr(),
+                          g_src.data_ptr(), g_vec.data_ptr(), g_img.data_ptr(), None, None, E_graph, g_E.data_ptr(),
+                          g_ws.data_ptr(), g_ws.numel(), stream.cuda_stream)
+            step = lambda: lib.eqmp_radius_graph_pbc(*graph_args)
         coop = N <= 16384  # the library's single cooperative launch covers up to 16,384 atoms
         launches_per_step = 1 if coop else 12
         n_edges = E_graph
@@ -578,15 +596,16 @@ def main():
             layer_e2e()
             h_out.copy_(out, non_blocking=True)
     elif args.which == "graph":
-        h_pos = torch.from_numpy(np.ascontiguousarray(wl.pos)).pin_memory()
-        h_outs = [torch.empty(a.shape, dtype=a.dtype).pin_memory() for a in (g_off, g_src, g_vec)]
+        h_pos = torch.from_numpy(np.ascontiguousarray(pos_np)).pin_memory()
+        g_res = (g_off, g_src, g_vec) + ((g_img,) if box is not None else ())
+        h_outs = [torch.empty(a.shape, dtype=a.dtype).pin_memory() for a in g_res]
         h2d = h_pos.numel() * 4
         d2h = sum(a.numel() * a.element_size() for a in h_outs)
 
         def e2e_step():
             g_pos.copy_(h_pos, non_blocking=True)
-            lib.eqmp_radius_graph(*graph_args)
-            for h, dd in zip(h_outs, (g_off, g_src, g_vec)):
+            step()
+            for h, dd in zip(h_outs, g_res):
                 h.copy_(dd, non_blocking=True)
     if args.which != "backward":
         for _ in range(3):
@@ -679,10 +698,10 @@ def main():
 
     version = kernel_version(wl, args.which, args.lmax, args.entry)
     if args.which == "graph":
-        # positions in; offsets, senders and edge vectors out
-        gbytes = 12 * wl.n_atoms + 4 * (wl.n_atoms + 1) + 16 * E_graph
+        # positions in; offsets, senders and edge vectors (and image indices) out
+        gbytes = 12 * wl.n_atoms + 4 * (wl.n_atoms + 1) + (20 if box is not None else 16) * E_graph
         label = ("radius-graph cooperative single launch" if coop else
-                 "radius-graph multi-kernel (12 launches)")
+                 "radius-graph multi-kernel (12 launches)") + (", periodic" if box is not None else "")
         roof = roofline(0.0, gbytes, ms, fp32_peak, hbm_peak, label, None,
                         "compulsory bytes: positions, offsets, senders, edge vectors")
         roof["algorithmic_bytes"] = gbytes
@@ -710,7 +729,10 @@ def main():
 
         pool.terminate()
         tg = time.perf_counter()
-        E_cpu = len(oracle_graph.radius_graph(wl.pos, wl.cutoff)["src"])
+        if box is None:
+            E_cpu = len(oracle_graph.radius_graph(wl.pos, wl.cutoff)["src"])
+        else:
+            E_cpu = len(oracle_graph.radius_graph_pbc(pos_np, wl.cutoff, box)["src"])
         wall = time.perf_counter() - tg
         cpu = {"value": E_cpu / wall, "unit": "edges/s", "cores": 1, "kind": "oracle",
                "sample": f"whole workload ({wl.n_atoms} atoms, {E_cpu} edges), k-d tree candidates + float32 test, {wall:.2f} s"}
@@ -727,7 +749,8 @@ def main():
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32" if wl.storage == "f32" else "bf16-storage/f32-compute", "data": "synthetic",
-        "config": workload_config(args.workload, wl, args.entry, world),
+        "config": dict(workload_config(args.workload, wl, args.entry, world),
+                       **({"boundaries": "periodic"} if args.which == "graph" and args.pbc else {})),
         "roofline": roof,
         "e2e": None if e2e_ms is None else {
             "value": n_edges * world / (e2e_ms * 1e-3), "unit": "edges/s",

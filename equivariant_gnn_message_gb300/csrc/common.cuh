@@ -104,6 +104,21 @@ __device__ __forceinline__ int4 balanced_range_off(const int* __restrict__ off, 
   return make_int4(hi[0], up ? hi[1] : hi[0], ohi[0], up ? ohi[1] : ohi[0]);
 }
 
+// The CTA's range searched by warp 0 alone and written to `slot` (shared
+// memory, 16 bytes); the other warps read it after the caller's next
+// __syncthreads.  Every CTA's first-round probes hit the same few lines of
+// the offsets; one warp per CTA instead of every warp sends fewer of those
+// requests (the aligned-frame kernel: 41.0 -> 38.9 us on the 1000-atom
+// radial workload; the shared-weight kernel measured slower with it and
+// keeps the per-warp search).
+__device__ __forceinline__ void balanced_range_publish(int4* slot, const int* __restrict__ off, int N, int G, int b,
+                                                       int alpha) {
+  if (threadIdx.x < 32) {
+    const int4 r = balanced_range_off(off, N, G, b, alpha);
+    if (threadIdx.x == 0) *slot = r;
+  }
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

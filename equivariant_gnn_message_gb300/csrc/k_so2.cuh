@@ -164,7 +164,8 @@ struct So2Cfg {
   static constexpr int OFF_RED = OFF_E + YR * kEntryFloats * 4;         // [2][EG][16][C]
   static constexpr int OFF_M = OFF_RED + 2 * EG * 16 * C * 4;          // radial: [8][17][C] float2
   static constexpr int OFF_BAR = OFF_M + M_BYTES;
-  static constexpr int SMEM_BYTES = OFF_BAR + 2 * S * 8 + 1024;
+  static constexpr int OFF_RANGE = OFF_BAR + 2 * S * 8;  // the CTA's range (int4)
+  static constexpr int SMEM_BYTES = OFF_RANGE + 16 + 1024;
 };
 
 // One padded D row (m) of level L from the edge entry into registers.
@@ -268,25 +269,16 @@ __global__ void __launch_bounds__(So2Cfg<C, XT, RADIAL>::NTHREADS, So2Cfg<C, XT,
   const int tid = threadIdx.x;
   // Contiguous receiver range, balanced on edges (a receiver's group sum and
   // store cost about one edge here).
-  const int4 rr = balanced_range_off(a.off, a.N, gridDim.x, blockIdx.x, 1);
-  const int r_begin = rr.x, r_end = rr.y;
+  int4* range_s = reinterpret_cast<int4*>(smem + K::OFF_RANGE);
+  balanced_range_publish(range_s, a.off, a.N, gridDim.x, blockIdx.x, 1);
   if (tid < S) {
     mbar_init(full0 + 8 * tid, 1);
     mbar_init(empty0 + 8 * tid, C);  // the C threads of the owning edge group
     fence_mbar_init();
   }
-  if constexpr (RADIAL) {
-    // M[k][p*C + c] -> Ms[(k*17 + p/2)*C + c] = (M[k][p][c], M[k][p+1][c])
-    for (int i = tid; i < 8 * 17 * C; i += K::NTHREADS) {
-      const int k = i / (17 * C), pp = (i / C) % 17, c = i % C;
-      Ms[i] = make_float2(__ldg(a.M + (size_t)k * 34 * C + (2 * pp) * C + c),
-                          __ldg(a.M + (size_t)k * 34 * C + (2 * pp + 1) * C + c));
-    }
-  } else {
-    float* ws = reinterpret_cast<float*>(Ms);
-    for (int i = tid; i < 34 * C; i += K::NTHREADS) ws[i] = __ldg(a.w + i);
-  }
   __syncthreads();
+  const int4 rr = *range_s;
+  const int r_begin = rr.x, r_end = rr.y;
   const int e_begin = min(max(rr.z, 0), a.E);
   const int e_end = max(e_begin, min(max(rr.w, 0), a.E));
   const int total = e_end - e_begin;
@@ -345,6 +337,49 @@ __global__ void __launch_bounds__(So2Cfg<C, XT, RADIAL>::NTHREADS, So2Cfg<C, XT,
   }
 
   // -------------------------------------------------------------- consumers
+  // The radial mixing matrix (or the shared weights) to shared memory, by
+  // the consumers while the producer builds the first edges; loads in
+  // batches of 8 per thread, each batch issued before its stores.
+  if constexpr (RADIAL) {
+    // M[k][p*C + c] -> Ms[(k*17 + p/2)*C + c] = (M[k][p][c], M[k][p+1][c])
+    if ((reinterpret_cast<uintptr_t>(a.M) & 15) == 0) {
+      constexpr int Q4 = 8 * 17 * C / 4;  // (k, path pair, 4 channels)
+      for (int base = 0; base < Q4; base += 8 * K::NCONS) {
+        float4 va[8], vb[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = base + tid + u * K::NCONS;
+          if (i < Q4) {
+            const int c4 = i % (C / 4), pp = (i / (C / 4)) % 17, k = i / (17 * (C / 4));
+            const float* row = a.M + (size_t)k * 34 * C + (size_t)(2 * pp) * C + 4 * c4;
+            va[u] = __ldg(reinterpret_cast<const float4*>(row));
+            vb[u] = __ldg(reinterpret_cast<const float4*>(row + C));
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = base + tid + u * K::NCONS;
+          if (i < Q4) {
+            const int c4 = i % (C / 4), pp = (i / (C / 4)) % 17, k = i / (17 * (C / 4));
+            float4* d = reinterpret_cast<float4*>(Ms + (k * 17 + pp) * C + 4 * c4);
+            d[0] = make_float4(va[u].x, vb[u].x, va[u].y, vb[u].y);
+            d[1] = make_float4(va[u].z, vb[u].z, va[u].w, vb[u].w);
+          }
+        }
+      }
+    } else {
+      for (int i = tid; i < 8 * 17 * C; i += K::NCONS) {
+        const int k = i / (17 * C), pp = (i / C) % 17, c = i % C;
+        Ms[i] = make_float2(__ldg(a.M + (size_t)k * 34 * C + (2 * pp) * C + c),
+                            __ldg(a.M + (size_t)k * 34 * C + (2 * pp + 1) * C + c));
+      }
+    }
+  } else {
+    float* ws = reinterpret_cast<float*>(Ms);
+    for (int i = tid; i < 34 * C; i += K::NCONS) ws[i] = __ldg(a.w + i);
+  }
+  named_barrier(2, K::NCONS);  // M (or w) visible to every consumer
+
   const int c = tid % C, g = tid / C;
   const uint32_t xlog = (uint32_t)(c * 16 * (int)sizeof(XT));
   const uint32_t xo[2] = {swz128(xlog), swz128(xlog + 16)};

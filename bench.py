@@ -23,7 +23,8 @@ Prints ONE JSON line (rank 0):
                higher of the derived one (SM count x 128 lanes x 2 flops x
                max SM clock) and the measured one (eqmp_fp32_peak_probe);
   workloads    the same measurement (time, roofline, clocks) for the
-               100k-atom, the dense bf16 and the radial-weight workloads;
+               100k-atom, the dense bf16 and the radial-weight workloads,
+               and the 100k-atom workload renumbered in Morton order;
   cpu_baseline the CPU oracle (numpy, fp64) on a bounded sample of the same
                workload on this host's cores, plus one-thread runs of the
                tiny, pages and radial workloads.
@@ -49,7 +50,7 @@ METRIC_GRAPH = "edges/s radius graph (CSR by receiver, edge vectors)"
 FLUSH_BYTES = 256 << 20
 HEADLINE = "pages_1k_c32"
 # Measured beside the headline in the default run (the other full-size configurations).
-EXTRA_WORKLOADS = ("scale_100k_c64", "dense_10k_c128_bf16", "radial_1k_c32")
+EXTRA_WORKLOADS = ("scale_100k_c64", "dense_10k_c128_bf16", "radial_1k_c32", "scale_100k_c64_morton")
 # One-thread oracle runs (the small configurations).
 SINGLE_THREAD_WORKLOADS = ("tiny_64", "pages_1k_c32", "radial_1k_c32")
 GROUP = 32  # timed steps queued behind one GPU spin
@@ -64,6 +65,7 @@ NCU_TRAFFIC = {
     ("dense_10k_c128_bf16", "k_shared-pairs-v5"): 48796160 + 11876864,
     ("radial_1k_c32", "k_so2-v4"): 2888704 + 0,
     ("radial_1k_c32", "k_so2-v5"): 2899456 + 0,
+    ("scale_100k_c64_morton", "k_shared-pairs-v5"): 1679304960 + 394390272,
 }
 
 # aligned-frame terms per degree (one per output order and path with m2 = 0)

@@ -22,6 +22,12 @@ Recipe (one generator for every workload):
 The workloads mirror the sizes on the Batmobile blog (1000 atoms, 32
 channels, about 20 neighbours, cutoff 4-6 A, 1000-5000 atoms per batch)
 and E2Former-V2's dense regime (k about 30-100 neighbours, N ~ 1e4).
+
+Atom order: draw order (spatially random, the hardest case for the row
+gather), or, with order="morton", the same atoms and features renumbered
+along the Morton (Z-order) curve of their cutoff-sized cells, the order a
+cell-list neighbour builder leaves atoms in.  Renumbering is a permutation
+of the input, applied before the graph is built.
 """
 from dataclasses import dataclass
 from typing import Optional
@@ -39,6 +45,9 @@ WORKLOADS = {
     "radial_1k_c32":  dict(n_atoms=1000, cutoff=5.0, channels=32, weights="radial", storage="f32", seed=3),
     "scale_100k_c64": dict(n_atoms=100_000, cutoff=5.0, channels=64, weights="shared", storage="f32", seed=4),
     "dense_10k_c128_bf16": dict(n_atoms=10_000, cutoff=7.0, channels=128, weights="shared", storage="bf16", seed=5),
+    # the scale workload's atoms and features, renumbered in Morton order of their cells
+    "scale_100k_c64_morton": dict(n_atoms=100_000, cutoff=5.0, channels=64, weights="shared", storage="f32", seed=4,
+                                  order="morton"),
 }
 
 
@@ -101,6 +110,23 @@ def radial_basis(d: np.ndarray, n_basis: int = 8, r_max: float = 5.0, sigma: flo
     return (g * env[:, None]).astype(np.float32)
 
 
+def morton_order(pos: np.ndarray, cell: float) -> np.ndarray:
+    """Permutation sorting atoms along the Morton curve of their cells
+    (cell coordinates floor(p / cell), 21 bits per axis interleaved)."""
+    c = np.floor(np.asarray(pos, np.float64) / cell).astype(np.int64)
+    c -= c.min(axis=0) if len(c) else 0
+
+    def spread(v):
+        v = v.astype(np.uint64) & np.uint64(0x1FFFFF)
+        out = np.zeros_like(v)
+        for b in range(21):
+            out |= ((v >> np.uint64(b)) & np.uint64(1)) << np.uint64(3 * b)
+        return out
+
+    key = spread(c[:, 0]) | (spread(c[:, 1]) << np.uint64(1)) | (spread(c[:, 2]) << np.uint64(2))
+    return np.argsort(key, kind="stable")
+
+
 def n_paths(l_max: int) -> int:
     """Number of (l1, l2, l3) with |l1-l2| <= l3 <= l1+l2, all <= l_max."""
     return sum(min(l_max, a + b) - abs(a - b) + 1 for a in range(l_max + 1) for b in range(l_max + 1))
@@ -129,6 +155,9 @@ def make_workload(name: str = None, *, n_atoms=None, cutoff=None, channels=None,
         w = (rng.standard_normal((P, C)) / np.sqrt(P)).astype(np.float32)
     else:
         M = (rng.standard_normal((8, P * C)) / np.sqrt(8.0)).astype(np.float32)
+    if spec.get("order", "draw") == "morton":
+        perm = morton_order(pos, float(spec["cutoff"]))
+        pos, x = pos[perm], x[perm]
     src, dst = radius_graph(pos, float(spec["cutoff"]))
     vec = (pos[src] - pos[dst]).astype(np.float32)
     if spec["weights"] != "shared":

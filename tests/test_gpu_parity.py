@@ -84,7 +84,7 @@ def test_workload_full_parity(eq, name, entry):
     _check_full(eq, make_workload(name), entry)
 
 
-@pytest.mark.parametrize("name", ["scale_100k_c64", "dense_10k_c128_bf16"])
+@pytest.mark.parametrize("name", ["scale_100k_c64", "dense_10k_c128_bf16", "scale_100k_c64_morton"])
 def test_workload_full_size_every_receiver(eq, name):
     """The two largest workloads in the launch configuration the benchmark
     times, compared element by element on every receiver (100,000 and

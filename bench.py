@@ -14,7 +14,8 @@ Prints ONE JSON line (rank 0):
                host queues each group of steps behind a short GPU spin, so
                host-side enqueue jitter never shows up as device time);
   e2e          the same metric through the public API with pinned host
-               buffers: H2D of the step's inputs, the layer, D2H of out;
+               buffers: H2D of the step's inputs, the layer, D2H of out
+               (for eqmp_fused: one eqmp_fused_staged call per step);
   roofline     t_roof = max(FMA count / FP32 peak, compulsory bytes / HBM
                peak); frac = t_roof / measured time, bound = the larger
                term.  FMA count of the lowest-FMA exact schedule (shared
@@ -593,12 +594,24 @@ def main():
         h2d = sum(np.ascontiguousarray(a).nbytes for a in parts.values())
         d2h = h_out.numel() * h_out.element_size()
         layer_e2e = layer_step(eq, args.entry, args.lmax, d_in, out, Yb)
+        if args.entry == "fused" and args.lmax == 3:
+            # one C-ABI call per step: the packed inputs' host-to-device
+            # copy, the layer, the result's device-to-host copy
+            e2e_api = "eqmp_fused_staged"
 
-        def e2e_step():
-            d_pack.copy_(h_pack, non_blocking=True)
-            layer_e2e()
-            h_out.copy_(out, non_blocking=True)
+            def e2e_step():
+                eq.eqmp_fused_staged(h_pack, d_pack, d_in["vec"], d_in["x"], d_in["off"], d_in["src"], out, h_out,
+                                     w=d_in["w"], R=d_in["R"], M=d_in["M"])
+        else:
+            e2e_api = "torch copies + " + {"so2": "eqmp_fused_so2", "tp_scatter": "eqmp_sh + eqmp_tp_scatter"}.get(
+                args.entry, "eqmp_fused_lmax")
+
+            def e2e_step():
+                d_pack.copy_(h_pack, non_blocking=True)
+                layer_e2e()
+                h_out.copy_(out, non_blocking=True)
     elif args.which == "graph":
+        e2e_api = "torch copies + eqmp_radius_graph" + ("_pbc" if box is not None else "")
         h_pos = torch.from_numpy(np.ascontiguousarray(pos_np)).pin_memory()
         g_res = (g_off, g_src, g_vec) + ((g_img,) if box is not None else ())
         h_outs = [torch.empty(a.shape, dtype=a.dtype).pin_memory() for a in g_res]
@@ -757,7 +770,7 @@ def main():
         "roofline": roof,
         "e2e": None if e2e_ms is None else {
             "value": n_edges * world / (e2e_ms * 1e-3), "unit": "edges/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "api": e2e_api},
         "pass": args.which,
         "l_max": args.lmax,
         "graph_edges": None if args.which != "graph" else E_graph,

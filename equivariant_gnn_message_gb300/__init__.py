@@ -11,6 +11,7 @@ Entry points (same names as the C ABI):
   eqmp_sh(vec, Y=None)                         -> Y [E, 16]
   eqmp_tp_scatter(Y, x, row_offsets, src, ...)  -> out [N, C, 16]
   eqmp_fused(vec, x, row_offsets, src, ...)     -> out [N, C, 16]
+  eqmp_fused_staged(h_in, d_in, ..., out, h_out) -> h_out: copy in, layer, copy out
   eqmp_fused_so2(...)                           -> out, aligned-frame schedule
   eqmp_validate_graph(row_offsets, src, n_src, n_edges)
   eqmp_device_error()                           -> int (watchdog code)
@@ -26,7 +27,8 @@ import os
 
 __all__ = [
     "EqmpError", "load_library", "library_path", "eqmp_num_paths", "eqmp_path_table",
-    "eqmp_status_string", "eqmp_sh", "eqmp_tp_scatter", "eqmp_fused", "eqmp_fused_so2", "eqmp_validate_graph",
+    "eqmp_status_string", "eqmp_sh", "eqmp_tp_scatter", "eqmp_fused", "eqmp_fused_staged", "eqmp_fused_so2",
+    "eqmp_validate_graph",
     "eqmp_device_error", "eqmp_fused_backward", "eqmp_fused_backward_noalloc", "eqmp_radius_graph", "eqmp_fused_lmax",
     "eqmp_num_paths_lmax", "eqmp_watchdog_selftest", "eqmp_fp32_peak_probe", "sender_view", "EQMP_OK", "EQMP_ERR_INVALID_ARG", "EQMP_ERR_UNSUPPORTED",
     "EQMP_ERR_CUDA", "EQMP_ERR_DEVICE_TIMEOUT", "EQMP_ERR_GRAPH",
@@ -80,6 +82,9 @@ def load_library():
     lib.eqmp_fused.restype = i32
     lib.eqmp_fused_so2.argtypes = layer
     lib.eqmp_fused_so2.restype = i32
+    sz = ctypes.c_size_t
+    lib.eqmp_fused_staged.argtypes = [vp, vp, sz] + layer[:-1] + [vp, sz, vp]
+    lib.eqmp_fused_staged.restype = i32
     lib.eqmp_validate_graph.argtypes = [vp, vp, i64, i64, i64, vp]
     lib.eqmp_validate_graph.restype = i32
     lib.eqmp_device_error.argtypes = [ctypes.POINTER(i32)]
@@ -231,6 +236,49 @@ def eqmp_fused(vec, x, row_offsets, src, w=None, R=None, M=None, out=None, strea
 
     _require(vec, "vec", torch.float32)
     return _layer("eqmp_fused", vec, x, row_offsets, src, w, R, M, out, stream, n_edges)
+
+
+def eqmp_fused_staged(h_in, d_in, vec, x, row_offsets, src, out, h_out, w=None, R=None, M=None, stream=None,
+                      n_edges=None):
+    """One step from host memory: h_in (pinned CPU uint8) -> d_in (CUDA
+    uint8, same size), eqmp_fused on the CUDA tensors given (views into
+    d_in), out -> h_out (pinned CPU, out's size).  Asynchronous on the
+    stream; synchronise before reading h_out."""
+    import torch
+
+    _require(h_in, "h_in", torch.uint8, cuda=False)
+    _require(d_in, "d_in", torch.uint8)
+    _require(h_out, "h_out", out.dtype, cuda=False)
+    _require(vec, "vec", torch.float32)
+    _require(x, "x", (torch.float32, torch.bfloat16))
+    _require(row_offsets, "row_offsets", torch.int32)
+    _require(src, "src", torch.int32)
+    for name, t in (("w", w), ("R", R), ("M", M)):
+        _require(t, name, torch.float32)
+    if h_in.is_cuda or h_out.is_cuda:
+        raise ValueError("h_in and h_out are host tensors")
+    if h_in.numel() != d_in.numel():
+        raise ValueError("h_in and d_in must have the same size")
+    if x.dim() != 3 or x.shape[2] != 16:
+        raise ValueError("x must be [N_src, C, 16]")
+    n_src, C = x.shape[0], x.shape[1]
+    N = row_offsets.shape[0] - 1
+    E = n_edges if n_edges is not None else vec.shape[0]
+    _require(out, "out", x.dtype)
+    if tuple(out.shape) != (N, C, 16) or tuple(h_out.shape) != (N, C, 16):
+        raise ValueError("out and h_out must be [N, C, 16]")
+    dt = EQMP_BF16 if x.dtype == torch.bfloat16 else EQMP_F32
+    if w is not None:
+        wt = Weights(ctypes.c_void_p(w.data_ptr()), None, None, 0)
+    else:
+        wt = Weights(None, ctypes.c_void_p(R.data_ptr()) if R is not None else None,
+                     ctypes.c_void_p(M.data_ptr()) if M is not None else None,
+                     R.shape[1] if R is not None and R.dim() == 2 else 0)
+    st = load_library().eqmp_fused_staged(
+        _ptr(h_in), _ptr(d_in), h_in.numel(), _ptr(vec), _ptr(x), n_src, dt, _ptr(row_offsets), _ptr(src),
+        N, E, C, wt, _ptr(out), dt, _ptr(h_out), h_out.numel() * h_out.element_size(), _stream(stream))
+    _check(st, "eqmp_fused_staged")
+    return h_out
 
 
 def eqmp_fused_so2(vec, x, row_offsets, src, w=None, R=None, M=None, out=None, stream=None,

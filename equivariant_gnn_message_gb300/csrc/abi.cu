@@ -270,6 +270,26 @@ eqmp_status eqmp_fused(const float* vec, const void* x, int64_t N_src, eqmp_dtyp
                    reinterpret_cast<cudaStream_t>(stream));
 }
 
+eqmp_status eqmp_fused_staged(const void* h_in, void* d_in, size_t in_bytes, const float* vec,
+                              const void* x, int64_t N_src, eqmp_dtype x_dtype,
+                              const int32_t* row_offsets, const int32_t* src, int64_t N, int64_t E,
+                              int32_t C, eqmp_weights weights, void* out, eqmp_dtype out_dtype,
+                              void* h_out, size_t out_bytes, eqmp_stream_t stream) {
+  if ((in_bytes > 0 && (!h_in || !d_in)) || (out_bytes > 0 && (!h_out || !out))) return EQMP_ERR_INVALID_ARG;
+  if (N < 0 || C <= 0 || (out_dtype != EQMP_F32 && out_dtype != EQMP_BF16)) return EQMP_ERR_INVALID_ARG;
+  const size_t out_size = (size_t)N * (size_t)C * 16 * (out_dtype == EQMP_BF16 ? 2 : 4);
+  if (out_bytes > out_size) return EQMP_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (in_bytes > 0 && cudaMemcpyAsync(d_in, h_in, in_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return EQMP_ERR_CUDA;
+  const eqmp_status s = run_layer(true, vec, x, N_src, x_dtype, row_offsets, src, N, E, C, weights, out,
+                                  out_dtype, st);
+  if (s != EQMP_OK) return s;
+  if (out_bytes > 0 && cudaMemcpyAsync(h_out, out, out_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return EQMP_ERR_CUDA;
+  return EQMP_OK;
+}
+
 eqmp_status eqmp_validate_graph(const int32_t* row_offsets, const int32_t* src, int64_t N,
                                 int64_t N_src, int64_t E, eqmp_stream_t stream) {
   if (N < 0 || N_src < 0 || E < 0 || N > INT32_MAX - 1 || N_src > INT32_MAX || E > INT32_MAX)

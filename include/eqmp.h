@@ -139,6 +139,32 @@ eqmp_status eqmp_fused(const float* vec, const void* x, int64_t N_src, eqmp_dtyp
                        eqmp_stream_t stream);
 
 /*
+ * eqmp_fused for a caller whose inputs and result live in host memory: one
+ * call stages a whole step on `stream`, in this order:
+ *   1. a copy of in_bytes bytes from h_in (host) to d_in (device);
+ *   2. eqmp_fused with the layer arguments given, device pointers that may
+ *      point into d_in (the caller packs the step's arrays into one block);
+ *   3. a copy of out_bytes bytes from out (device) to h_out (host).
+ * The caller synchronises `stream` before reading h_out.  h_in and h_out
+ * should be page-locked for the copies to overlap the host; pageable memory
+ * works, with copies that wait for the host.  No device memory is
+ * allocated.
+ *   h_in, d_in   host / device blocks of in_bytes bytes (NULL only with
+ *                in_bytes == 0)
+ *   h_out        host block of out_bytes bytes (NULL only with
+ *                out_bytes == 0); out_bytes <= the size of out
+ * Errors: EQMP_ERR_INVALID_ARG for a missing block or out_bytes beyond out,
+ * before any copy; the layer's errors as eqmp_fused (the input copy is then
+ * already queued, the output copy is not); EQMP_ERR_CUDA when a copy cannot
+ * be queued.
+ */
+eqmp_status eqmp_fused_staged(const void* h_in, void* d_in, size_t in_bytes, const float* vec,
+                              const void* x, int64_t N_src, eqmp_dtype x_dtype,
+                              const int32_t* row_offsets, const int32_t* src, int64_t N, int64_t E,
+                              int32_t C, eqmp_weights weights, void* out, eqmp_dtype out_dtype,
+                              void* h_out, size_t out_bytes, eqmp_stream_t stream);
+
+/*
  * Backward of eqmp_fused (fp32 storage): gradients of a scalar loss L given
  * grad_out = dL/dout [N][C][16] fp32 (16-byte aligned):
  *   grad_x   [N_src][C][16]  dL/dx, every row written (0 for nodes that send nothing)

@@ -131,3 +131,18 @@ def test_backward_wrappers_reject_a_wrong_dtype_before_any_call(lib, entry):
             fn(**kw, w=torch.zeros(34, 8, dtype=f32))
     with pytest.raises(ValueError, match="CUDA"):  # right dtypes, host memory
         fn(**args, w=torch.zeros(34, 8, dtype=f32))
+
+
+def test_staged_entry_rejects_missing_blocks_before_any_copy(lib):
+    """eqmp_fused_staged checks its host/device blocks and the output size
+    before queueing anything (no GPU needed: every call below fails first)."""
+    import equivariant_gnn_message_gb300 as eq
+
+    d = ctypes.c_void_p(256)  # never dereferenced
+    w = eq.Weights(d, None, None, 0)
+    layer = (d, d, 8, eq.EQMP_F32, d, d, 4, 8, 8, w, d, eq.EQMP_F32)
+    assert lib.eqmp_fused_staged(None, d, 16, *layer, d, 16, None) == eq.EQMP_ERR_INVALID_ARG   # no h_in
+    assert lib.eqmp_fused_staged(d, None, 16, *layer, d, 16, None) == eq.EQMP_ERR_INVALID_ARG   # no d_in
+    assert lib.eqmp_fused_staged(d, d, 16, *layer, None, 16, None) == eq.EQMP_ERR_INVALID_ARG   # no h_out
+    # out holds 4 x 8 x 16 floats = 2048 bytes
+    assert lib.eqmp_fused_staged(d, d, 16, *layer, d, 2049, None) == eq.EQMP_ERR_INVALID_ARG

@@ -25,7 +25,9 @@ Prints ONE JSON line (rank 0):
                max SM clock) and the measured one (eqmp_fp32_peak_probe);
   workloads    the same measurement (time, roofline, clocks) for the
                100k-atom, the dense bf16 and the radial-weight workloads,
-               and the 100k-atom workload renumbered in Morton order;
+               the 100k-atom workload renumbered in Morton order, and the
+               rows past the layer: the backward pass, the open and the
+               periodic radius graph, the degree-6 layer;
   cpu_baseline the CPU oracle (numpy, fp64) on a bounded sample of the same
                workload on this host's cores, plus one-thread runs of the
                tiny, pages and radial workloads.
@@ -52,6 +54,13 @@ FLUSH_BYTES = 256 << 20
 HEADLINE = "pages_1k_c32"
 # Measured beside the headline in the default run (the other full-size configurations).
 EXTRA_WORKLOADS = ("scale_100k_c64", "dense_10k_c128_bf16", "radial_1k_c32", "scale_100k_c64_morton")
+# The rows past the layer, measured in the same run: (label, workload, pass).
+EXTRA_PASSES = (("backward pages_1k_c32", "pages_1k_c32", "backward"),
+                ("backward radial_1k_c32", "radial_1k_c32", "backward"),
+                ("backward scale_100k_c64", "scale_100k_c64", "backward"),
+                ("radius graph scale_100k_c64", "scale_100k_c64", "graph"),
+                ("periodic radius graph scale_100k_c64", "scale_100k_c64", "graph_pbc"),
+                ("degree-6 layer pages_1k_c32", "pages_1k_c32", "lmax6"))
 # One-thread oracle runs (the small configurations).
 SINGLE_THREAD_WORKLOADS = ("tiny_64", "pages_1k_c32", "radial_1k_c32")
 GROUP = 32  # timed steps queued behind one GPU spin
@@ -641,24 +650,87 @@ def main():
     extra = []
     run_extra = (args.workload == HEADLINE and args.which == "forward" and args.lmax == 3
                  and args.entry == "fused" and not args.no_workloads)
-    extra_launches = 0
     if run_extra:
         del d
-        for name in EXTRA_WORKLOADS:
-            xw = make_workload(name)
-            xd = device_inputs(torch, xw, dev)
-            xo = torch.empty((xw.n_atoms, xw.channels, 16), dtype=xd["x"].dtype, device=dev)
-            xs = layer_step(eq, "fused", 3, xd, xo)
-            timer.warm(xs, args.warmup)
+
+        def timed(step_fn):
+            timer.warm(step_fn, args.warmup)
             barrier()
             ta = time.time()
-            xk = timer.run(xs, args.steps)
+            k = timer.run(step_fn, args.steps)
             barrier()
             tb = time.time()
-            xms = max_over_ranks(float(np.mean(xk)))
-            extra.append(dict(name=name, wl=xw, ms=xms, kernel_ms=xk, t=(ta, tb)))
-            extra_launches += args.steps
+            return max_over_ranks(float(np.mean(k))), k, (ta, tb)
+
+        wl_cache = {}
+
+        def get_wl(name, l_max=3):
+            if (name, l_max) not in wl_cache:
+                wl_cache[(name, l_max)] = make_workload(name, l_max=l_max)
+            return wl_cache[(name, l_max)]
+
+        for name in EXTRA_WORKLOADS:
+            xw = get_wl(name)
+            xd = device_inputs(torch, xw, dev)
+            xo = torch.empty((xw.n_atoms, xw.channels, 16), dtype=xd["x"].dtype, device=dev)
+            xms, xk, tt = timed(layer_step(eq, "fused", 3, xd, xo))
+            extra.append(dict(name=name, label=name, kind="forward", wl=xw, ms=xms, kernel_ms=xk, t=tt,
+                              launches=1, n_edges=xw.n_edges))
             del xd, xo
+            torch.cuda.empty_cache()
+
+        for label, name, kind in EXTRA_PASSES:
+            xw = get_wl(name, 6 if kind == "lmax6" else 3)
+            entry = dict(name=name, label=label, kind=kind, wl=xw, n_edges=xw.n_edges)
+            if kind == "backward":
+                xd = device_inputs(torch, xw, dev)
+                so, se = eq.sender_view(xw.src, xw.n_atoms)
+                g = torch.randn((xw.n_atoms, xw.channels, 16), device=dev,
+                                generator=torch.Generator(device=dev).manual_seed(0))
+                need = ("x", "vec", "w") if xw.w is not None else ("x", "vec", "R", "M")
+                bkw = dict(w=xd["w"]) if xw.w is not None else dict(R=xd["R"], M=xd["M"])
+                bargs = (xd["vec"], xd["x"], xd["off"], xd["src"], t(xw.dst), t(so), t(se), g)
+                fn = lambda: eq.eqmp_fused_backward(*bargs, need=need, **bkw)
+                entry["launches"] = 3
+            elif kind in ("graph", "graph_pbc"):
+                import ctypes
+
+                lib = eq.load_library()
+                Ng = xw.n_atoms
+                gbox = None
+                gpos = xw.pos
+                if kind == "graph_pbc":
+                    side = float((Ng / DENSITY) ** (1.0 / 3.0))
+                    gbox = (side, side, side)
+                    gpos = np.minimum(np.maximum(xw.pos, np.float32(0)), np.nextafter(np.float32(side), np.float32(0)))
+                xpos = t(gpos)
+                gws = torch.empty(lib.eqmp_radius_graph_workspace_size(Ng), dtype=torch.uint8, device=dev)
+                gE = torch.empty(1, dtype=torch.int64, device=dev)
+                gout, Eg = eq.eqmp_radius_graph(xpos, xw.cutoff, box=gbox)
+                gst = stream.cuda_stream
+                if gbox is None:
+                    gargs = (xpos.data_ptr(), Ng, ctypes.c_float(xw.cutoff), gout["off"].data_ptr(),
+                             gout["src"].data_ptr(), gout["vec"].data_ptr(), None, None, Eg, gE.data_ptr(),
+                             gws.data_ptr(), gws.numel(), gst)
+                    fn = lambda: lib.eqmp_radius_graph(*gargs)
+                else:
+                    glen = (ctypes.c_float * 3)(*gbox)
+                    gargs = (xpos.data_ptr(), Ng, ctypes.c_float(xw.cutoff), glen, gout["off"].data_ptr(),
+                             gout["src"].data_ptr(), gout["vec"].data_ptr(), gout["img"].data_ptr(), None, None,
+                             Eg, gE.data_ptr(), gws.data_ptr(), gws.numel(), gst)
+                    fn = lambda: lib.eqmp_radius_graph_pbc(*gargs)
+                entry["launches"] = 1 if Ng <= 16384 else 12
+                entry["n_edges"] = Eg
+                entry["gbytes"] = 12 * Ng + 4 * (Ng + 1) + (20 if gbox is not None else 16) * Eg
+            else:  # lmax6
+                xd = device_inputs(torch, xw, dev)
+                xo = torch.empty((xw.n_atoms, xw.channels, 49), dtype=torch.float32, device=dev)
+                lkw = dict(w=xd["w"]) if xw.w is not None else dict(R=xd["R"], M=xd["M"])
+                fn = lambda: eq.eqmp_fused_lmax(6, xd["vec"], xd["x"], xd["off"], xd["src"], out=xo, **lkw)
+                entry["launches"] = 1
+            entry["ms"], entry["kernel_ms"], entry["t"] = timed(fn)
+            extra.append(entry)
+            fn = None
             torch.cuda.empty_cache()
 
     # ---- FP32 throughput probe (paired FMAs only), outside every timed
@@ -726,16 +798,28 @@ def main():
 
     workloads = []
     for x in extra:
-        xw = x["wl"]
-        xv = kernel_version(xw, "forward", 3, "fused")
+        xw, kind = x["wl"], x["kind"]
+        if kind in ("graph", "graph_pbc"):
+            xroof = roofline(0.0, x["gbytes"], x["ms"], fp32_peak, hbm_peak,
+                            ("radius-graph cooperative single launch" if x["launches"] == 1 else
+                             "radius-graph multi-kernel (12 launches)") + (", periodic" if kind == "graph_pbc" else ""),
+                            None, "compulsory bytes: positions, offsets, senders, edge vectors"
+                            + (", image indices" if kind == "graph_pbc" else ""))
+        elif kind == "backward":
+            xroof = layer_roof(xw, x["ms"], kernel_version(xw, "backward", 3, "fused"), "backward", 3, "fused")
+        elif kind == "lmax6":
+            xroof = layer_roof(xw, x["ms"], kernel_version(xw, "forward", 6, "fused"), "forward", 6, "fused")
+        else:
+            xroof = layer_roof(xw, x["ms"], kernel_version(xw, "forward", 3, "fused"), "forward", 3, "fused")
         workloads.append({
-            "workload": x["name"], "n_atoms": xw.n_atoms, "n_edges": xw.n_edges, "channels": xw.channels,
+            "label": x["label"], "workload": x["name"], "pass": kind, "n_atoms": xw.n_atoms,
+            "n_edges": x["n_edges"], "channels": xw.channels,
             "storage": xw.storage, "weights": "shared" if xw.w is not None else "radial",
-            "ms_per_step": x["ms"], "value": xw.n_edges * world / (x["ms"] * 1e-3), "unit": "edges/s",
-            "steps": args.steps, "gpu_launches": args.steps,
+            "ms_per_step": x["ms"], "value": x["n_edges"] * world / (x["ms"] * 1e-3), "unit": "edges/s",
+            "steps": args.steps, "gpu_launches": args.steps * x["launches"],
             "kernel_ms": {"min": float(np.min(x["kernel_ms"])), "median": float(np.median(x["kernel_ms"])),
                           "max": float(np.max(x["kernel_ms"]))},
-            "roofline": layer_roof(xw, x["ms"], xv, "forward", 3, "fused"),
+            "roofline": xroof,
             "clocks": sampler.summary(*x["t"]),
         })
 

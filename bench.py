@@ -64,6 +64,7 @@ EXTRA_PASSES = (("backward pages_1k_c32", "pages_1k_c32", "backward"),
 # One-thread oracle runs (the small configurations).
 SINGLE_THREAD_WORKLOADS = ("tiny_64", "pages_1k_c32", "radial_1k_c32")
 GROUP = 32  # timed steps queued behind one GPU spin
+PIPE = 4  # streams (and buffer sets) of the pipelined end-to-end measurement
 # DRAM bytes per launch of the layer kernel from the ncu capture recorded in
 # profiles/ (None until captured for the current kernel version).
 # Keyed by (workload, kernel version); a changed kernel gets a new version
@@ -569,6 +570,7 @@ def main():
     # inputs sit in one pinned host block (each array 256-byte aligned) and
     # go over in one host->device copy; the result comes back in one copy.
     e2e_ms, h2d, d2h = None, 0, 0
+    pipe_sets, e2e_serial_ms, e2e_mode = None, None, None
     if args.which == "forward":
         parts = {"vec": wl.vec, "off": wl.off, "src": wl.src,
                  "x": wl.x_bf16_bits.view(np.int16) if wl.storage == "bf16" else wl.x}
@@ -608,9 +610,21 @@ def main():
             # copy, the layer, the result's device-to-host copy
             e2e_api = "eqmp_fused_staged"
 
-            def e2e_step():
-                eq.eqmp_fused_staged(h_pack, d_pack, d_in["vec"], d_in["x"], d_in["off"], d_in["src"], out, h_out,
-                                     w=d_in["w"], R=d_in["R"], M=d_in["M"])
+            def staged(dp, di, o, ho, st=None):
+                # checked and marshalled once; each step is the C call alone
+                return eq.eqmp_fused_staged(h_pack, dp, di["vec"], di["x"], di["off"], di["src"], o, ho,
+                                            w=di["w"], R=di["R"], M=di["M"], stream=st, prepare=True)
+
+            e2e_step = staged(d_pack, d_in, out, h_out, stream)
+
+            # the same step on PIPE streams, one buffer set each: step k's
+            # copies run while earlier steps' layers do
+            pipe_sets = [(d_pack, d_in, out, h_out)]
+            for _ in range(PIPE - 1):
+                dp2 = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+                di2 = {k: None if v is None else dp2[v.data_ptr() - d_pack.data_ptr():][:v.numel() * v.element_size()]
+                       .view(v.dtype).view(v.shape) for k, v in d_in.items()}
+                pipe_sets.append((dp2, di2, torch.empty_like(out), torch.empty_like(h_out).pin_memory()))
         else:
             e2e_api = "torch copies + " + {"so2": "eqmp_fused_so2", "tp_scatter": "eqmp_sh + eqmp_tp_scatter"}.get(
                 args.entry, "eqmp_fused_lmax")
@@ -645,6 +659,46 @@ def main():
             e_e[i].record(stream)
         barrier()
         e2e_ms = max_over_ranks(float(np.mean([s.elapsed_time(e) for s, e in zip(e_s, e_e)])))
+        e2e_mode = "serial: one stream, L2 flushed between steps, per-step events"
+        if pipe_sets is not None:
+            # K steps on PIPE streams, each step's inputs copied in and its
+            # result copied out and read on the host (after its step's event)
+            # before its buffers take step k+PIPE; one span from the first
+            # copy to the last result
+            e2e_serial_ms = e2e_ms
+            streams = [torch.cuda.Stream(device=dev) for _ in range(PIPE)]
+            # each buffer set's step recorded once as a CUDA graph (eqmp_plan_staged)
+            plans = [eq.eqmp_plan_staged(h_pack, dp, di["vec"], di["x"], di["off"], di["src"], o, ho,
+                                         w=di["w"], R=di["R"], M=di["M"]) for dp, di, o, ho in pipe_sets]
+            runs = [lambda b=b: plans[b].launch(streams[b]) for b in range(PIPE)]
+            host_bytes = [ps[3].view(torch.uint8).numpy().reshape(-1) for ps in pipe_sets]
+            for i in range(2 * PIPE):
+                runs[i % PIPE]()
+            torch.cuda.synchronize()
+            barrier()
+            t_beg, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t_beg.record(streams[0])
+            for st_ in streams[1:]:
+                st_.wait_event(t_beg)
+            done = [torch.cuda.Event() for _ in range(args.steps)]
+            check = 0.0
+            for i in range(args.steps):
+                if i >= PIPE:
+                    done[i - PIPE].synchronize()
+                    check += float(host_bytes[i % PIPE][0])  # step i-PIPE's result, read on the host
+                runs[i % PIPE]()
+                done[i].record(streams[i % PIPE])
+            for i in range(max(0, args.steps - PIPE), args.steps):
+                streams[0].wait_event(done[i])
+            t_end.record(streams[0])
+            torch.cuda.synchronize()
+            barrier()
+            e2e_ms = max_over_ranks(t_beg.elapsed_time(t_end) / args.steps)
+            e2e_mode = (f"pipelined: {PIPE} streams, one device block each, each step one CUDA graph launch "
+                        "(eqmp_plan_staged), no L2 flush (inputs arrive by copy)")
+            e2e_api = "eqmp_plan_staged + eqmp_plan_launch"
+            for p_ in plans:
+                p_.destroy()
 
     # ---- the other full-size workloads, same timing, one entry each
     extra = []
@@ -854,7 +908,8 @@ def main():
         "roofline": roof,
         "e2e": None if e2e_ms is None else {
             "value": n_edges * world / (e2e_ms * 1e-3), "unit": "edges/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "api": e2e_api},
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "api": e2e_api,
+            "mode": e2e_mode, "serial_ms_per_step": e2e_serial_ms},
         "pass": args.which,
         "l_max": args.lmax,
         "graph_edges": None if args.which != "graph" else E_graph,

@@ -12,6 +12,9 @@ Entry points (same names as the C ABI):
   eqmp_tp_scatter(Y, x, row_offsets, src, ...)  -> out [N, C, 16]
   eqmp_fused(vec, x, row_offsets, src, ...)     -> out [N, C, 16]
   eqmp_fused_staged(h_in, d_in, ..., out, h_out) -> h_out: copy in, layer, copy out
+                                                (prepare=True: a prepared call for a step loop)
+  eqmp_plan_staged(h_in, d_in, ..., out, h_out)  -> plan; plan.launch(stream): the same step as one
+                                                CUDA graph launch
   eqmp_fused_so2(...)                           -> out, aligned-frame schedule
   eqmp_validate_graph(row_offsets, src, n_src, n_edges)
   eqmp_device_error()                           -> int (watchdog code)
@@ -27,7 +30,8 @@ import os
 
 __all__ = [
     "EqmpError", "load_library", "library_path", "eqmp_num_paths", "eqmp_path_table",
-    "eqmp_status_string", "eqmp_sh", "eqmp_tp_scatter", "eqmp_fused", "eqmp_fused_staged", "eqmp_fused_so2",
+    "eqmp_status_string", "eqmp_sh", "eqmp_tp_scatter", "eqmp_fused", "eqmp_fused_staged", "eqmp_plan_staged",
+    "eqmp_fused_so2",
     "eqmp_validate_graph",
     "eqmp_device_error", "eqmp_fused_backward", "eqmp_fused_backward_noalloc", "eqmp_radius_graph", "eqmp_fused_lmax",
     "eqmp_num_paths_lmax", "eqmp_watchdog_selftest", "eqmp_fp32_peak_probe", "sender_view", "EQMP_OK", "EQMP_ERR_INVALID_ARG", "EQMP_ERR_UNSUPPORTED",
@@ -85,6 +89,12 @@ def load_library():
     sz = ctypes.c_size_t
     lib.eqmp_fused_staged.argtypes = [vp, vp, sz] + layer[:-1] + [vp, sz, vp]
     lib.eqmp_fused_staged.restype = i32
+    lib.eqmp_plan_staged.argtypes = [vp, vp, sz] + layer[:-1] + [vp, sz, ctypes.POINTER(vp)]
+    lib.eqmp_plan_staged.restype = i32
+    lib.eqmp_plan_launch.argtypes = [vp, vp]
+    lib.eqmp_plan_launch.restype = i32
+    lib.eqmp_plan_destroy.argtypes = [vp]
+    lib.eqmp_plan_destroy.restype = i32
     lib.eqmp_validate_graph.argtypes = [vp, vp, i64, i64, i64, vp]
     lib.eqmp_validate_graph.restype = i32
     lib.eqmp_device_error.argtypes = [ctypes.POINTER(i32)]
@@ -239,11 +249,16 @@ def eqmp_fused(vec, x, row_offsets, src, w=None, R=None, M=None, out=None, strea
 
 
 def eqmp_fused_staged(h_in, d_in, vec, x, row_offsets, src, out, h_out, w=None, R=None, M=None, stream=None,
-                      n_edges=None):
+                      n_edges=None, prepare=False):
     """One step from host memory: h_in (pinned CPU uint8) -> d_in (CUDA
     uint8, same size), eqmp_fused on the CUDA tensors given (views into
     d_in), out -> h_out (pinned CPU, out's size).  Asynchronous on the
-    stream; synchronise before reading h_out."""
+    stream; synchronise before reading h_out.
+
+    prepare=True checks and marshals the arguments once and returns a
+    function of no arguments that issues the same C call (for a loop that
+    repeats the step on the same buffers; the tensors must stay alive and
+    unmoved while it is used).  It raises EqmpError on a non-OK status."""
     import torch
 
     _require(h_in, "h_in", torch.uint8, cuda=False)
@@ -274,11 +289,63 @@ def eqmp_fused_staged(h_in, d_in, vec, x, row_offsets, src, out, h_out, w=None, 
         wt = Weights(None, ctypes.c_void_p(R.data_ptr()) if R is not None else None,
                      ctypes.c_void_p(M.data_ptr()) if M is not None else None,
                      R.shape[1] if R is not None and R.dim() == 2 else 0)
-    st = load_library().eqmp_fused_staged(
-        _ptr(h_in), _ptr(d_in), h_in.numel(), _ptr(vec), _ptr(x), n_src, dt, _ptr(row_offsets), _ptr(src),
-        N, E, C, wt, _ptr(out), dt, _ptr(h_out), h_out.numel() * h_out.element_size(), _stream(stream))
-    _check(st, "eqmp_fused_staged")
+    fn = load_library().eqmp_fused_staged
+    args = (_ptr(h_in), _ptr(d_in), h_in.numel(), _ptr(vec), _ptr(x), n_src, dt, _ptr(row_offsets), _ptr(src),
+            N, E, C, wt, _ptr(out), dt, _ptr(h_out), h_out.numel() * h_out.element_size(), _stream(stream))
+    if prepare == "plan":
+        return _Plan(args[:-1], (h_in, d_in, vec, x, row_offsets, src, out, h_out, w, R, M))
+    if prepare:
+        keep = (h_in, d_in, vec, x, row_offsets, src, out, h_out, w, R, M, stream)
+
+        def run(_keep=keep):
+            st = fn(*args)
+            if st != EQMP_OK:
+                raise EqmpError(st, "eqmp_fused_staged")
+            return h_out
+        return run
+    _check(fn(*args), "eqmp_fused_staged")
     return h_out
+
+
+class _Plan:
+    """A staged step recorded once as a CUDA graph (eqmp_plan_staged);
+    launch(stream) replays it with one graph launch."""
+
+    def __init__(self, args, keep):
+        lib = load_library()
+        h = ctypes.c_void_p()
+        _check(lib.eqmp_plan_staged(*args, ctypes.byref(h)), "eqmp_plan_staged")
+        self._h, self._keep, self._lib = h, keep, lib
+        self.h_out = keep[7]
+
+    def launch(self, stream=None):
+        st = self._lib.eqmp_plan_launch(self._h, _stream(stream))
+        if st != EQMP_OK:
+            raise EqmpError(st, "eqmp_plan_launch")
+        return self.h_out
+
+    def destroy(self):
+        if self._h:
+            self._lib.eqmp_plan_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:  # pragma: no cover - interpreter shutdown
+            pass
+
+
+def eqmp_plan_staged(h_in, d_in, vec, x, row_offsets, src, out, h_out, w=None, R=None, M=None, n_edges=None):
+    """The step of eqmp_fused_staged recorded once as a CUDA graph: returns a
+    plan whose launch(stream=None) replays the input copy, the layer and the
+    result copy with one graph launch.  The tensors must stay alive and
+    unmoved while the plan is used (the plan holds references to them);
+    h_in and h_out must be pinned."""
+    if not (h_in.is_pinned() and h_out.is_pinned()):
+        raise ValueError("h_in and h_out must be pinned for a plan")
+    return eqmp_fused_staged(h_in, d_in, vec, x, row_offsets, src, out, h_out, w=w, R=R, M=M, n_edges=n_edges,
+                             prepare="plan")
 
 
 def eqmp_fused_so2(vec, x, row_offsets, src, w=None, R=None, M=None, out=None, stream=None,

@@ -290,6 +290,59 @@ eqmp_status eqmp_fused_staged(const void* h_in, void* d_in, size_t in_bytes, con
   return EQMP_OK;
 }
 
+struct eqmp_plan_st {
+  cudaGraph_t graph;
+  cudaGraphExec_t exec;
+};
+
+eqmp_status eqmp_plan_staged(const void* h_in, void* d_in, size_t in_bytes, const float* vec, const void* x,
+                             int64_t N_src, eqmp_dtype x_dtype, const int32_t* row_offsets, const int32_t* src,
+                             int64_t N, int64_t E, int32_t C, eqmp_weights weights, void* out,
+                             eqmp_dtype out_dtype, void* h_out, size_t out_bytes, eqmp_plan* plan) {
+  if (!plan) return EQMP_ERR_INVALID_ARG;
+  *plan = nullptr;
+  // per-device state first: nothing below may allocate while capturing
+  DeviceInfo dev;
+  eqmp_status s = device_info(&dev);
+  if (s != EQMP_OK) return s;
+  cudaStream_t cs = nullptr;
+  if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) return EQMP_ERR_CUDA;
+  if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed) != cudaSuccess) {
+    cudaStreamDestroy(cs);
+    return EQMP_ERR_CUDA;
+  }
+  s = eqmp_fused_staged(h_in, d_in, in_bytes, vec, x, N_src, x_dtype, row_offsets, src, N, E, C, weights, out,
+                        out_dtype, h_out, out_bytes, reinterpret_cast<eqmp_stream_t>(cs));
+  cudaGraph_t g = nullptr;
+  const cudaError_t ce = cudaStreamEndCapture(cs, &g);  // ends the capture whatever happened inside
+  cudaStreamDestroy(cs);
+  if (s != EQMP_OK || ce != cudaSuccess || !g) {
+    if (g) cudaGraphDestroy(g);
+    cudaGetLastError();  // clear the error a failed capture reports, so the next call does not see it
+    return s != EQMP_OK ? s : EQMP_ERR_CUDA;
+  }
+  cudaGraphExec_t ex = nullptr;
+  if (cudaGraphInstantiate(&ex, g, 0) != cudaSuccess) {
+    cudaGraphDestroy(g);
+    return EQMP_ERR_CUDA;
+  }
+  *plan = new eqmp_plan_st{g, ex};
+  return EQMP_OK;
+}
+
+eqmp_status eqmp_plan_launch(eqmp_plan plan, eqmp_stream_t stream) {
+  if (!plan) return EQMP_ERR_INVALID_ARG;
+  return cuda_status(cudaGraphLaunch(plan->exec, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+eqmp_status eqmp_plan_destroy(eqmp_plan plan) {
+  if (!plan) return EQMP_OK;
+  const cudaError_t a = cudaGraphExecDestroy(plan->exec);
+  const cudaError_t b = cudaGraphDestroy(plan->graph);
+  delete plan;
+  return a == cudaSuccess && b == cudaSuccess ? EQMP_OK : EQMP_ERR_CUDA;
+}
+
 eqmp_status eqmp_validate_graph(const int32_t* row_offsets, const int32_t* src, int64_t N,
                                 int64_t N_src, int64_t E, eqmp_stream_t stream) {
   if (N < 0 || N_src < 0 || E < 0 || N > INT32_MAX - 1 || N_src > INT32_MAX || E > INT32_MAX)

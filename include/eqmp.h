@@ -165,6 +165,33 @@ eqmp_status eqmp_fused_staged(const void* h_in, void* d_in, size_t in_bytes, con
                               void* h_out, size_t out_bytes, eqmp_stream_t stream);
 
 /*
+ * A staged step recorded once and replayed: eqmp_plan_staged takes the
+ * arguments of eqmp_fused_staged (without the stream), records the input
+ * copy, the layer and the result copy into a CUDA graph (captured on a
+ * private stream; nothing runs at this point) and returns it in *plan.
+ * eqmp_plan_launch replays the whole step on `stream` with one graph
+ * launch, asynchronously; the caller synchronises before reading h_out.
+ * A plan keeps the pointers and sizes it was made with: the buffers must
+ * stay allocated, and h_in and h_out page-locked, until it is destroyed;
+ * their contents may change between launches.  Launches of one plan must
+ * not overlap each other (same stream, or ordered by the caller).
+ * eqmp_plan_destroy frees the graph (NULL: no-op).
+ * Errors: as eqmp_fused_staged at planning time (then *plan = NULL);
+ * EQMP_ERR_INVALID_ARG for a NULL plan; EQMP_ERR_CUDA when the capture,
+ * instantiation or launch fails.  The plan records the layer's launch
+ * configuration for the device current at planning time.
+ */
+typedef struct eqmp_plan_st* eqmp_plan;
+
+eqmp_status eqmp_plan_staged(const void* h_in, void* d_in, size_t in_bytes, const float* vec,
+                             const void* x, int64_t N_src, eqmp_dtype x_dtype,
+                             const int32_t* row_offsets, const int32_t* src, int64_t N, int64_t E,
+                             int32_t C, eqmp_weights weights, void* out, eqmp_dtype out_dtype,
+                             void* h_out, size_t out_bytes, eqmp_plan* plan);
+eqmp_status eqmp_plan_launch(eqmp_plan plan, eqmp_stream_t stream);
+eqmp_status eqmp_plan_destroy(eqmp_plan plan);
+
+/*
  * Backward of eqmp_fused (fp32 storage): gradients of a scalar loss L given
  * grad_out = dL/dout [N][C][16] fp32 (16-byte aligned):
  *   grad_x   [N_src][C][16]  dL/dx, every row written (0 for nodes that send nothing)

@@ -67,3 +67,74 @@ def test_staged_equals_device_call_and_oracle(eq, name):
     want = layer.message_pass(wl.vec, wl.x, wl.off, wl.src, **oracle_kw(wl))
     assert rel_err(got, want) <= TOL[wl.storage]
     assert eq.eqmp_device_error() == 0
+
+
+def test_prepared_staged_call_on_two_streams(eq):
+    """prepare=True returns a call that repeats the step on the same
+    buffers; two prepared calls on two streams, alternating, give the same
+    bits as the one-off call."""
+    import torch
+
+    wl = make_workload("pages_1k_c32")
+    sets = []
+    for _ in range(2):
+        h, d, v = _pack(torch, wl)
+        out = torch.empty((wl.n_atoms, wl.channels, 16), dtype=v["x"].dtype, device="cuda")
+        h_out = torch.full(out.shape, float("nan"), dtype=out.dtype).pin_memory()
+        sets.append((h, d, v, out, h_out))
+    h, d, v, out, h_out = sets[0]
+    eq.eqmp_fused_staged(h, d, v["vec"], v["x"], v["off"], v["src"], out, h_out, w=v["w"])
+    torch.cuda.synchronize()
+    ref = h_out.clone()
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    runs = [eq.eqmp_fused_staged(hh, dd, vv["vec"], vv["x"], vv["off"], vv["src"], oo, ho, w=vv["w"],
+                                 stream=streams[b], prepare=True)
+            for b, (hh, dd, vv, oo, ho) in enumerate(sets)]
+    for i in range(6):
+        runs[i % 2]()
+    torch.cuda.synchronize()
+    for b in range(2):
+        assert sets[b][4].equal(ref)
+    want = layer.message_pass(wl.vec, wl.x, wl.off, wl.src, w=wl.w)
+    assert rel_err(ref.numpy().astype(np.float64), want) <= TOL["f32"]
+    assert eq.eqmp_device_error() == 0
+
+
+def test_plan_replays_the_staged_step(eq):
+    """eqmp_plan_staged records the step once; launches on two streams (two
+    plans over two buffer sets) give the one-off call's bits, and the plan
+    follows new input contents."""
+    import torch
+
+    wl = make_workload("pages_1k_c32")
+    sets = []
+    for _ in range(2):
+        h, d, v = _pack(torch, wl)
+        out = torch.empty((wl.n_atoms, wl.channels, 16), dtype=v["x"].dtype, device="cuda")
+        h_out = torch.full(out.shape, float("nan"), dtype=out.dtype).pin_memory()
+        sets.append((h, d, v, out, h_out))
+    h, d, v, out, h_out = sets[0]
+    eq.eqmp_fused_staged(h, d, v["vec"], v["x"], v["off"], v["src"], out, h_out, w=v["w"])
+    torch.cuda.synchronize()
+    ref = h_out.clone()
+    plans = [eq.eqmp_plan_staged(hh, dd, vv["vec"], vv["x"], vv["off"], vv["src"], oo, ho, w=vv["w"])
+             for hh, dd, vv, oo, ho in sets]
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    for b in range(2):
+        sets[b][4].fill_(float("nan"))
+    for i in range(6):
+        plans[i % 2].launch(streams[i % 2])
+    torch.cuda.synchronize()
+    for b in range(2):
+        assert sets[b][4].equal(ref)
+    # new features in the host block: the next launch copies and uses them
+    h0 = sets[0][0]
+    xo = v["x"].data_ptr() - d.data_ptr()
+    nx = wl.x.nbytes
+    h0.numpy()[xo:xo + nx] = (2.0 * wl.x).view(np.uint8).reshape(-1)
+    plans[0].launch(streams[0])
+    torch.cuda.synchronize()
+    assert torch.allclose(sets[0][4], 2.0 * ref, rtol=1e-6, atol=1e-6)
+    for p in plans:
+        p.destroy()
+    assert eq.eqmp_device_error() == 0

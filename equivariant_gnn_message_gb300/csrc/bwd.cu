@@ -63,6 +63,15 @@ static long long bwd_slots(long long N, int sms) {
   return (want < cap ? want : cap) * K::GROUPS;
 }
 
+// Blocks of k_bwd_wv with radial weights (no per-block workspace rows).
+template <int C>
+static long long radial_wv_grid(long long N, int sms) {
+  using K = BwdCfg<C, true>;
+  const long long want = (N + K::NODES - 1) / K::NODES;
+  const long long cap = (long long)sms * kBwdGridPerSm;
+  return want < cap ? want : cap;
+}
+
 static long long slots_for(int C, long long N, int sms) {
   switch (C) {
     case 8: return bwd_slots<8>(N, sms);
@@ -106,16 +115,31 @@ static eqmp_status run_dx_shared(const BwdArgs& b, int C, cudaStream_t st, const
   return launch_shared_dx_f32(a, C, map, st, dev);
 }
 
+// dL/dM from the per-edge path sums S (a.ws, [E][34C]): chunk partials
+// after S in the workspace, then their fixed-order sum.
+static eqmp_status reduce_M(const BwdArgs& a, int C, float* gM, cudaStream_t st) {
+  const int cols = 34 * C;
+  float* part = a.ws + (size_t)a.E * cols;
+  k_bwd_partial_M<<<dim3((cols + kRedX - 1) / kRedX, kRmChunks), dim3(kRedX, kRedY), 0, st>>>(
+      a.R, a.ws, a.off, a.N, a.E, cols, part);
+  if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
+  k_bwd_reduce_w<<<(8 * cols + kRedX - 1) / kRedX, dim3(kRedX, kRedY), 0, st>>>(part, kRmChunks, 8 * cols, gM);
+  return cuda_status(cudaGetLastError());
+}
+
+// Radial workspace: S rows for every edge, then the chunk partials of dL/dM.
+static long long radial_ws_floats(long long E, int C) { return (E + 8ll * kRmChunks) * 34 * C; }
+
 template <int C, bool RADIAL>
-static eqmp_status run_bwd(const BwdArgs& a, bool want_x, bool want_wv, float* gw, float* gM, int e0, int e1,
+static eqmp_status run_bwd(const BwdArgs& a, bool want_x, bool want_wv, float* gw, float* gM,
                            cudaStream_t st, const DeviceInfo& dev) {
   using K = BwdCfg<C, RADIAL>;
   if (!RADIAL && want_x) {
     const eqmp_status s = run_dx_shared(a, C, st, dev);
     if (s != EQMP_OK) return s;
   } else if (want_x && a.N_src > 0) {
-    if constexpr (RADIAL) {  // per-edge weights: one group of lanes per sender
-      const long long want = (a.N_src + K::GROUPS - 1) / K::GROUPS;
+    if constexpr (RADIAL) {  // per-edge weights: one group of lanes (or a block) per sender
+      const long long want = (a.N_src + K::NODES - 1) / K::NODES;
       const long long cap = (long long)dev.sms * 16;
       k_bwd_x<C, RADIAL><<<(int)(want < cap ? want : cap), K::NT, 0, st>>>(a);
       if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
@@ -126,7 +150,7 @@ static eqmp_status run_bwd(const BwdArgs& a, bool want_x, bool want_wv, float* g
     return EQMP_OK;
   }
   if (want_wv && a.N > 0) {
-    const int grid = (int)(bwd_slots<C>(a.N, dev.sms) / K::GROUPS);
+    const int grid = (int)(RADIAL ? radial_wv_grid<C>(a.N, dev.sms) : bwd_slots<C>(a.N, dev.sms) / K::GROUPS);
     const int smem = RADIAL ? 0 : K::GROUPS * 34 * C * 4;
     static unsigned long long attr_done = 0;
     if (ensure_smem_attr(k_bwd_wv<C, RADIAL>, smem > 0 ? smem : 1, &attr_done) != cudaSuccess)
@@ -137,23 +161,20 @@ static eqmp_status run_bwd(const BwdArgs& a, bool want_x, bool want_wv, float* g
       k_bwd_reduce_w<<<(34 * C + kRedX - 1) / kRedX, dim3(kRedX, kRedY), 0, st>>>(a.ws, grid * K::GROUPS, 34 * C, gw);
       if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
     }
-    if (RADIAL && gM) {
-      k_bwd_reduce_M<<<dim3((34 * C + kRedX - 1) / kRedX, 8), dim3(kRedX, kRedY), 0, st>>>(a.R, a.ws, e0, e1, 34 * C, gM);
-      if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
-    }
+    if (RADIAL && gM) return reduce_M(a, C, gM, st);
   }
   return EQMP_OK;
 }
 
 template <bool RADIAL>
 static eqmp_status dispatch_bwd(int C, const BwdArgs& a, bool want_x, bool want_wv, float* gw, float* gM,
-                                int e0, int e1, cudaStream_t st, const DeviceInfo& dev) {
+                                cudaStream_t st, const DeviceInfo& dev) {
   switch (C) {
-    case 8: return run_bwd<8, RADIAL>(a, want_x, want_wv, gw, gM, e0, e1, st, dev);
-    case 16: return run_bwd<16, RADIAL>(a, want_x, want_wv, gw, gM, e0, e1, st, dev);
-    case 32: return run_bwd<32, RADIAL>(a, want_x, want_wv, gw, gM, e0, e1, st, dev);
-    case 64: return run_bwd<64, RADIAL>(a, want_x, want_wv, gw, gM, e0, e1, st, dev);
-    case 128: return run_bwd<128, RADIAL>(a, want_x, want_wv, gw, gM, e0, e1, st, dev);
+    case 8: return run_bwd<8, RADIAL>(a, want_x, want_wv, gw, gM, st, dev);
+    case 16: return run_bwd<16, RADIAL>(a, want_x, want_wv, gw, gM, st, dev);
+    case 32: return run_bwd<32, RADIAL>(a, want_x, want_wv, gw, gM, st, dev);
+    case 64: return run_bwd<64, RADIAL>(a, want_x, want_wv, gw, gM, st, dev);
+    case 128: return run_bwd<128, RADIAL>(a, want_x, want_wv, gw, gM, st, dev);
   }
   return EQMP_ERR_UNSUPPORTED;
 }
@@ -168,7 +189,7 @@ extern "C" {
 
 int64_t eqmp_fused_backward_workspace_size(int64_t N, int64_t E, int32_t C, int32_t radial) {
   if (N < 0 || E < 0) return -1;
-  if (radial) return E * 34 * (int64_t)C * 4;
+  if (radial) return radial_ws_floats(E, C) * 4;
   DeviceInfo dev;
   if (device_info(&dev) != EQMP_OK) return -1;
   const long long slots = slots_for(C, N, dev.sms);
@@ -208,32 +229,21 @@ eqmp_status eqmp_fused_backward(const float* vec, const float* x, int64_t N_src,
   if (want_wv && need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
     return EQMP_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  int e0 = 0, e1 = 0;
-  if (radial && grad_M && N > 0) {
-    // the edge range of this call's receivers, read once (synchronous)
-    int h[2] = {0, 0};
-    if (cudaMemcpyAsync(&h[0], row_offsets, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-        cudaMemcpyAsync(&h[1], row_offsets + N, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-        cudaStreamSynchronize(st) != cudaSuccess)
-      return EQMP_ERR_CUDA;
-    e0 = h[0] < 0 ? 0 : (h[0] > E ? (int)E : h[0]);
-    e1 = h[1] < e0 ? e0 : (h[1] > E ? (int)E : h[1]);
-  }
   BwdArgs a{};
   a.vec = vec; a.x = x; a.off = row_offsets; a.src = src; a.dst = dst;
   a.send_off = send_offsets; a.send_edges = send_edges;
   a.w = weights.w; a.R = weights.R; a.M = weights.M; a.g = grad_out;
   a.gx = grad_x; a.gvec = grad_vec; a.gR = grad_R; a.ws = static_cast<float*>(workspace);
   a.N = (int)N; a.E = (int)E; a.N_src = (int)N_src; a.n_send = (int)E_send;
-  if (radial && grad_M && e1 == e0) {  // no edge: dL/dM = 0
+  if (radial && grad_M && N == 0) {  // no receiver, no edge: dL/dM = 0
     if (cudaMemsetAsync(grad_M, 0, (size_t)8 * 34 * C * 4, st) != cudaSuccess) return EQMP_ERR_CUDA;
     grad_M = nullptr;
   }
   if (!radial && grad_w && N == 0) {
     if (cudaMemsetAsync(grad_w, 0, (size_t)34 * C * 4, st) != cudaSuccess) return EQMP_ERR_CUDA;
   }
-  return radial ? dispatch_bwd<true>(C, a, want_x, want_wv, nullptr, grad_M, e0, e1, st, dev)
-                : dispatch_bwd<false>(C, a, want_x, want_wv, grad_w, nullptr, 0, 0, st, dev);
+  return radial ? dispatch_bwd<true>(C, a, want_x, want_wv, nullptr, grad_M, st, dev)
+                : dispatch_bwd<false>(C, a, want_x, want_wv, grad_w, nullptr, st, dev);
 }
 
 }  // extern "C"
@@ -272,15 +282,15 @@ static eqmp_status noalloc_scratch(float** out) {
 }
 
 template <int C, bool RADIAL>
-static eqmp_status run_bwd_noalloc(const BwdArgs& a, bool want_x, bool want_wv, float* gw, float* gM, int e0,
-                                   int e1, cudaStream_t st, const DeviceInfo& dev) {
+static eqmp_status run_bwd_noalloc(const BwdArgs& a, bool want_x, bool want_wv, float* gw, float* gM,
+                                   cudaStream_t st, const DeviceInfo& dev) {
   using K = BwdCfg<C, RADIAL>;
   if (!RADIAL && want_x) {
     const eqmp_status s = run_dx_shared(a, C, st, dev);
     if (s != EQMP_OK) return s;
   } else if (want_x && a.N_src > 0) {
-    if constexpr (RADIAL) {  // per-edge weights: one group of lanes per sender
-      const long long want = (a.N_src + K::GROUPS - 1) / K::GROUPS;
+    if constexpr (RADIAL) {  // per-edge weights: one group of lanes (or a block) per sender
+      const long long want = (a.N_src + K::NODES - 1) / K::NODES;
       const long long cap = (long long)dev.sms * 16;
       k_bwd_x<C, RADIAL><<<(int)(want < cap ? want : cap), K::NT, 0, st>>>(a);
       if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
@@ -294,7 +304,7 @@ static eqmp_status run_bwd_noalloc(const BwdArgs& a, bool want_x, bool want_wv, 
   if (want_wv && a.N > 0) {
     // as many receiver groups as the static scratch holds partial rows for
     const long long fit = (long long)(kNoAllocBytes / ((size_t)34 * C * 4)) / K::GROUPS;
-    long long grid = bwd_slots<C>(a.N, dev.sms) / K::GROUPS;
+    long long grid = RADIAL ? radial_wv_grid<C>(a.N, dev.sms) : bwd_slots<C>(a.N, dev.sms) / K::GROUPS;
     if (!RADIAL && grid > fit) grid = fit;
     const int smem = RADIAL ? 0 : K::GROUPS * 34 * C * 4;
     static unsigned long long attr_done = 0;
@@ -306,23 +316,20 @@ static eqmp_status run_bwd_noalloc(const BwdArgs& a, bool want_x, bool want_wv, 
       k_bwd_reduce_w<<<(34 * C + kRedX - 1) / kRedX, dim3(kRedX, kRedY), 0, st>>>(a.ws, (int)grid * K::GROUPS, 34 * C, gw);
       if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
     }
-    if (RADIAL && gM) {
-      k_bwd_reduce_M<<<dim3((34 * C + kRedX - 1) / kRedX, 8), dim3(kRedX, kRedY), 0, st>>>(a.R, a.ws, e0, e1, 34 * C, gM);
-      if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
-    }
+    if (RADIAL && gM) return reduce_M(a, C, gM, st);
   }
   return EQMP_OK;
 }
 
 template <bool RADIAL>
 static eqmp_status dispatch_bwd_noalloc(int C, const BwdArgs& a, bool want_x, bool want_wv, float* gw, float* gM,
-                                        int e0, int e1, cudaStream_t st, const DeviceInfo& dev) {
+                                        cudaStream_t st, const DeviceInfo& dev) {
   switch (C) {
-    case 8: return run_bwd_noalloc<8, RADIAL>(a, want_x, want_wv, gw, gM, e0, e1, st, dev);
-    case 16: return run_bwd_noalloc<16, RADIAL>(a, want_x, want_wv, gw, gM, e0, e1, st, dev);
-    case 32: return run_bwd_noalloc<32, RADIAL>(a, want_x, want_wv, gw, gM, e0, e1, st, dev);
-    case 64: return run_bwd_noalloc<64, RADIAL>(a, want_x, want_wv, gw, gM, e0, e1, st, dev);
-    case 128: return run_bwd_noalloc<128, RADIAL>(a, want_x, want_wv, gw, gM, e0, e1, st, dev);
+    case 8: return run_bwd_noalloc<8, RADIAL>(a, want_x, want_wv, gw, gM, st, dev);
+    case 16: return run_bwd_noalloc<16, RADIAL>(a, want_x, want_wv, gw, gM, st, dev);
+    case 32: return run_bwd_noalloc<32, RADIAL>(a, want_x, want_wv, gw, gM, st, dev);
+    case 64: return run_bwd_noalloc<64, RADIAL>(a, want_x, want_wv, gw, gM, st, dev);
+    case 128: return run_bwd_noalloc<128, RADIAL>(a, want_x, want_wv, gw, gM, st, dev);
   }
   return EQMP_ERR_UNSUPPORTED;
 }
@@ -358,9 +365,10 @@ eqmp_status eqmp_fused_backward_noalloc(const float* vec, const float* x, int64_
   if (E > 0 && (want_x || want_wv) && (!vec || !src || !x || !aligned16(x) || N_src < 1))
     return EQMP_ERR_INVALID_ARG;
   if (radial && E > 0 && (!aligned16(weights.R) || (grad_R && !aligned16(grad_R)))) return EQMP_ERR_INVALID_ARG;
-  // Radial weights keep one scratch row of 34*C floats per edge: beyond the
-  // static array this entry point cannot run (use eqmp_fused_backward).
-  if (radial && want_wv && (size_t)E * 34 * (size_t)C * 4 > kNoAllocBytes) return EQMP_ERR_UNSUPPORTED;
+  // Radial weights keep one scratch row of 34*C floats per edge (and the
+  // dL/dM chunk partials): beyond the static array this entry point cannot
+  // run (use eqmp_fused_backward).
+  if (radial && want_wv && (size_t)radial_ws_floats(E, C) * 4 > kNoAllocBytes) return EQMP_ERR_UNSUPPORTED;
   DeviceInfo dev;
   eqmp_status s = device_info(&dev);
   if (s != EQMP_OK) return s;
@@ -368,31 +376,21 @@ eqmp_status eqmp_fused_backward_noalloc(const float* vec, const float* x, int64_
   s = noalloc_scratch(&scratch);
   if (s != EQMP_OK) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  int e0 = 0, e1 = 0;
-  if (radial && grad_M && N > 0) {
-    int h[2] = {0, 0};
-    if (cudaMemcpyAsync(&h[0], row_offsets, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-        cudaMemcpyAsync(&h[1], row_offsets + N, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-        cudaStreamSynchronize(st) != cudaSuccess)
-      return EQMP_ERR_CUDA;
-    e0 = h[0] < 0 ? 0 : (h[0] > E ? (int)E : h[0]);
-    e1 = h[1] < e0 ? e0 : (h[1] > E ? (int)E : h[1]);
-  }
   BwdArgs a{};
   a.vec = vec; a.x = x; a.off = row_offsets; a.src = src; a.dst = dst;
   a.send_off = send_offsets; a.send_edges = send_edges;
   a.w = weights.w; a.R = weights.R; a.M = weights.M; a.g = grad_out;
   a.gx = grad_x; a.gvec = grad_vec; a.gR = grad_R; a.ws = scratch;
   a.N = (int)N; a.E = (int)E; a.N_src = (int)N_src; a.n_send = (int)E_send;
-  if (radial && grad_M && e1 == e0) {
+  if (radial && grad_M && N == 0) {
     if (cudaMemsetAsync(grad_M, 0, (size_t)8 * 34 * C * 4, st) != cudaSuccess) return EQMP_ERR_CUDA;
     grad_M = nullptr;
   }
   if (!radial && grad_w && N == 0) {
     if (cudaMemsetAsync(grad_w, 0, (size_t)34 * C * 4, st) != cudaSuccess) return EQMP_ERR_CUDA;
   }
-  return radial ? dispatch_bwd_noalloc<true>(C, a, want_x, want_wv, nullptr, grad_M, e0, e1, st, dev)
-                : dispatch_bwd_noalloc<false>(C, a, want_x, want_wv, grad_w, nullptr, 0, 0, st, dev);
+  return radial ? dispatch_bwd_noalloc<true>(C, a, want_x, want_wv, nullptr, grad_M, st, dev)
+                : dispatch_bwd_noalloc<false>(C, a, want_x, want_wv, grad_w, nullptr, st, dev);
 }
 
 }  // extern "C"

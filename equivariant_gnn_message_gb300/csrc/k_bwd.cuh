@@ -146,6 +146,12 @@ struct BwdCfg {
   static constexpr int CPL = C / G;           // channels per lane
   static constexpr int NT = 128;
   static constexpr int GROUPS = NT / G;       // node groups per block
+  // Radial weights with whole-warp groups: the block's four warps share one
+  // node and take every fourth of its edges (four times the warps in
+  // flight; a node's edges are independent work, and the sender sums of
+  // dL/dx are added over the four warps in order).
+  static constexpr int SPLIT = RADIAL && G == 32 ? GROUPS : 1;
+  static constexpr int NODES = GROUPS / SPLIT;  // nodes per block at a time
 };
 
 // Weight of path P for channel c of edge e.
@@ -170,17 +176,21 @@ __device__ __forceinline__ void bx_all(const BwdArgs& a, int c, const float (&rk
 template <int C, bool RADIAL>
 __global__ void __launch_bounds__(128) k_bwd_x(const BwdArgs a) {
   using K = BwdCfg<C, RADIAL>;
+  __shared__ float xred[K::SPLIT > 1 ? K::SPLIT * 16 * 32 : 1];
   const int grp = threadIdx.x / K::G, lane = threadIdx.x % K::G;
-  for (int j = blockIdx.x * K::GROUPS + grp; j < a.N_src; j += gridDim.x * K::GROUPS) {
-    const int a0 = min(max(__ldg(a.send_off + j), 0), a.n_send);
-    const int a1 = min(max(__ldg(a.send_off + j + 1), 0), a.n_send);
+  const int node = grp / K::SPLIT, sub = grp % K::SPLIT;
+  for (int jb = blockIdx.x * K::NODES; jb < a.N_src; jb += gridDim.x * K::NODES) {  // block-uniform
+    const int j = jb + node;
+    const bool live = j < a.N_src;
+    const int a0 = live ? min(max(__ldg(a.send_off + j), 0), a.n_send) : 0;
+    const int a1 = live ? min(max(__ldg(a.send_off + j + 1), 0), a.n_send) : 0;
 #pragma unroll 1
     for (int cc = 0; cc < K::CPL; ++cc) {
       const int c = lane + cc * K::G;
       float acc[16];
 #pragma unroll
       for (int k = 0; k < 16; ++k) acc[k] = 0.0f;
-      for (int q = a0; q < a1; ++q) {
+      for (int q = a0 + sub; q < a1; q += K::SPLIT) {
         const int e = __ldg(a.send_edges + q);
         if (e < 0 || e >= a.E) continue;
         const int i = __ldg(a.dst + e);
@@ -197,9 +207,27 @@ __global__ void __launch_bounds__(128) k_bwd_x(const BwdArgs a) {
         }
         bx_all<C, RADIAL>(a, c, rk, gv, yv, acc, std::make_integer_sequence<int, tables::kNumPaths>{});
       }
-      float4* o = reinterpret_cast<float4*>(a.gx + ((size_t)j * C + c) * 16);
+      if constexpr (K::SPLIT > 1) {
+        // the warps' partial sums, added in warp order by warp 0
 #pragma unroll
-      for (int h = 0; h < 4; ++h) o[h] = make_float4(acc[4 * h], acc[4 * h + 1], acc[4 * h + 2], acc[4 * h + 3]);
+        for (int k = 0; k < 16; ++k) xred[(sub * 16 + k) * 32 + lane] = acc[k];
+        __syncthreads();
+        if (sub == 0) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            float t = xred[k * 32 + lane];
+#pragma unroll
+            for (int w = 1; w < K::SPLIT; ++w) t += xred[(w * 16 + k) * 32 + lane];
+            acc[k] = t;
+          }
+        }
+        __syncthreads();
+      }
+      if (live && sub == 0) {
+        float4* o = reinterpret_cast<float4*>(a.gx + ((size_t)j * C + c) * 16);
+#pragma unroll
+        for (int h = 0; h < 4; ++h) o[h] = make_float4(acc[4 * h], acc[4 * h + 1], acc[4 * h + 2], acc[4 * h + 3]);
+      }
     }
   }
 }
@@ -258,17 +286,22 @@ __global__ void __launch_bounds__(128) k_bwd_wv(const BwdArgs a) {
   // Every lane of a warp runs the same number of edge iterations (the
   // group-sum shuffles need the whole warp): groups whose receiver has
   // fewer edges idle through the extra ones.
+  // Radial weights (SPLIT > 1): the block's warps share a receiver and take
+  // every SPLIT-th edge; each edge's outputs are its own.
   const int warp_groups = 32 / K::G;
-  const int r_first = blockIdx.x * K::GROUPS + (grp / warp_groups) * warp_groups;
-  for (int rbase = r_first; rbase < a.N; rbase += gridDim.x * K::GROUPS) {
-    const int r = rbase + grp % warp_groups;
+  const int sub = K::SPLIT > 1 ? grp % K::SPLIT : 0;
+  const int r_first = K::SPLIT > 1 ? blockIdx.x * K::NODES + grp / K::SPLIT
+                                   : blockIdx.x * K::GROUPS + (grp / warp_groups) * warp_groups;
+  const int r_step = K::SPLIT > 1 ? gridDim.x * K::NODES : gridDim.x * K::GROUPS;
+  for (int rbase = r_first; rbase < a.N; rbase += r_step) {
+    const int r = K::SPLIT > 1 ? rbase : rbase + grp % warp_groups;
     const bool live = r < a.N;
     const int a0 = live ? min(max(__ldg(a.off + r), 0), a.E) : 0;
     const int a1 = live ? max(a0, min(max(__ldg(a.off + r + 1), 0), a.E)) : 0;
     int deg = a1 - a0;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) deg = max(deg, __shfl_xor_sync(0xffffffffu, deg, o));
-    for (int t = 0; t < deg; ++t) {
+    for (int t = sub; t < deg; t += K::SPLIT) {
       const int e = a0 + t;
       const bool on = e < a1;
       float dY[16], gr[8];
@@ -361,23 +394,50 @@ __global__ void __launch_bounds__(kRedX* kRedY) k_bwd_reduce_w(const float* ws, 
   }
 }
 
-// dL/dM[k][col] = sum over edges e in [e0, e1) of R[e][k] S[e][col].
-__global__ void __launch_bounds__(kRedX* kRedY) k_bwd_reduce_M(const float* R, const float* S, int e0, int e1,
-                                                              int cols, float* gM) {
-  __shared__ float part[kRedY][kRedX];
-  const int k = blockIdx.y;
+// dL/dM[k][col] = sum over this call's edges e of R[e][k] S[e][col], in two
+// fixed-order stages.  Stage 1 (k_bwd_partial_M): the edge range
+// [off[0], off[N]) (read on the device, clamped) is cut into kRmChunks
+// equal chunks; block (column tile, chunk) has thread (x, y) sum the edges
+// y, y+16, ... of its chunk for column x and all 8 k at once (each S entry
+// is read once), then the 16 partials are added in y order and written to
+// part[chunk][k][col].  Stage 2 (k_bwd_reduce_w over kRmChunks slots)
+// adds the chunks in order.  An empty range gives zeros.
+constexpr int kRmChunks = 16;
+
+__global__ void __launch_bounds__(kRedX* kRedY) k_bwd_partial_M(const float* __restrict__ R,
+                                                               const float* __restrict__ S,
+                                                               const int32_t* __restrict__ off, int N, int E,
+                                                               int cols, float* __restrict__ part) {
+  __shared__ float red[kRedY][8][kRedX];
   const int col = blockIdx.x * kRedX + threadIdx.x;
-  float s = 0.0f;
-  if (col < cols)
-    for (int e = e0 + threadIdx.y; e < e1; e += kRedY)
-      s = fmaf(__ldg(R + (size_t)e * 8 + k), __ldg(S + (size_t)e * cols + col), s);
-  part[threadIdx.y][threadIdx.x] = s;
+  const int chunk = blockIdx.y;
+  const int e0 = min(max(__ldg(off), 0), E);
+  const int e1 = max(e0, min(max(__ldg(off + N), 0), E));
+  const long long span = e1 - e0;
+  const int c0 = e0 + (int)(span * chunk / kRmChunks), c1 = e0 + (int)(span * (chunk + 1) / kRmChunks);
+  float acc[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
+  if (col < cols) {
+    for (int e = c0 + threadIdx.y; e < c1; e += kRedY) {
+      const float sv = __ldg(S + (size_t)e * cols + col);
+      const float4 r0 = __ldg(reinterpret_cast<const float4*>(R) + 2 * (size_t)e);
+      const float4 r1 = __ldg(reinterpret_cast<const float4*>(R) + 2 * (size_t)e + 1);
+      acc[0] = fmaf(r0.x, sv, acc[0]); acc[1] = fmaf(r0.y, sv, acc[1]);
+      acc[2] = fmaf(r0.z, sv, acc[2]); acc[3] = fmaf(r0.w, sv, acc[3]);
+      acc[4] = fmaf(r1.x, sv, acc[4]); acc[5] = fmaf(r1.y, sv, acc[5]);
+      acc[6] = fmaf(r1.z, sv, acc[6]); acc[7] = fmaf(r1.w, sv, acc[7]);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) red[threadIdx.y][k][threadIdx.x] = acc[k];
   __syncthreads();
-  if (threadIdx.y == 0 && col < cols) {
+  if (threadIdx.y < 8 && col < cols) {  // thread (x, k) adds the 16 partials of (k, col) in order
+    const int k = threadIdx.y;
     float t = 0.0f;
 #pragma unroll
-    for (int y = 0; y < kRedY; ++y) t += part[y][threadIdx.x];
-    gM[(size_t)k * cols + col] = t;
+    for (int y = 0; y < kRedY; ++y) t += red[y][k][threadIdx.x];
+    part[((size_t)chunk * 8 + k) * cols + col] = t;
   }
 }
 

@@ -209,8 +209,8 @@ eqmp_status eqmp_plan_destroy(eqmp_plan plan);
  * row_offsets/src like the forward.  workspace: device memory of at least
  * eqmp_fused_backward_workspace_size(N, E, C, radial) bytes (16-byte aligned),
  * used for the fixed-order (deterministic) weight-gradient reductions; its
- * contents on entry are ignored.  x must be fp32.  Radial grad_M reads
- * row_offsets[0] and row_offsets[N] back to the host (synchronises the stream).
+ * contents on entry are ignored.  x must be fp32.  Nothing synchronises
+ * the stream.
  */
 int64_t eqmp_fused_backward_workspace_size(int64_t N, int64_t E, int32_t C, int32_t radial);
 

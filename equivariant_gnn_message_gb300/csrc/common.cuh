@@ -60,19 +60,8 @@ __device__ __forceinline__ int split_probe(int lo, int hi, int lane) {
 // further dependent load.
 __device__ __forceinline__ int4 balanced_range_off(const int* __restrict__ off, int N, int G, int b, int alpha) {
   const int lane = threadIdx.x & 31;
-  // Round 1, all loads independent: the 32 spread probes (shared by both
-  // bounds), off[0] and off[N], and for each bound a window of 32
-  // consecutive offsets around its proportional position b N / G.  With
-  // near-uniform degrees the window holds the answer and the search ends
-  // here, one dependent load after the launch instead of two.
+  // round 1: the probes of both bounds coincide; off[0] and off[N] load with them
   const int p1 = split_probe(0, N, lane);
-  int ws[2], wv[2];
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const long long g = (long long)(b + k) * N / G - 16;
-    ws[k] = (int)min(max(g, 0ll), (long long)max(N - 31, 0));
-    wv[k] = ws[k] + lane <= N ? __ldg(off + ws[k] + lane) : 0;
-  }
   const int o_p1 = __ldg(off + p1);
   const int o0 = __ldg(off), oN = __ldg(off + N);
   const long long total = (long long)max(oN - o0, 0) + (long long)alpha * N;
@@ -87,25 +76,6 @@ __device__ __forceinline__ int4 balanced_range_off(const int* __restrict__ off, 
     ohi[k] = __shfl_sync(0xffffffffu, o_p1, f);
     const int prev = __shfl_sync(0xffffffffu, p1, f > 0 ? f - 1 : 0);
     lo[k] = f == 0 ? 0 : prev + 1;
-    // the window: the answer inside it (exact), at or before its start, or
-    // after its end; each case narrows [lo, hi] and keeps the answer in it
-    const int c = ws[k] + lane;
-    const long long wc = (long long)(wv[k] - o0) + (long long)alpha * c;
-    const unsigned gw = __ballot_sync(0xffffffffu, c <= N && (c == N || wc >= tgt[k]));
-    if (gw != 0u) {
-      const int fw = __ffs(gw) - 1;
-      const int y = ws[k] + fw;
-      const int oy = __shfl_sync(0xffffffffu, wv[k], fw);
-      if (fw > 0 || y == 0) {
-        lo[k] = hi[k] = y;
-        ohi[k] = oy;
-      } else if (y < hi[k]) {
-        hi[k] = y;
-        ohi[k] = oy;
-      }
-    } else {
-      lo[k] = max(lo[k], min(ws[k] + 31, N) + 1);
-    }
   }
   if (b == 0) { lo[0] = hi[0] = 0; ohi[0] = o0; }
   if (b == G - 1) { lo[1] = hi[1] = N; ohi[1] = oN; }

@@ -12,11 +12,11 @@ constexpr int kBwdGridPerSm = 8;
 // dw and dvec with shared weights in the forward kernel's schedule
 // (k_bwd_sw.cuh); C = 32 and 64.  One workspace row of [34][C] partial dw
 // per CTA (at most max_rows CTAs), summed in order by k_bwd_reduce_w.
-template <int C>
+template <int C, int KQ = 4, bool DW = true, bool DV = true>
 static eqmp_status launch_bwd_sw(const BwdArgs& a, float* gw, long long max_rows, cudaStream_t st,
                                  const DeviceInfo& dev) {
-  using K = BwdSwCfg<C>;
-  auto kern = k_bwd_sw<C>;
+  using K = BwdSwCfg<C, KQ, DW, DV>;
+  auto kern = k_bwd_sw<C, KQ, DW, DV>;
   static unsigned long long attr_done = 0;
   static int occ_cache[64] = {0};
   if (ensure_smem_attr(kern, K::SMEM_BYTES, &attr_done) != cudaSuccess) return EQMP_ERR_CUDA;
@@ -48,7 +48,7 @@ static eqmp_status launch_bwd_sw(const BwdArgs& a, float* gw, long long max_rows
   }
   kern<<<(int)grid, K::NTHREADS, K::SMEM_BYTES, st>>>(map, a, dev.watchdog);
   if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
-  if (gw) {
+  if (DW && gw) {
     k_bwd_reduce_w<<<(34 * C + kRedX - 1) / kRedX, dim3(kRedX, kRedY), 0, st>>>(a.ws, (int)grid, 34 * C, gw);
     if (cudaGetLastError() != cudaSuccess) return EQMP_ERR_CUDA;
   }
@@ -81,6 +81,27 @@ static long long slots_for(int C, long long N, int sms) {
     case 128: return bwd_slots<128>(N, sms);
   }
   return -1;
+}
+
+// dw and dvec with shared weights.  C = 32: one kernel forms both (KQ = 4,
+// A and H in registers together).  C = 64: dw by the forward's schedule
+// (KQ = 8, A contracted with g per receiver) and dvec by a second pass
+// (KQ = 8, H only), each with half the threads of the fused kernel; the
+// fused form at KQ = 4 spent most of its issue slots on the per-edge dY
+// reduction over its 256 threads.
+template <int C>
+static eqmp_status run_dw_dvec(const BwdArgs& a, float* gw, long long max_rows, cudaStream_t st,
+                               const DeviceInfo& dev) {
+  if constexpr (C == 64) {
+    if (gw) {
+      const eqmp_status s = launch_bwd_sw<C, 8, true, false>(a, gw, max_rows, st, dev);
+      if (s != EQMP_OK) return s;
+    }
+    if (a.gvec) return launch_bwd_sw<C, 8, false, true>(a, nullptr, max_rows, st, dev);
+    return EQMP_OK;
+  } else {
+    return launch_bwd_sw<C>(a, gw, max_rows, st, dev);
+  }
 }
 
 // Gradient of x with shared weights:
@@ -146,7 +167,7 @@ static eqmp_status run_bwd(const BwdArgs& a, bool want_x, bool want_wv, float* g
     }
   }
   if constexpr (!RADIAL && (C == 32 || C == 64)) {
-    if (want_wv && a.N > 0) return launch_bwd_sw<C>(a, gw, 1ll << 40, st, dev);
+    if (want_wv && a.N > 0) return run_dw_dvec<C>(a, gw, 1ll << 40, st, dev);
     return EQMP_OK;
   }
   if (want_wv && a.N > 0) {
@@ -298,7 +319,7 @@ static eqmp_status run_bwd_noalloc(const BwdArgs& a, bool want_x, bool want_wv, 
   }
   if constexpr (!RADIAL && (C == 32 || C == 64)) {
     if (want_wv && a.N > 0)
-      return launch_bwd_sw<C>(a, gw, (long long)(kNoAllocBytes / ((size_t)34 * C * 4)), st, dev);
+      return run_dw_dvec<C>(a, gw, (long long)(kNoAllocBytes / ((size_t)34 * C * 4)), st, dev);
     return EQMP_OK;
   }
   if (want_wv && a.N > 0) {

@@ -33,28 +33,34 @@
 
 namespace eqmp {
 
-template <int C>
+// KQ_ k1 values per thread; DW: accumulate A and form dw; DV: form H and
+// each edge's dY (dvec).  Both at KQ = 4 (A and H fit together), or one of
+// them at KQ = 8 (a kernel each, half the threads in every dY reduction).
+template <int C, int KQ_ = 4, bool DW = true, bool DV = true>
 struct BwdSwCfg {
-  using B = SharedCfg<C, 4, float, true>;
-  static constexpr int KQ = 4, NQ = B::NQ, NCONS = B::NCONS, NCW = B::NCW;
+  using B = SharedCfg<C, KQ_, float, true>;
+  static constexpr int KQ = KQ_, NQ = B::NQ, NCONS = B::NCONS, NCW = B::NCW;
   static constexpr bool WS = B::WS;
   static_assert(WS, "the shared-weight gradient kernel is warp-specialised (C >= 32)");
+  static_assert(DW || DV, "nothing to compute");
+  static_assert(KQ == 4 || !(DW && DV), "A and H together fit only at KQ = 4");
   static constexpr int CONS0 = B::CONS0, NTHREADS = B::NTHREADS, MIN_BLOCKS = B::MIN_BLOCKS;
   static constexpr int RP = B::RP, RC = B::RC, NP = B::NP, YR = B::YR, ROWS = B::ROWS;
   static constexpr int ROW_BYTES = B::ROW_BYTES, SLOT = B::SLOT, XBYTES = B::XBYTES;
   // shared memory: x slots, SH ring, dY ring [S][NCW][16] (one entry per
-  // slot), per-thread dw partials [NQ][34][C], weights [34][C], barriers
-  static constexpr int FIXED_NO_S = YR * 64 + NQ * 34 * C * 4 + 34 * C * 4 + 1024 + 1024;
-  static constexpr int PER_SLOT = SLOT + NCW * 16 * 4 + 2 * 8;
+  // slot; DV), per-thread dw partials [NQ][34][C] (DW), weights [34][C]
+  // (DV), barriers
+  static constexpr int FIXED_NO_S = YR * 64 + (DW ? NQ * 34 * C * 4 : 0) + (DV ? 34 * C * 4 : 0) + 1024 + 1024;
+  static constexpr int PER_SLOT = SLOT + (DV ? NCW * 16 * 4 : 0) + 2 * 8;
   static constexpr int S_FIT = (227 * 1024 / MIN_BLOCKS - FIXED_NO_S) / PER_SLOT;
   static constexpr int S = S_FIT >= 32 ? 32 : S_FIT >= 16 ? 16 : S_FIT >= 8 ? 8 : 4;
   static_assert(S_FIT >= 4, "not even four slots fit");
   static constexpr int OFF_X = 0;
   static constexpr int OFF_Y = OFF_X + S * SLOT;
   static constexpr int OFF_DY = OFF_Y + YR * 64;
-  static constexpr int OFF_DW = OFF_DY + S * NCW * 16 * 4;
-  static constexpr int OFF_W = OFF_DW + NQ * 34 * C * 4;
-  static constexpr int OFF_BAR = OFF_W + 34 * C * 4;
+  static constexpr int OFF_DW = OFF_DY + (DV ? S * NCW * 16 * 4 : 0);
+  static constexpr int OFF_W = OFF_DW + (DW ? NQ * 34 * C * 4 : 0);
+  static constexpr int OFF_BAR = OFF_W + (DV ? 34 * C * 4 : 0);
   static constexpr int SMEM_BYTES = OFF_BAR + 2 * S * 8 + 1024;
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
@@ -143,11 +149,27 @@ __device__ __forceinline__ void dw_quad(const float2 (&acc)[KQ][8], const float 
   (dw_path<C, KQ, Q, Ps>(acc, g, dwp), ...);
 }
 
-template <int C>
-__global__ void __launch_bounds__(BwdSwCfg<C>::NTHREADS, BwdSwCfg<C>::MIN_BLOCKS)
+// q-dispatch of a quad template (NQ = 16 / KQ quads per channel).
+template <int KQ, typename F>
+__device__ __forceinline__ void on_quad(int q, F&& f) {
+  if constexpr (KQ == 4) {
+    switch (q) {
+      case 0: f(std::integral_constant<int, 0>{}); break;
+      case 1: f(std::integral_constant<int, 1>{}); break;
+      case 2: f(std::integral_constant<int, 2>{}); break;
+      default: f(std::integral_constant<int, 3>{}); break;
+    }
+  } else {
+    if (q == 0) f(std::integral_constant<int, 0>{});
+    else f(std::integral_constant<int, 1>{});
+  }
+}
+
+template <int C, int KQ_ = 4, bool DW = true, bool DV = true>
+__global__ void __launch_bounds__(BwdSwCfg<C, KQ_, DW, DV>::NTHREADS, BwdSwCfg<C, KQ_, DW, DV>::MIN_BLOCKS)
     k_bwd_sw(const __grid_constant__ CUtensorMap tmap, const BwdArgs a, int* watchdog) {
-  using K = BwdSwCfg<C>;
-  constexpr int S = K::S, KQ = 4;
+  using K = BwdSwCfg<C, KQ_, DW, DV>;
+  constexpr int S = K::S, KQ = K::KQ;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_align<1024>(smem_raw);
   float4* ys = reinterpret_cast<float4*>(smem + K::OFF_Y);
@@ -214,7 +236,7 @@ __global__ void __launch_bounds__(BwdSwCfg<C>::NTHREADS, BwdSwCfg<C>::MIN_BLOCKS
       a.gvec[3 * (size_t)e + 1] = oy;
       a.gvec[3 * (size_t)e + 2] = oz;
     };
-    const bool want_vec = a.gvec != nullptr;
+    const bool want_vec = DV && a.gvec != nullptr;
     bool ok = true;
     int node_nx;
     float vx_nx, vy_nx, vz_nx;
@@ -287,7 +309,7 @@ __global__ void __launch_bounds__(BwdSwCfg<C>::NTHREADS, BwdSwCfg<C>::MIN_BLOCKS
   setmaxnreg_inc<K::RC>();
   const int ct = tid - K::CONS0;
   const int c = ct % C, q = ct / C, lane = tid & 31, cw = ct >> 5;
-  {
+  if constexpr (DV) {
     constexpr int PER = (34 * C + K::NCONS - 1) / K::NCONS;
     float wv[PER];
 #pragma unroll
@@ -315,8 +337,10 @@ __global__ void __launch_bounds__(BwdSwCfg<C>::NTHREADS, BwdSwCfg<C>::MIN_BLOCKS
   uint32_t n = 0;
   bool failed = false;
   float* dwp = dwq + (size_t)q * 34 * C + c;  // this thread's partials, path p at dwp[p * C]
+  if constexpr (DW) {
 #pragma unroll
-  for (int p = 0; p < 34; ++p) dwp[p * C] = 0.0f;
+    for (int p = 0; p < 34; ++p) dwp[p * C] = 0.0f;
+  }
 
   auto full_bar = [&](uint32_t m) { return full0 + 8 * (m % S); };
   auto full_par = [&](uint32_t m) { return (m / S) & 1u; };
@@ -339,7 +363,11 @@ __global__ void __launch_bounds__(BwdSwCfg<C>::NTHREADS, BwdSwCfg<C>::MIN_BLOCKS
   // then release the slot.
   auto edge = [&](float2 (&acc)[KQ][8], const float2 (&H)[KQ][8], uint32_t m, const float2 (&yv)[8],
                   const float (&xv)[KQ]) {
-    fma_edge<KQ>(acc, yv, xv);
+    if constexpr (DW) fma_edge<KQ>(acc, yv, xv);
+    if constexpr (!DV) {
+      mbar_arrive(empty0 + 8 * (m % S));
+      return;
+    }
     float2 dy[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) dy[k] = make_float2(0.0f, 0.0f);
@@ -395,24 +423,23 @@ __global__ void __launch_bounds__(BwdSwCfg<C>::NTHREADS, BwdSwCfg<C>::MIN_BLOCKS
       }
     };
     float g[16];
-    load_g(g);
     float2 H[KQ][8];
-#pragma unroll
-    for (int i = 0; i < KQ; ++i)
-#pragma unroll
-      for (int k = 0; k < 8; ++k) H[i][k] = make_float2(0.0f, 0.0f);
     using Seq = std::make_integer_sequence<int, tables::kNumPaths>;
-    switch (q) {
-      case 0: h_quad<C, KQ, 0>(g, wcol, H, Seq{}); break;
-      case 1: h_quad<C, KQ, 1>(g, wcol, H, Seq{}); break;
-      case 2: h_quad<C, KQ, 2>(g, wcol, H, Seq{}); break;
-      default: h_quad<C, KQ, 3>(g, wcol, H, Seq{}); break;
+    if constexpr (DV) {
+      load_g(g);
+#pragma unroll
+      for (int i = 0; i < KQ; ++i)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) H[i][k] = make_float2(0.0f, 0.0f);
+      on_quad<KQ>(q, [&](auto Qc) { h_quad<C, KQ, decltype(Qc)::value>(g, wcol, H, Seq{}); });
     }
     float2 acc[KQ][8];
+    if constexpr (DW) {
 #pragma unroll
-    for (int i = 0; i < KQ; ++i)
+      for (int i = 0; i < KQ; ++i)
 #pragma unroll
-      for (int k = 0; k < 8; ++k) acc[i][k] = make_float2(0.0f, 0.0f);
+        for (int k = 0; k < 8; ++k) acc[i][k] = make_float2(0.0f, 0.0f);
+    }
     int j = 0;
     for (; j + 2 <= deg; j += 2, n += 2) {
       {
@@ -439,14 +466,12 @@ __global__ void __launch_bounds__(BwdSwCfg<C>::NTHREADS, BwdSwCfg<C>::MIN_BLOCKS
       load_edge(n + 2, yB, xB);
       ++n;
     }
-    load_g(g);
-    switch (q) {
-      case 0: dw_quad<C, KQ, 0>(acc, g, dwp, Seq{}); break;
-      case 1: dw_quad<C, KQ, 1>(acc, g, dwp, Seq{}); break;
-      case 2: dw_quad<C, KQ, 2>(acc, g, dwp, Seq{}); break;
-      default: dw_quad<C, KQ, 3>(acc, g, dwp, Seq{}); break;
+    if constexpr (DW) {
+      load_g(g);
+      on_quad<KQ>(q, [&](auto Qc) { dw_quad<C, KQ, decltype(Qc)::value>(acc, g, dwp, Seq{}); });
     }
   }
+  if constexpr (!DW) return;
   // quad partials -> one workspace row [34][C] per CTA, quads added in order
   named_barrier(1, K::NCONS);
   float* row = a.ws + (size_t)blockIdx.x * 34 * C;

@@ -45,6 +45,9 @@ WORKLOADS = {
     "radial_1k_c32":  dict(n_atoms=1000, cutoff=5.0, channels=32, weights="radial", storage="f32", seed=3),
     "scale_100k_c64": dict(n_atoms=100_000, cutoff=5.0, channels=64, weights="shared", storage="f32", seed=4),
     "dense_10k_c128_bf16": dict(n_atoms=10_000, cutoff=7.0, channels=128, weights="shared", storage="bf16", seed=5),
+    # a quarter of the scale workload (same density, cutoff and channels): the
+    # size for multi-pass profiler captures of the C = 64 kernels (x 102 MB)
+    "scale_25k_c64":  dict(n_atoms=25_000, cutoff=5.0, channels=64, weights="shared", storage="f32", seed=7),
     # the scale workload's atoms and features, renumbered in Morton order of their cells
     "scale_100k_c64_morton": dict(n_atoms=100_000, cutoff=5.0, channels=64, weights="shared", storage="f32", seed=4,
                                   order="morton"),

@@ -55,6 +55,13 @@ constexpr int kScanTile = kScanThreads * kScanItems;
 constexpr int kNeighThreads = 256;
 constexpr int kSortWarps = 8;
 constexpr int kSortCap = 512;          // row length sorted in shared memory
+// Walk modes of the neighbour pass (neigh_row) and the per-row scratch of
+// the single-walk path: rows up to kRowScratch senders are kept from the
+// counting walk, longer ones are walked again.  Used up to kScratchMaxAtoms
+// (the scratch is kRowScratch ints per atom).
+constexpr int kWalkCount = 0, kWalkFill = 1, kWalkScratch = 2, kWalkFixup = 3;
+constexpr int kRowScratch = 48;
+constexpr long long kScratchMaxAtoms = 1ll << 22;
 constexpr float kCellRange = 4096.0f;  // |p| / cell side must stay below this
 constexpr long long kGraphMaxAtoms = 1ll << 30;  // keeps the bucket count <= 2^31
 constexpr long long kGraphMaxAtomsPbc = 1ll << 26;  // keys sender * 27 + image stay below 2^31
@@ -276,17 +283,23 @@ __global__ void k_scatter(const float* __restrict__ pos, int N, const int32_t* _
 // its lowest lane); the warp then walks the concatenation of those buckets,
 // one candidate per lane per round, finding each candidate's bucket by a
 // binary search over the lanes' running sizes.
-// FILL = false: row_offsets[i] = degree of i (row_offsets[N] = 0).
-// FILL = true:  senders of i written, unsorted, to src[off[i] .. off[i+1]).
+// MODE kWalkCount:   row_offsets[i] = degree of i (row_offsets[N] = 0).
+// MODE kWalkFill:    senders of i written, unsorted, to src[off[i] .. off[i+1]).
+// MODE kWalkScratch: the count of kWalkCount, and the first kRowScratch
+//                    senders (in walk order) into cand[i * kRowScratch ..],
+//                    so that rows that fit need no second walk.
+// MODE kWalkFixup:   kWalkFill for the rows longer than kRowScratch only
+//                    (row_offsets already scanned); the others return at once.
 // PBC: each lane names a (wrapped cell, image) pair; duplicates are merged
 // on (bucket, image); a candidate is tested with its lane's image shift and
 // the fill writes sender * 27 + image.
-template <bool FILL, bool PBC>
+template <int MODE, bool PBC>
 __device__ __forceinline__ void neigh_row(long long wg, int lane, const float4* __restrict__ bucket_pos, float inv,
                                           float rc2, uint32_t mask, const int32_t* __restrict__ start,
                                           const int32_t* __restrict__ bucket_atoms,
                                           int32_t* __restrict__ row_offsets, int32_t* __restrict__ src,
-                                          long long e_cap, const Box& box) {
+                                          long long e_cap, const Box& box, int32_t* __restrict__ cand = nullptr) {
+  constexpr bool FILL = MODE == kWalkFill || MODE == kWalkFixup;
   const int i = bucket_atoms[wg];  // the receiver sits at slot wg of the bucket order
   const float4 pw = bucket_pos[wg];
   const float3 pi = make_float3(pw.x, pw.y, pw.z);
@@ -295,6 +308,7 @@ __device__ __forceinline__ void neigh_row(long long wg, int lane, const float4* 
     w = row_offsets[i];
     w_end = row_offsets[i + 1];
     if (w < 0 || w_end > e_cap || w_end < w) return;  // row outside the caller's capacity
+    if (MODE == kWalkFixup && w_end - w <= kRowScratch) return;  // the scratch walk has this row
   }
   uint32_t h;
   int sigma = kSelfImage;  // this lane's image (PBC)
@@ -361,23 +375,31 @@ __device__ __forceinline__ void neigh_row(long long wg, int lane, const float4* 
       if (hit && at < w_end) src[at] = PBC ? bucket_atoms[slot] * kImages + lsig : bucket_atoms[slot];
       w += __popc(bal);
     } else {
+      if (MODE == kWalkScratch) {
+        const int at = count + __popc(bal & ((1u << lane) - 1u));
+        if (hit && at < kRowScratch)
+          cand[(size_t)i * kRowScratch + at] = PBC ? bucket_atoms[slot] * kImages + lsig : bucket_atoms[slot];
+      }
       count += __popc(bal);
     }
   }
   if (!FILL && lane == 0) row_offsets[i] = count;
 }
 
-template <bool FILL, bool PBC>
+template <int MODE, bool PBC>
 __global__ void __launch_bounds__(kNeighThreads) k_neigh(const float4* __restrict__ bucket_pos, int N, float inv,
                                                          float rc2, uint32_t mask, const int32_t* __restrict__ start,
                                                          const int32_t* __restrict__ bucket_atoms,
                                                          int32_t* __restrict__ row_offsets,
-                                                         int32_t* __restrict__ src, long long e_cap, const Box box) {
+                                                         int32_t* __restrict__ src, long long e_cap, const Box box,
+                                                         int32_t* __restrict__ cand) {
+  constexpr bool FILL = MODE == kWalkFill || MODE == kWalkFixup;
   const int lane = threadIdx.x & 31;
   const long long wg = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (!FILL && wg == 0 && lane == 0) row_offsets[N] = 0;
   if (wg < N)
-    neigh_row<FILL, PBC>(wg, lane, bucket_pos, inv, rc2, mask, start, bucket_atoms, row_offsets, src, e_cap, box);
+    neigh_row<MODE, PBC>(wg, lane, bucket_pos, inv, rc2, mask, start, bucket_atoms, row_offsets, src, e_cap, box,
+                         cand);
 }
 
 // ------------------------------------------------------------ row sort
@@ -411,18 +433,22 @@ __device__ __forceinline__ void put_edge(long long e, int key, int i, float3 pi,
   if (dst) dst[e] = i;
 }
 
+// cand (single-walk path): rows of at most kRowScratch senders come from
+// the counting walk's scratch row instead of src.
 template <bool PBC>
 __device__ __forceinline__ void sort_row(int i, int lane, int32_t* sm, const float* __restrict__ pos,
                                          const int32_t* __restrict__ row_offsets, int32_t* __restrict__ src,
                                          int32_t* __restrict__ img, float* __restrict__ vec,
-                                         int32_t* __restrict__ dst, long long e_cap, const Box& box) {
+                                         int32_t* __restrict__ dst, long long e_cap, const Box& box,
+                                         const int32_t* __restrict__ cand = nullptr) {
   const long long beg = row_offsets[i], end = row_offsets[i + 1];
   if (beg < 0 || end > e_cap || end < beg) return;
   const int k = (int)(end - beg);
   const float3 pi = load_pos(pos, i);
   int32_t* row = src + beg;
+  const int32_t* from = cand && k <= kRowScratch ? cand + (size_t)i * kRowScratch : row;
   if (k <= kSortCap) {
-    for (int a = lane; a < k; a += 32) sm[a] = row[a];
+    for (int a = lane; a < k; a += 32) sm[a] = from[a];
     __syncwarp();
     for (int a = lane; a < k; a += 32) {
       const int v = sm[a];
@@ -450,11 +476,12 @@ __global__ void __launch_bounds__(kSortWarps * 32) k_sort(const float* __restric
                                                           const int32_t* __restrict__ row_offsets,
                                                           int32_t* __restrict__ src, int32_t* __restrict__ img,
                                                           float* __restrict__ vec, int32_t* __restrict__ dst,
-                                                          long long e_cap, const Box box) {
+                                                          long long e_cap, const Box box,
+                                                          const int32_t* __restrict__ cand) {
   __shared__ int32_t rows[kSortWarps][kSortCap];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int i = blockIdx.x * kSortWarps + wid;
-  if (i < N) sort_row<PBC>(i, lane, rows[wid], pos, row_offsets, src, img, vec, dst, e_cap, box);
+  if (i < N) sort_row<PBC>(i, lane, rows[wid], pos, row_offsets, src, img, vec, dst, e_cap, box, cand);
 }
 
 // rev[e] for e = (i <- j): the position of (j <- i) in row j (binary search;
@@ -616,13 +643,13 @@ __global__ void __launch_bounds__(kSortWarps * 32) k_graph_coop(const CoopArgs g
   if (!grid_sync(g.bar, gen, g.watchdog)) return;
   if (tid == 0) g.row_offsets[g.N] = 0;
   for (long long w = warp0; w < g.N; w += nwarps)
-    neigh_row<false, PBC>(w, lane, g.bucket_pos, g.inv, g.rc2, g.mask, g.start, g.bucket_atoms, g.row_offsets,
+    neigh_row<kWalkCount, PBC>(w, lane, g.bucket_pos, g.inv, g.rc2, g.mask, g.start, g.bucket_atoms, g.row_offsets,
                           nullptr, g.e_cap, g.box);
   if (!grid_sync(g.bar, gen, g.watchdog)) return;
   if (!grid_scan(g.row_offsets, (long long)g.N + 1, g.sums, g.bar, gen, g.watchdog, g.bad, g.e_total)) return;
   if (g.e_cap <= 0) return;
   for (long long w = warp0; w < g.N; w += nwarps)
-    neigh_row<true, PBC>(w, lane, g.bucket_pos, g.inv, g.rc2, g.mask, g.start, g.bucket_atoms, g.row_offsets,
+    neigh_row<kWalkFill, PBC>(w, lane, g.bucket_pos, g.inv, g.rc2, g.mask, g.start, g.bucket_atoms, g.row_offsets,
                          g.src, g.e_cap, g.box);
   if (!grid_sync(g.bar, gen, g.watchdog)) return;
   for (long long i = warp0; i < g.N; i += nwarps)
@@ -637,7 +664,8 @@ __global__ void __launch_bounds__(kSortWarps * 32) k_graph_coop(const CoopArgs g
 struct GraphWs {
   long long H = 0;
   size_t atom_bucket = 0, start = 0, fill = 0, bucket_atoms = 0, bucket_pos = 0, sums = 0, bad = 0, coop = 0,
-         bytes = 0;
+         cand = 0, bytes = 0;
+  bool scratch = false;  // the single-walk path's per-row scratch is present
 };
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -658,6 +686,9 @@ GraphWs graph_ws(long long N) {
   w.sums = o;        o = align256(o + 8 * (size_t)nb);
   w.bad = o;         o = align256(o + 4);
   w.coop = o;        o = align256(o + 8 * (size_t)kCoopMaxBlocks + 16);  // block totals + barrier words
+  // single-walk scratch rows (multi-kernel path above the single launch's size)
+  w.scratch = N > kCoopMaxAtoms && N <= kScratchMaxAtoms;
+  w.cand = o;        o = align256(o + (w.scratch ? 4 * (size_t)kRowScratch * (size_t)N : 0));
   w.bytes = o;
   return w;
 }
@@ -755,16 +786,28 @@ eqmp_status radius_graph_run(const float* pos, int64_t N, float cutoff, const Bo
   if (err != cudaSuccess) return EQMP_ERR_CUDA;
   if (N > 0)
     k_scatter<<<nblk, kNeighThreads, 0, st>>>(pos, (int)N, atom_bucket, start, fill, bucket_atoms, bucket_pos);
+  // One walk counts each row and keeps its first kRowScratch senders; after
+  // the scan a second walk fills only the rows longer than that (without the
+  // scratch: a counting walk, then a filling walk of every row).
   const long long wblk = (N * 32 + kNeighThreads - 1) / kNeighThreads;  // one warp per receiver
-  k_neigh<false, PBC><<<(unsigned)(wblk > 0 ? wblk : 1), kNeighThreads, 0, st>>>(
-      bucket_pos, (int)N, inv, rc2, mask, start, bucket_atoms, row_offsets, nullptr, E_cap, box);
+  int32_t* cand = w.scratch ? reinterpret_cast<int32_t*>(base + w.cand) : nullptr;
+  if (cand)
+    k_neigh<kWalkScratch, PBC><<<(unsigned)(wblk > 0 ? wblk : 1), kNeighThreads, 0, st>>>(
+        bucket_pos, (int)N, inv, rc2, mask, start, bucket_atoms, row_offsets, nullptr, E_cap, box, cand);
+  else
+    k_neigh<kWalkCount, PBC><<<(unsigned)(wblk > 0 ? wblk : 1), kNeighThreads, 0, st>>>(
+        bucket_pos, (int)N, inv, rc2, mask, start, bucket_atoms, row_offsets, nullptr, E_cap, box, nullptr);
   err = exclusive_scan(row_offsets, N + 1, sums, bad, reinterpret_cast<long long*>(E_total), st);
   if (err != cudaSuccess) return EQMP_ERR_CUDA;
   if (N > 0 && E_cap > 0) {
-    k_neigh<true, PBC><<<(unsigned)wblk, kNeighThreads, 0, st>>>(bucket_pos, (int)N, inv, rc2, mask, start,
-                                                                 bucket_atoms, row_offsets, src, E_cap, box);
+    if (cand)
+      k_neigh<kWalkFixup, PBC><<<(unsigned)wblk, kNeighThreads, 0, st>>>(
+          bucket_pos, (int)N, inv, rc2, mask, start, bucket_atoms, row_offsets, src, E_cap, box, nullptr);
+    else
+      k_neigh<kWalkFill, PBC><<<(unsigned)wblk, kNeighThreads, 0, st>>>(
+          bucket_pos, (int)N, inv, rc2, mask, start, bucket_atoms, row_offsets, src, E_cap, box, nullptr);
     const int sblk = (int)((N + kSortWarps - 1) / kSortWarps);
-    k_sort<PBC><<<sblk, kSortWarps * 32, 0, st>>>(pos, (int)N, row_offsets, src, img, vec, dst, E_cap, box);
+    k_sort<PBC><<<sblk, kSortWarps * 32, 0, st>>>(pos, (int)N, row_offsets, src, img, vec, dst, E_cap, box, cand);
     if (rev) k_rev<PBC><<<sblk, kSortWarps * 32, 0, st>>>((int)N, row_offsets, src, img, rev, E_cap);
   }
   return cuda_status(cudaGetLastError());

@@ -60,8 +60,8 @@ constexpr int kSortCap = 512;          // row length sorted in shared memory
 // counting walk, longer ones are walked again.  Used up to kScratchMaxAtoms
 // (the scratch is kRowScratch ints per atom).
 constexpr int kWalkCount = 0, kWalkFill = 1, kWalkScratch = 2, kWalkFixup = 3;
-constexpr int kRowScratch = 48;
-constexpr long long kScratchMaxAtoms = 1ll << 22;
+constexpr int kRowScratch = 96;
+constexpr long long kScratchMaxAtoms = 1ll << 21;
 constexpr float kCellRange = 4096.0f;  // |p| / cell side must stay below this
 constexpr long long kGraphMaxAtoms = 1ll << 30;  // keeps the bucket count <= 2^31
 constexpr long long kGraphMaxAtomsPbc = 1ll << 26;  // keys sender * 27 + image stay below 2^31
@@ -541,6 +541,7 @@ struct CoopArgs {
   long long* e_total;
   int* watchdog;
   Box box;  // periodic box (k_graph_coop<true>)
+  int32_t* cand;  // per-row scratch of the single walk, or nullptr
 };
 
 // Grid barrier with a bounded wait: false (and the watchdog set) if the
@@ -642,18 +643,31 @@ __global__ void __launch_bounds__(kSortWarps * 32) k_graph_coop(const CoopArgs g
     scatter_one((int)i, g.pos, g.atom_bucket, g.start, g.fill, g.bucket_atoms, g.bucket_pos);
   if (!grid_sync(g.bar, gen, g.watchdog)) return;
   if (tid == 0) g.row_offsets[g.N] = 0;
-  for (long long w = warp0; w < g.N; w += nwarps)
-    neigh_row<kWalkCount, PBC>(w, lane, g.bucket_pos, g.inv, g.rc2, g.mask, g.start, g.bucket_atoms, g.row_offsets,
-                          nullptr, g.e_cap, g.box);
+  // one walk counts each row and keeps its first kRowScratch senders; the
+  // second walk fills only longer rows (see radius_graph_run)
+  for (long long w = warp0; w < g.N; w += nwarps) {
+    if (g.cand)
+      neigh_row<kWalkScratch, PBC>(w, lane, g.bucket_pos, g.inv, g.rc2, g.mask, g.start, g.bucket_atoms,
+                                   g.row_offsets, nullptr, g.e_cap, g.box, g.cand);
+    else
+      neigh_row<kWalkCount, PBC>(w, lane, g.bucket_pos, g.inv, g.rc2, g.mask, g.start, g.bucket_atoms,
+                                 g.row_offsets, nullptr, g.e_cap, g.box);
+  }
   if (!grid_sync(g.bar, gen, g.watchdog)) return;
   if (!grid_scan(g.row_offsets, (long long)g.N + 1, g.sums, g.bar, gen, g.watchdog, g.bad, g.e_total)) return;
   if (g.e_cap <= 0) return;
-  for (long long w = warp0; w < g.N; w += nwarps)
-    neigh_row<kWalkFill, PBC>(w, lane, g.bucket_pos, g.inv, g.rc2, g.mask, g.start, g.bucket_atoms, g.row_offsets,
-                         g.src, g.e_cap, g.box);
+  for (long long w = warp0; w < g.N; w += nwarps) {
+    if (g.cand)
+      neigh_row<kWalkFixup, PBC>(w, lane, g.bucket_pos, g.inv, g.rc2, g.mask, g.start, g.bucket_atoms,
+                                 g.row_offsets, g.src, g.e_cap, g.box);
+    else
+      neigh_row<kWalkFill, PBC>(w, lane, g.bucket_pos, g.inv, g.rc2, g.mask, g.start, g.bucket_atoms,
+                                g.row_offsets, g.src, g.e_cap, g.box);
+  }
   if (!grid_sync(g.bar, gen, g.watchdog)) return;
   for (long long i = warp0; i < g.N; i += nwarps)
-    sort_row<PBC>((int)i, lane, rows[wid], g.pos, g.row_offsets, g.src, g.img, g.vec, g.dst, g.e_cap, g.box);
+    sort_row<PBC>((int)i, lane, rows[wid], g.pos, g.row_offsets, g.src, g.img, g.vec, g.dst, g.e_cap, g.box,
+                  g.cand);
   if (!g.rev) return;
   if (!grid_sync(g.bar, gen, g.watchdog)) return;
   for (long long i = warp0; i < g.N; i += nwarps)
@@ -686,8 +700,8 @@ GraphWs graph_ws(long long N) {
   w.sums = o;        o = align256(o + 8 * (size_t)nb);
   w.bad = o;         o = align256(o + 4);
   w.coop = o;        o = align256(o + 8 * (size_t)kCoopMaxBlocks + 16);  // block totals + barrier words
-  // single-walk scratch rows (multi-kernel path above the single launch's size)
-  w.scratch = N > kCoopMaxAtoms && N <= kScratchMaxAtoms;
+  // single-walk scratch rows
+  w.scratch = N <= kScratchMaxAtoms;
   w.cand = o;        o = align256(o + (w.scratch ? 4 * (size_t)kRowScratch * (size_t)N : 0));
   w.bytes = o;
   return w;
@@ -769,6 +783,7 @@ eqmp_status radius_graph_run(const float* pos, int64_t N, float cutoff, const Bo
       g.e_total = reinterpret_cast<long long*>(E_total);
       g.watchdog = dev.watchdog;
       g.box = box;
+      g.cand = w.scratch ? reinterpret_cast<int32_t*>(base + w.cand) : nullptr;
       if (cudaMemsetAsync(g.bar, 0, 2 * sizeof(unsigned), st) != cudaSuccess) return EQMP_ERR_CUDA;
       void* params[] = {&g};
       const cudaError_t err = cudaLaunchCooperativeKernel((const void*)k_graph_coop<PBC>, dim3((unsigned)grid),

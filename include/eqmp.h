@@ -320,10 +320,10 @@ eqmp_status eqmp_fused_lmax(int32_t l_max, const float* vec, const float* x, int
  *                still valid but src/vec/dst/rev are unspecified: allocate
  *                E edges and call again.
  *   workspace    device memory, 256-byte aligned, of at least
- *                eqmp_radius_graph_workspace_size(N) bytes (about 40 N
- *                bytes, plus 192 N bytes of per-row scratch for
- *                16,384 < N <= 2^22); owned by the caller; no other call may
- *                use it until this one completes.
+ *                eqmp_radius_graph_workspace_size(N) bytes (40 to 56 N
+ *                bytes, plus 384 N bytes of per-row scratch for
+ *                N <= 2^21); owned by the caller; no other call may use it
+ *                until this one completes.
  * N up to 2^30 (EQMP_ERR_UNSUPPORTED above).  Asynchronous on `stream`; no
  * host synchronisation.  Cost is linear in N for bounded density; a row
  * longer than 512 edges is sorted in time quadratic in its length.

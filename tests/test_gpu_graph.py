@@ -59,17 +59,17 @@ def test_workload_graphs_bit_exact(eq, name):
 
 
 def test_rows_past_the_scratch_length(eq):
-    """Above the single launch's size the walk keeps rows of up to 48 senders
-    and walks again for longer ones: a dense 20,000-atom box (cutoff 7,
-    about 48 neighbours, so rows on both sides of the length) and a box with
-    a crowded corner (rows of a few hundred)."""
+    """The first walk keeps rows of up to 96 senders and the second walks
+    again for longer ones: a dense 20,000-atom box at cutoff 9 (about 100
+    neighbours, so rows on both sides of the length) and a box with a crowded
+    corner (rows of a few hundred)."""
     rng = np.random.default_rng(23)
     n = 20_000
     side = (n / DENSITY) ** (1 / 3)
     pos = rng.uniform(0, side, (n, 3)).astype(np.float32)
-    got = _same(eq, pos, 7.0)
+    got = _same(eq, pos, 9.0)
     deg = np.diff(got["off"])
-    assert (deg <= 48).any() and (deg > 48).any()
+    assert (deg <= 96).any() and (deg > 96).any()
     pos2 = pos.copy()
     pos2[:600] = rng.uniform(0, 4.0, (600, 3)).astype(np.float32)
     got2 = _same(eq, pos2, 5.0)

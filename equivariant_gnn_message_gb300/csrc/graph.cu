@@ -59,7 +59,7 @@ constexpr int kSortCap = 512;          // row length sorted in shared memory
 // the single-walk path: rows up to kRowScratch senders are kept from the
 // counting walk, longer ones are walked again.  Used up to kScratchMaxAtoms
 // (the scratch is kRowScratch ints per atom).
-constexpr int kWalkCount = 0, kWalkFill = 1, kWalkScratch = 2, kWalkFixup = 3;
+constexpr int kWalkCount = 0, kWalkFill = 1, kWalkScratch = 2;
 constexpr int kRowScratch = 96;
 constexpr long long kScratchMaxAtoms = 1ll << 21;
 constexpr float kCellRange = 4096.0f;  // |p| / cell side must stay below this
@@ -288,8 +288,7 @@ __global__ void k_scatter(const float* __restrict__ pos, int N, const int32_t* _
 // MODE kWalkScratch: the count of kWalkCount, and the first kRowScratch
 //                    senders (in walk order) into cand[i * kRowScratch ..],
 //                    so that rows that fit need no second walk.
-// MODE kWalkFixup:   kWalkFill for the rows longer than kRowScratch only
-//                    (row_offsets already scanned); the others return at once.
+// (The rows longer than kRowScratch are filled afterwards by fixup_rows.)
 // PBC: each lane names a (wrapped cell, image) pair; duplicates are merged
 // on (bucket, image); a candidate is tested with its lane's image shift and
 // the fill writes sender * 27 + image.
@@ -299,7 +298,7 @@ __device__ __forceinline__ void neigh_row(long long wg, int lane, const float4* 
                                           const int32_t* __restrict__ bucket_atoms,
                                           int32_t* __restrict__ row_offsets, int32_t* __restrict__ src,
                                           long long e_cap, const Box& box, int32_t* __restrict__ cand = nullptr) {
-  constexpr bool FILL = MODE == kWalkFill || MODE == kWalkFixup;
+  constexpr bool FILL = MODE == kWalkFill;
   const int i = bucket_atoms[wg];  // the receiver sits at slot wg of the bucket order
   const float4 pw = bucket_pos[wg];
   const float3 pi = make_float3(pw.x, pw.y, pw.z);
@@ -308,7 +307,6 @@ __device__ __forceinline__ void neigh_row(long long wg, int lane, const float4* 
     w = row_offsets[i];
     w_end = row_offsets[i + 1];
     if (w < 0 || w_end > e_cap || w_end < w) return;  // row outside the caller's capacity
-    if (MODE == kWalkFixup && w_end - w <= kRowScratch) return;  // the scratch walk has this row
   }
   uint32_t h;
   int sigma = kSelfImage;  // this lane's image (PBC)
@@ -393,13 +391,48 @@ __global__ void __launch_bounds__(kNeighThreads) k_neigh(const float4* __restric
                                                          int32_t* __restrict__ row_offsets,
                                                          int32_t* __restrict__ src, long long e_cap, const Box box,
                                                          int32_t* __restrict__ cand) {
-  constexpr bool FILL = MODE == kWalkFill || MODE == kWalkFixup;
+  constexpr bool FILL = MODE == kWalkFill;
   const int lane = threadIdx.x & 31;
   const long long wg = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (!FILL && wg == 0 && lane == 0) row_offsets[N] = 0;
   if (wg < N)
     neigh_row<MODE, PBC>(wg, lane, bucket_pos, inv, rc2, mask, start, bucket_atoms, row_offsets, src, e_cap, box,
                          cand);
+}
+
+// Second walk of the single-walk path: thread t checks the receiver at slot
+// t of the bucket order, and its warp walks together (kWalkFill) each of
+// its 32 receivers whose row is longer than the scratch row.
+template <bool PBC>
+__device__ __forceinline__ void fixup_rows(long long base, int lane, long long n, const float4* __restrict__ bucket_pos,
+                                           float inv, float rc2, uint32_t mask, const int32_t* __restrict__ start,
+                                           const int32_t* __restrict__ bucket_atoms,
+                                           int32_t* __restrict__ row_offsets, int32_t* __restrict__ src,
+                                           long long e_cap, const Box& box) {
+  const long long wg = base + lane;
+  bool longer = false;
+  if (wg < n) {
+    const int i = bucket_atoms[wg];
+    longer = (long long)row_offsets[i + 1] - row_offsets[i] > kRowScratch;
+  }
+  unsigned todo = __ballot_sync(0xffffffffu, longer);
+  while (todo) {
+    const int l = __ffs(todo) - 1;
+    todo &= todo - 1;
+    neigh_row<kWalkFill, PBC>(base + l, lane, bucket_pos, inv, rc2, mask, start, bucket_atoms, row_offsets, src,
+                              e_cap, box);
+  }
+}
+
+template <bool PBC>
+__global__ void __launch_bounds__(kNeighThreads) k_fixup(const float4* __restrict__ bucket_pos, int N, float inv,
+                                                         float rc2, uint32_t mask, const int32_t* __restrict__ start,
+                                                         const int32_t* __restrict__ bucket_atoms,
+                                                         int32_t* __restrict__ row_offsets,
+                                                         int32_t* __restrict__ src, long long e_cap, const Box box) {
+  const long long base = ((long long)blockIdx.x * blockDim.x + threadIdx.x) & ~31ll;
+  fixup_rows<PBC>(base, threadIdx.x & 31, N, bucket_pos, inv, rc2, mask, start, bucket_atoms, row_offsets, src,
+                  e_cap, box);
 }
 
 // ------------------------------------------------------------ row sort
@@ -656,11 +689,12 @@ __global__ void __launch_bounds__(kSortWarps * 32) k_graph_coop(const CoopArgs g
   if (!grid_sync(g.bar, gen, g.watchdog)) return;
   if (!grid_scan(g.row_offsets, (long long)g.N + 1, g.sums, g.bar, gen, g.watchdog, g.bad, g.e_total)) return;
   if (g.e_cap <= 0) return;
-  for (long long w = warp0; w < g.N; w += nwarps) {
-    if (g.cand)
-      neigh_row<kWalkFixup, PBC>(w, lane, g.bucket_pos, g.inv, g.rc2, g.mask, g.start, g.bucket_atoms,
-                                 g.row_offsets, g.src, g.e_cap, g.box);
-    else
+  if (g.cand) {
+    for (long long b = warp0 * 32; b < g.N; b += nwarps * 32)
+      fixup_rows<PBC>(b, lane, g.N, g.bucket_pos, g.inv, g.rc2, g.mask, g.start, g.bucket_atoms, g.row_offsets,
+                      g.src, g.e_cap, g.box);
+  } else {
+    for (long long w = warp0; w < g.N; w += nwarps)
       neigh_row<kWalkFill, PBC>(w, lane, g.bucket_pos, g.inv, g.rc2, g.mask, g.start, g.bucket_atoms,
                                 g.row_offsets, g.src, g.e_cap, g.box);
   }
@@ -816,8 +850,8 @@ eqmp_status radius_graph_run(const float* pos, int64_t N, float cutoff, const Bo
   if (err != cudaSuccess) return EQMP_ERR_CUDA;
   if (N > 0 && E_cap > 0) {
     if (cand)
-      k_neigh<kWalkFixup, PBC><<<(unsigned)wblk, kNeighThreads, 0, st>>>(
-          bucket_pos, (int)N, inv, rc2, mask, start, bucket_atoms, row_offsets, src, E_cap, box, nullptr);
+      k_fixup<PBC><<<(unsigned)((N + kNeighThreads - 1) / kNeighThreads), kNeighThreads, 0, st>>>(
+          bucket_pos, (int)N, inv, rc2, mask, start, bucket_atoms, row_offsets, src, E_cap, box);
     else
       k_neigh<kWalkFill, PBC><<<(unsigned)wblk, kNeighThreads, 0, st>>>(
           bucket_pos, (int)N, inv, rc2, mask, start, bucket_atoms, row_offsets, src, E_cap, box, nullptr);

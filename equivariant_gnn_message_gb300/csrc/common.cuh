@@ -24,7 +24,8 @@ namespace eqmp {
 // device); kernels receive its address.  It becomes nonzero once any
 // bounded wait has given up and is read and cleared by eqmp_device_error().
 // Codes: 1 consumer full-wait, 2 producer empty-wait, 3 producer drain,
-// 4 grid barrier of the single-launch radius graph, 5 the watchdog self-test.
+// 4 grid barrier of the single-launch radius graph, 5 the watchdog self-test,
+// 7 the look-back of the radius graph's single-pass scan.
 
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s
 

@@ -158,11 +158,38 @@ __device__ __forceinline__ long long block_exclusive(long long v, long long* war
   return r;
 }
 
-__global__ void __launch_bounds__(kScanThreads) k_scan_local(int32_t* __restrict__ data, long long n,
-                                                             long long* __restrict__ block_sums) {
+// Single-pass exclusive scan (decoupled look-back): each block takes the
+// next tile in launch order from a ticket counter, scans it, publishes its
+// aggregate, and adds up its predecessors' published values until it meets
+// an inclusive prefix (tile 0 publishes one at once); then it publishes its
+// own inclusive prefix and writes its tile.  A block waits only for tiles
+// that earlier blocks hold, so the scan completes whatever the residency;
+// every wait is bounded (watchdog code 7).  Status words: bits 63..62 flag
+// (1 aggregate, 2 inclusive), 61..0 the value (saturated; a sum that large is
+// reported as too many edges anyway).  status[] and the ticket start at zero
+// (k_clear).
+constexpr unsigned long long kScanAgg = 1ull << 62, kScanIncl = 2ull << 62, kScanVal = (1ull << 62) - 1;
+
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64g(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__global__ void __launch_bounds__(kScanThreads) k_scan_1p(int32_t* __restrict__ data, long long n,
+                                                          unsigned long long* __restrict__ status,
+                                                          unsigned* __restrict__ ticket, const int* __restrict__ bad,
+                                                          long long* __restrict__ e_total, int* watchdog) {
   __shared__ long long warp_tot[32];
-  __shared__ long long total;
-  const long long base = (long long)blockIdx.x * kScanTile + (long long)threadIdx.x * kScanItems;
+  __shared__ long long total, prefix_s;
+  __shared__ unsigned tile_s;
+  if (threadIdx.x == 0) tile_s = atomicAdd(ticket, 1u);
+  __syncthreads();
+  const long long t = tile_s;
+  const long long base = t * kScanTile + (long long)threadIdx.x * kScanItems;
   int v[kScanItems];
   long long s = 0;
 #pragma unroll
@@ -171,52 +198,51 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_local(int32_t* __restrict
     s += v[k];
   }
   long long run = block_exclusive(s, warp_tot, &total);
+  if (threadIdx.x == 0) {
+    const unsigned long long agg = (unsigned long long)min(total, (long long)kScanVal);
+    long long prefix = 0;
+    if (t == 0) {
+      st_release_u64(status, kScanIncl | agg);
+    } else {
+      st_release_u64(status + t, kScanAgg | agg);
+      long long j = t - 1;
+      const unsigned long long t0 = global_ns();
+      while (j >= 0) {
+        const unsigned long long w = ld_acquire_u64g(status + j);
+        if (w == 0ull) {
+          if (global_ns() - t0 > kWaitLimitNs) {
+            watchdog_trip(watchdog, 7);
+            break;
+          }
+          continue;
+        }
+        prefix += (long long)(w & kScanVal);
+        if (w & kScanIncl) break;
+        --j;
+      }
+      st_release_u64(status + t, kScanIncl | (unsigned long long)min(prefix + total, (long long)kScanVal));
+    }
+    prefix_s = prefix;
+    if (e_total && t == (long long)gridDim.x - 1) {  // the last tile knows the grand total
+      long long e = prefix + total;
+      if (e > INT32_MAX) e = -2;
+      if (*bad) e = -1;
+      *e_total = e;
+    }
+  }
+  __syncthreads();
+  run += prefix_s;
 #pragma unroll
   for (int k = 0; k < kScanItems; ++k) {
     if (base + k < n) data[base + k] = (int32_t)run;
     run += v[k];
   }
-  if (threadIdx.x == 0) block_sums[blockIdx.x] = total;
 }
 
-// One block: exclusive scan of the block totals (any count, in tiles), the
-// grand total, and the edge count reported to the caller when asked.
-__global__ void __launch_bounds__(kScanThreads) k_scan_top(long long* __restrict__ sums, long long nb,
-                                                           const int* __restrict__ bad,
-                                                           long long* __restrict__ e_total) {
-  __shared__ long long warp_tot[32];
-  __shared__ long long total;
-  long long carry = 0;
-  for (long long b0 = 0; b0 < nb; b0 += kScanThreads) {
-    const long long b = b0 + threadIdx.x;
-    const long long v = b < nb ? sums[b] : 0;
-    const long long r = block_exclusive(v, warp_tot, &total);
-    if (b < nb) sums[b] = carry + r;
-    carry += total;
-    __syncthreads();
-  }
-  if (e_total && threadIdx.x == 0) {
-    long long e = carry;
-    if (e > INT32_MAX) e = -2;
-    if (*bad) e = -1;
-    *e_total = e;
-  }
-}
-
-__global__ void __launch_bounds__(kScanThreads) k_scan_add(int32_t* __restrict__ data, long long n,
-                                                           const long long* __restrict__ block_sums) {
-  const int add = (int)block_sums[blockIdx.x];
-  const long long base = (long long)blockIdx.x * kScanTile;
-  for (int k = threadIdx.x; k < kScanTile; k += kScanThreads)
-    if (base + k < n) data[base + k] += add;
-}
-
-cudaError_t exclusive_scan(int32_t* data, long long n, long long* block_sums, const int* bad, long long* e_total,
-                           cudaStream_t st) {
+cudaError_t exclusive_scan(int32_t* data, long long n, unsigned long long* status, unsigned* ticket, const int* bad,
+                           long long* e_total, int* watchdog, cudaStream_t st) {
   const long long nb = (n + kScanTile - 1) / kScanTile;
-  k_scan_local<<<(unsigned)nb, kScanThreads, 0, st>>>(data, n, block_sums);
-  k_scan_top<<<1, kScanThreads, 0, st>>>(block_sums, nb, bad, e_total);
-  k_scan_add<<<(unsigned)nb, kScanThreads, 0, st>>>(data, n, block_sums);
+  k_scan_1p<<<(unsigned)nb, kScanThreads, 0, st>>>(data, n, status, ticket, bad, e_total, watchdog);
   return cudaGetLastError();
 }
 
@@ -711,8 +737,8 @@ __global__ void __launch_bounds__(kSortWarps * 32) k_graph_coop(const CoopArgs g
 // ------------------------------------------------------------ workspace
 struct GraphWs {
   long long H = 0;
-  size_t atom_bucket = 0, start = 0, fill = 0, bucket_atoms = 0, bucket_pos = 0, sums = 0, bad = 0, coop = 0,
-         cand = 0, bytes = 0;
+  size_t atom_bucket = 0, start = 0, fill = 0, scan_a = 0, scan_b = 0, tickets = 0, bucket_atoms = 0, bucket_pos = 0,
+         bad = 0, coop = 0, cand = 0, bytes = 0;
   bool scratch = false;  // the single-walk path's per-row scratch is present
 };
 
@@ -729,9 +755,13 @@ GraphWs graph_ws(long long N) {
   w.atom_bucket = o; o = align256(o + 4 * (size_t)N);
   w.start = o;       o = align256(o + 4 * (size_t)(H + 1));
   w.fill = o;        o = align256(o + 4 * (size_t)H);
+  // single-pass scan status (bucket starts, row offsets) and tickets; zeroed
+  // with start and fill
+  w.scan_a = o;      o = align256(o + 8 * (size_t)nb);
+  w.scan_b = o;      o = align256(o + 8 * (size_t)nb);
+  w.tickets = o;     o = align256(o + 8);
   w.bucket_atoms = o; o = align256(o + 4 * (size_t)N);
   w.bucket_pos = o;  o = align256(o + 16 * (size_t)N);
-  w.sums = o;        o = align256(o + 8 * (size_t)nb);
   w.bad = o;         o = align256(o + 4);
   w.coop = o;        o = align256(o + 8 * (size_t)kCoopMaxBlocks + 16);  // block totals + barrier words
   // single-walk scratch rows
@@ -772,7 +802,6 @@ eqmp_status radius_graph_run(const float* pos, int64_t N, float cutoff, const Bo
   int32_t* fill = reinterpret_cast<int32_t*>(base + w.fill);
   int32_t* bucket_atoms = reinterpret_cast<int32_t*>(base + w.bucket_atoms);
   float4* bucket_pos = reinterpret_cast<float4*>(base + w.bucket_pos);
-  long long* sums = reinterpret_cast<long long*>(base + w.sums);
   int* bad = reinterpret_cast<int*>(base + w.bad);
   // start and fill are adjacent: one clear covers both
   const long long n_clear = (long long)((w.bucket_atoms - w.start) / 4);
@@ -831,7 +860,11 @@ eqmp_status radius_graph_run(const float* pos, int64_t N, float cutoff, const Bo
   if (N > 0) {
     k_bin<PBC><<<nblk, kNeighThreads, 0, st>>>(pos, (int)N, inv, mask, atom_bucket, start, bad, box);
   }
-  cudaError_t err = exclusive_scan(start, w.H + 1, sums, bad, nullptr, st);
+  DeviceInfo sdev;
+  if (device_info(&sdev) != EQMP_OK) return EQMP_ERR_CUDA;
+  unsigned* tickets = reinterpret_cast<unsigned*>(base + w.tickets);
+  cudaError_t err = exclusive_scan(start, w.H + 1, reinterpret_cast<unsigned long long*>(base + w.scan_a), tickets,
+                                   bad, nullptr, sdev.watchdog, st);
   if (err != cudaSuccess) return EQMP_ERR_CUDA;
   if (N > 0)
     k_scatter<<<nblk, kNeighThreads, 0, st>>>(pos, (int)N, atom_bucket, start, fill, bucket_atoms, bucket_pos);
@@ -846,7 +879,8 @@ eqmp_status radius_graph_run(const float* pos, int64_t N, float cutoff, const Bo
   else
     k_neigh<kWalkCount, PBC><<<(unsigned)(wblk > 0 ? wblk : 1), kNeighThreads, 0, st>>>(
         bucket_pos, (int)N, inv, rc2, mask, start, bucket_atoms, row_offsets, nullptr, E_cap, box, nullptr);
-  err = exclusive_scan(row_offsets, N + 1, sums, bad, reinterpret_cast<long long*>(E_total), st);
+  err = exclusive_scan(row_offsets, N + 1, reinterpret_cast<unsigned long long*>(base + w.scan_b), tickets + 1, bad,
+                       reinterpret_cast<long long*>(E_total), sdev.watchdog, st);
   if (err != cudaSuccess) return EQMP_ERR_CUDA;
   if (N > 0 && E_cap > 0) {
     if (cand)

@@ -386,8 +386,9 @@ eqmp_status eqmp_validate_graph(const int32_t* row_offsets, const int32_t* src, 
  * call; otherwise a nonzero code naming the wait: 1 a consumer waiting for
  * a gathered row, 2 a producer waiting for a free slot, 3 a producer
  * draining its last slots, 4 a grid barrier of eqmp_radius_graph, 5 the
- * self-test below.  A nonzero code means the
- * outputs of the kernels since the last call are unspecified.  Returns
+ * self-test below, 7 the look-back of eqmp_radius_graph's prefix sums.
+ * A nonzero code means the outputs of the kernels since the last call are
+ * unspecified.  Returns
  * EQMP_ERR_DEVICE_TIMEOUT when *code != 0.
  */
 eqmp_status eqmp_device_error(int32_t* code);

@@ -76,6 +76,19 @@ def test_rows_past_the_scratch_length(eq):
     assert np.diff(got2["off"]).max() > 500
 
 
+def test_single_launch_rows_past_the_scratch_length(eq):
+    """The same in the single cooperative launch (3000 atoms): a crowded
+    corner gives rows of a few hundred next to ordinary ones."""
+    rng = np.random.default_rng(24)
+    n = 3000
+    side = (n / DENSITY) ** (1 / 3)
+    pos = rng.uniform(0, side, (n, 3)).astype(np.float32)
+    pos[:400] = rng.uniform(0, 4.0, (400, 3)).astype(np.float32)
+    got = _same(eq, pos, 5.0)
+    deg = np.diff(got["off"])
+    assert deg.max() > 96 and (deg <= 96).any()
+
+
 def test_ragged_sizes_and_negative_coordinates(eq):
     rng = np.random.default_rng(21)
     for n in (1, 2, 31, 257, 4099):

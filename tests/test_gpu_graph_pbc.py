@@ -144,3 +144,20 @@ def test_layer_on_a_periodic_graph_matches_the_oracle(eq):
                              t(g["src"], np.int32), w=t(w, np.float32)))
     want = layer.message_pass(g["vec"], x, g["off"], g["src"], w=w)
     assert rel_err(got, want) <= 1e-4
+
+
+@pytest.mark.parametrize("n", [3000, 20_000])
+def test_crowded_rows_past_the_scratch_length(eq, n):
+    """Rows longer than the 96-sender scratch of the first walk, in the
+    single launch (3000 atoms) and in the separate launches (20,000): a
+    crowded region straddling a box face, so its long rows hold senders
+    under several images."""
+    rng = np.random.default_rng(31 + n)
+    side = float((n / DENSITY) ** (1 / 3))
+    box = (side, side, side)
+    pos = rng.uniform(0, side, (n, 3))
+    crowd = rng.uniform(-2.0, 2.0, (400, 3)) + np.array([0.0, side / 2, side / 2])
+    pos[:400] = np.mod(crowd, side)
+    pos = _inside(pos, box)
+    got, _ = _same(eq, pos, 5.0, box)
+    assert np.diff(got["off"]).max() > 96

@@ -64,7 +64,7 @@ EXTRA_PASSES = (("backward pages_1k_c32", "pages_1k_c32", "backward"),
 # One-thread oracle runs (the small configurations).
 SINGLE_THREAD_WORKLOADS = ("tiny_64", "pages_1k_c32", "radial_1k_c32")
 GROUP = 32  # timed steps queued behind one GPU spin
-PIPE = 4  # streams (and buffer sets) of the pipelined end-to-end measurement
+PIPE = 6  # streams (and buffer sets) of the pipelined end-to-end measurement
 # DRAM bytes per launch of the layer kernel from the ncu capture recorded in
 # profiles/ (None until captured for the current kernel version).
 # Keyed by (workload, kernel version); a changed kernel gets a new version

@@ -25,7 +25,8 @@ namespace eqmp {
 // bounded wait has given up and is read and cleared by eqmp_device_error().
 // Codes: 1 consumer full-wait, 2 producer empty-wait, 3 producer drain,
 // 4 grid barrier of the single-launch radius graph, 5 the watchdog self-test,
-// 7 the look-back of the radius graph's single-pass scan.
+// 7 the look-back of the radius graph's single-pass scan, 8 a CTA waiting
+// for the piece of a receiver cut between it and the next CTA of its cluster.
 
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s
 
@@ -120,6 +121,119 @@ __device__ __forceinline__ void balanced_range_publish(int4* slot, const int* __
   }
 }
 
+// Edge-granular split inside clusters of Q CTAs.  Cluster k (CTAs kQ ..
+// kQ+Q-1) takes the whole receivers [R0, R1) between the cuts of targets
+// T kQ / G and T (k+1)Q / G, as above.  Its own work W0 = work(R0) ..
+// W1 = work(R1) is then cut evenly: CTA kQ+i starts at t = W0 + (W1-W0) i/Q,
+// which falls in receiver r with work(r) < t <= work(r+1), at edge
+// off[r] + (t - work(r)) when that is below off[r+1] (the receiver is then
+// shared by the CTAs on both sides), else at the receiver boundary r+1.
+// Both CTAs beside a cut compute it from the same target with the same
+// search, so they agree on it bit for bit.  A receiver cut this way is
+// summed in pieces: the CTA after a cut hands its piece to the CTA before
+// it (head_cut), which adds it to its own piece (tail_cut); a CTA inside
+// one long receiver has both.
+struct CutRange {
+  int r_begin, r_end;  // receivers touched, [r_begin, r_end)
+  int e_begin, e_end;  // edges, [e_begin, e_end), as loaded (unclamped)
+  bool head_cut;       // receiver r_begin started before e_begin
+  bool tail_cut;       // receiver r_end - 1 continues past e_end
+};
+
+// First r in [lo0, hi0] with work(r) >= tgt[k] for two targets (hi0 counts
+// as reaching both), with ohi = off[r] and olo = off[r - 1] (olo is only
+// meaningful when r > lo0).  The warp's 32-ary search from above, sharing
+// the first round's probes between the targets.
+__device__ __forceinline__ void work_search2(const int* __restrict__ off, int lo0, int hi0, int ohi0, int o0,
+                                             int alpha, const long long (&tgt)[2], int (&hi)[2], int (&ohi)[2],
+                                             int (&olo)[2]) {
+  const int lane = threadIdx.x & 31;
+  const int p1 = split_probe(lo0, hi0, lane);
+  const int o_p1 = p1 < hi0 ? __ldg(off + p1) : ohi0;
+  int lo[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const long long w = (long long)(o_p1 - o0) + (long long)alpha * p1;
+    const unsigned ge = __ballot_sync(0xffffffffu, p1 == hi0 || w >= tgt[k]);
+    const int f = __ffs(ge) - 1;
+    const int g = f > 0 ? f - 1 : 0;
+    hi[k] = __shfl_sync(0xffffffffu, p1, f);
+    ohi[k] = __shfl_sync(0xffffffffu, o_p1, f);
+    const int prev = __shfl_sync(0xffffffffu, p1, g);
+    const int oprev = __shfl_sync(0xffffffffu, o_p1, g);
+    lo[k] = f == 0 ? lo0 : prev + 1;
+    olo[k] = f == 0 ? 0 : oprev;
+  }
+  while (lo[0] < hi[0] || lo[1] < hi[1]) {
+    int p[2], o[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      p[k] = split_probe(lo[k], hi[k], lane);
+      o[k] = lo[k] < hi[k] && p[k] < hi[k] ? __ldg(off + p[k]) : 0;
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      if (lo[k] >= hi[k]) continue;  // warp-uniform
+      const long long w = (long long)(o[k] - o0) + (long long)alpha * p[k];
+      const unsigned ge = __ballot_sync(0xffffffffu, p[k] == hi[k] || w >= tgt[k]);
+      const int f = __ffs(ge) - 1;
+      const int g = f > 0 ? f - 1 : 0;
+      const int nh = __shfl_sync(0xffffffffu, p[k], f);
+      const int of = __shfl_sync(0xffffffffu, o[k], f);
+      const int prev = __shfl_sync(0xffffffffu, p[k], g);
+      const int oprev = __shfl_sync(0xffffffffu, o[k], g);
+      if (f > 0) { lo[k] = prev + 1; olo[k] = oprev; }
+      if (nh != hi[k]) ohi[k] = of;
+      hi[k] = nh;
+    }
+  }
+}
+
+__device__ __forceinline__ CutRange cluster_cut_range(const int* __restrict__ off, int N, int G, int b, int Q,
+                                                      int alpha) {
+  const int o0 = __ldg(off), oN = __ldg(off + N);
+  const long long total = (long long)max(oN - o0, 0) + (long long)alpha * N;
+  const int k0 = b - b % Q, i = b - k0;  // the cluster's first CTA; this CTA's rank in it
+  // phase 1: the cluster's whole receivers [R0, R1)
+  int hi[2], ohi[2], olo[2];
+  {
+    const long long tgt[2] = {total * k0 / G, total * (k0 + Q) / G};
+    work_search2(off, 0, N, oN, o0, alpha, tgt, hi, ohi, olo);
+  }
+  if (k0 == 0) { hi[0] = 0; ohi[0] = o0; }
+  if (k0 + Q >= G) { hi[1] = N; ohi[1] = oN; }
+  const int R0 = hi[0], E0 = ohi[0];
+  const int R1 = max(hi[1], R0), E1 = max(ohi[1], E0);
+  // phase 2: this CTA's cuts inside [R0, R1]
+  const long long W0 = (long long)(E0 - o0) + (long long)alpha * R0;
+  const long long W1 = max((long long)(E1 - o0) + (long long)alpha * R1, W0);
+  const long long tgt[2] = {W0 + (W1 - W0) * i / Q, W0 + (W1 - W0) * (i + 1) / Q};
+  work_search2(off, R0, R1, E1, o0, alpha, tgt, hi, ohi, olo);
+  // cut k as (receiver, edge, inside)
+  auto place = [&](int k, int& r, int& e, bool& inside) {
+    r = hi[k]; e = ohi[k]; inside = false;
+    if (hi[k] > R0) {
+      const long long wprev = (long long)(olo[k] - o0) + (long long)alpha * (hi[k] - 1);
+      const long long ee = (long long)olo[k] + (tgt[k] - wprev);
+      if (ee < (long long)ohi[k]) { r = hi[k] - 1; e = (int)ee; inside = true; }
+    }
+    if (e <= E0) { r = R0; e = E0; inside = false; }
+    if (e >= E1) { r = R1; e = E1; inside = false; }
+  };
+  int rb = R0, eb = E0, re = R1, ee = E1;
+  bool ib = false, ie = false;
+  if (i != 0) place(0, rb, eb, ib);
+  if (i != Q - 1) place(1, re, ee, ie);
+  CutRange c;
+  c.r_begin = rb;
+  c.e_begin = eb;
+  c.e_end = max(ee, eb);
+  c.r_end = max(ie ? re + 1 : re, rb);
+  c.head_cut = ib;
+  c.tail_cut = ie;
+  return c;
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -198,6 +312,57 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
+}
+
+// ---------------------------------------------------------------- clusters
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+// The address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Arrive on an mbarrier of another CTA of the cluster (address from map_rank),
+// releasing this thread's earlier writes (and those ordered before them) at
+// cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+// Bounded wait on a local mbarrier that other CTAs of the cluster arrive on,
+// acquiring at cluster scope.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(1000000u)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, int* wd, int code) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      watchdog_trip(wd, code);
+      return false;
+    }
+  }
 }
 
 // Out-of-line slow path of a wait whose first try failed: keeps the hot loop

@@ -17,6 +17,10 @@
 // into a 64-entry edge ring; then one TMA row copy of x[src] per edge into an
 // S-slot ring (128-byte swizzle), as in k_shared.  Receiver partials of the
 // groups are summed through shared memory in group order (deterministic).
+// CTAs run in clusters of Q; inside a cluster the edges are cut at edge
+// granularity (cluster_cut_range), and the CTA after a cut hands its piece
+// of the cut receiver to the CTA before it through distributed shared
+// memory, which adds it to its own piece (deterministic: own piece first).
 #pragma once
 
 #include <cuda.h>
@@ -144,6 +148,11 @@ __device__ __forceinline__ void wigner_blocks(float x, float y, float z, float* 
 template <int C, typename XT, bool RADIAL>
 struct So2Cfg {
   static constexpr int NCONS = 128;
+#ifdef EQMP_TUNE_SO2_Q
+  static constexpr int Q = EQMP_TUNE_SO2_Q;            // cluster size (experiments)
+#else
+  static constexpr int Q = 2;                          // cluster size
+#endif
   static constexpr int EG = NCONS / C;                 // edge groups
   static constexpr int NTHREADS = NCONS + 32;
   static constexpr int ROW_BYTES = C * 16 * (int)sizeof(XT);
@@ -152,7 +161,8 @@ struct So2Cfg {
   static constexpr int YR = 64;
   // radial: M as [8][17][C] float2; shared: w as [34][C]
   static constexpr int M_BYTES = RADIAL ? 8 * 34 * C * 4 : 34 * C * 4;
-  static constexpr int FIXED = YR * kEntryFloats * 4 + 2 * EG * 16 * C * 4 + M_BYTES + 2 * 16 * 8 + 2048;
+  static constexpr int FIXED = YR * kEntryFloats * 4 + 2 * EG * 16 * C * 4 + M_BYTES + 16 * C * 4 + 2 * 16 * 8 + 16 +
+                               32 + 2048;
   // two CTAs per SM when at least 4 slots fit in half the shared memory
   static constexpr int S_FIT2 = (113 * 1024 - FIXED) / SLOT;
   static constexpr int MINB = S_FIT2 >= 4 ? 2 : 1;
@@ -163,9 +173,10 @@ struct So2Cfg {
   static constexpr int OFF_E = OFF_X + S * SLOT;                       // edge ring
   static constexpr int OFF_RED = OFF_E + YR * kEntryFloats * 4;         // [2][EG][16][C]
   static constexpr int OFF_M = OFF_RED + 2 * EG * 16 * C * 4;          // radial: [8][17][C] float2
-  static constexpr int OFF_BAR = OFF_M + M_BYTES;
-  static constexpr int OFF_RANGE = OFF_BAR + 2 * S * 8;  // the CTA's range (int4)
-  static constexpr int SMEM_BYTES = OFF_RANGE + 16 + 1024;
+  static constexpr int OFF_EX = OFF_M + M_BYTES;                       // [16][C]: piece handed over
+  static constexpr int OFF_BAR = OFF_EX + 16 * C * 4;                  // full[S], empty[S], xfull
+  static constexpr int OFF_RANGE = OFF_BAR + 2 * S * 8 + 16;           // the CTA's CutRange
+  static constexpr int SMEM_BYTES = OFF_RANGE + 32 + 1024;
 };
 
 // One padded D row (m) of level L from the edge entry into registers.
@@ -254,6 +265,51 @@ __device__ __forceinline__ void so2_all(const float2* Ms, int c, const float2 (&
   (so2_pair<Qs, C, RADIAL>(Ms, c, rr, xr, mp), ...);
 }
 
+// The radial mixing matrix (or the shared weights) to shared memory by NT
+// threads (t = 0 .. NT-1), while warp 0 searches the CTA's range; loads in
+// batches of 8 per thread, each batch issued before its stores.
+template <int C, bool RADIAL, int NT>
+__device__ __forceinline__ void so2_stage_weights(const LayerArgs& a, float2* Ms, int t) {
+  if constexpr (RADIAL) {
+    // M[k][p*C + c] -> Ms[(k*17 + p/2)*C + c] = (M[k][p][c], M[k][p+1][c])
+    if ((reinterpret_cast<uintptr_t>(a.M) & 15) == 0) {
+      constexpr int Q4 = 8 * 17 * C / 4;  // (k, path pair, 4 channels)
+      for (int base = 0; base < Q4; base += 8 * NT) {
+        float4 va[8], vb[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = base + t + u * NT;
+          if (i < Q4) {
+            const int c4 = i % (C / 4), pp = (i / (C / 4)) % 17, k = i / (17 * (C / 4));
+            const float* row = a.M + (size_t)k * 34 * C + (size_t)(2 * pp) * C + 4 * c4;
+            va[u] = __ldg(reinterpret_cast<const float4*>(row));
+            vb[u] = __ldg(reinterpret_cast<const float4*>(row + C));
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = base + t + u * NT;
+          if (i < Q4) {
+            const int c4 = i % (C / 4), pp = (i / (C / 4)) % 17, k = i / (17 * (C / 4));
+            float4* d = reinterpret_cast<float4*>(Ms + (k * 17 + pp) * C + 4 * c4);
+            d[0] = make_float4(va[u].x, vb[u].x, va[u].y, vb[u].y);
+            d[1] = make_float4(va[u].z, vb[u].z, va[u].w, vb[u].w);
+          }
+        }
+      }
+    } else {
+      for (int i = t; i < 8 * 17 * C; i += NT) {
+        const int k = i / (17 * C), pp = (i / C) % 17, c = i % C;
+        Ms[i] = make_float2(__ldg(a.M + (size_t)k * 34 * C + (2 * pp) * C + c),
+                            __ldg(a.M + (size_t)k * 34 * C + (2 * pp + 1) * C + c));
+      }
+    }
+  } else {
+    float* ws = reinterpret_cast<float*>(Ms);
+    for (int i = t; i < 34 * C; i += NT) ws[i] = __ldg(a.w + i);
+  }
+}
+
 template <int C, typename XT, bool RADIAL>
 __global__ void __launch_bounds__(So2Cfg<C, XT, RADIAL>::NTHREADS, So2Cfg<C, XT, RADIAL>::MINB)
     k_so2(const __grid_constant__ CUtensorMap tmap, const LayerArgs a) {
@@ -264,23 +320,34 @@ __global__ void __launch_bounds__(So2Cfg<C, XT, RADIAL>::NTHREADS, So2Cfg<C, XT,
   float* ering = reinterpret_cast<float*>(smem + K::OFF_E);
   float* red = reinterpret_cast<float*>(smem + K::OFF_RED);
   float2* Ms = reinterpret_cast<float2*>(smem + K::OFF_M);
+  float* ex = reinterpret_cast<float*>(smem + K::OFF_EX);
   const uint32_t full0 = smem_u32(smem + K::OFF_BAR);
   const uint32_t empty0 = full0 + 8 * S;
+  const uint32_t xfull = empty0 + 8 * S;  // the next CTA's piece is in its ex
   const int tid = threadIdx.x;
-  // Contiguous receiver range, balanced on edges (a receiver's group sum and
-  // store cost about one edge here).
-  int4* range_s = reinterpret_cast<int4*>(smem + K::OFF_RANGE);
-  balanced_range_publish(range_s, a.off, a.N, gridDim.x, blockIdx.x, 1);
+  // Edge range, balanced on edges (a receiver's group sum and store cost
+  // about one edge here), cut at edge granularity inside the cluster.
+  CutRange* range_s = reinterpret_cast<CutRange*>(smem + K::OFF_RANGE);
+  if (tid < 32) {
+    const CutRange cr = cluster_cut_range(a.off, a.N, gridDim.x, blockIdx.x, K::Q, 1);
+    if (tid == 0) *range_s = cr;
+  }
+  if (tid >= 32 && tid < K::NCONS) so2_stage_weights<C, RADIAL, K::NCONS - 32>(a, Ms, tid - 32);
   if (tid < S) {
     mbar_init(full0 + 8 * tid, 1);
     mbar_init(empty0 + 8 * tid, C);  // the C threads of the owning edge group
+    if (tid == 0) mbar_init(xfull, 1);
     fence_mbar_init();
   }
   __syncthreads();
-  const int4 rr = *range_s;
-  const int r_begin = rr.x, r_end = rr.y;
-  const int e_begin = min(max(rr.z, 0), a.E);
-  const int e_end = max(e_begin, min(max(rr.w, 0), a.E));
+  // Two cluster barriers: this one (arrive now, wait before any remote
+  // access) publishes the initialised barriers; the one at the end keeps
+  // every CTA's shared memory alive until the cluster's remote accesses are done.
+  cluster_arrive();
+  const CutRange cr = *range_s;
+  const int r_begin = cr.r_begin, r_end = cr.r_end;
+  const int e_begin = min(max(cr.e_begin, 0), a.E);
+  const int e_end = max(e_begin, min(max(cr.e_end, 0), a.E));
   const int total = e_end - e_begin;
 
   if (tid >= K::NCONS) {
@@ -333,52 +400,15 @@ __global__ void __launch_bounds__(So2Cfg<C, XT, RADIAL>::NTHREADS, So2Cfg<C, XT,
       for (uint32_t i = first; i < last; ++i)
         if (!mbar_wait(full0 + 8 * (i % S), (i / S) & 1u, a.watchdog, 3)) break;
     }
+    cluster_wait();
+    cluster_arrive();
+    cluster_wait();
     return;
   }
 
   // -------------------------------------------------------------- consumers
-  // The radial mixing matrix (or the shared weights) to shared memory, by
-  // the consumers while the producer builds the first edges; loads in
-  // batches of 8 per thread, each batch issued before its stores.
-  if constexpr (RADIAL) {
-    // M[k][p*C + c] -> Ms[(k*17 + p/2)*C + c] = (M[k][p][c], M[k][p+1][c])
-    if ((reinterpret_cast<uintptr_t>(a.M) & 15) == 0) {
-      constexpr int Q4 = 8 * 17 * C / 4;  // (k, path pair, 4 channels)
-      for (int base = 0; base < Q4; base += 8 * K::NCONS) {
-        float4 va[8], vb[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int i = base + tid + u * K::NCONS;
-          if (i < Q4) {
-            const int c4 = i % (C / 4), pp = (i / (C / 4)) % 17, k = i / (17 * (C / 4));
-            const float* row = a.M + (size_t)k * 34 * C + (size_t)(2 * pp) * C + 4 * c4;
-            va[u] = __ldg(reinterpret_cast<const float4*>(row));
-            vb[u] = __ldg(reinterpret_cast<const float4*>(row + C));
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int i = base + tid + u * K::NCONS;
-          if (i < Q4) {
-            const int c4 = i % (C / 4), pp = (i / (C / 4)) % 17, k = i / (17 * (C / 4));
-            float4* d = reinterpret_cast<float4*>(Ms + (k * 17 + pp) * C + 4 * c4);
-            d[0] = make_float4(va[u].x, vb[u].x, va[u].y, vb[u].y);
-            d[1] = make_float4(va[u].z, vb[u].z, va[u].w, vb[u].w);
-          }
-        }
-      }
-    } else {
-      for (int i = tid; i < 8 * 17 * C; i += K::NCONS) {
-        const int k = i / (17 * C), pp = (i / C) % 17, c = i % C;
-        Ms[i] = make_float2(__ldg(a.M + (size_t)k * 34 * C + (2 * pp) * C + c),
-                            __ldg(a.M + (size_t)k * 34 * C + (2 * pp + 1) * C + c));
-      }
-    }
-  } else {
-    float* ws = reinterpret_cast<float*>(Ms);
-    for (int i = tid; i < 34 * C; i += K::NCONS) ws[i] = __ldg(a.w + i);
-  }
-  named_barrier(2, K::NCONS);  // M (or w) visible to every consumer
+  cluster_wait();              // every CTA of the cluster has initialised its barriers
+  const uint32_t rank = cluster_rank();
 
   const int c = tid % C, g = tid / C;
   const uint32_t xlog = (uint32_t)(c * 16 * (int)sizeof(XT));
@@ -387,8 +417,8 @@ __global__ void __launch_bounds__(So2Cfg<C, XT, RADIAL>::NTHREADS, So2Cfg<C, XT,
   int buf = 0;
   uint32_t n = 0;
   for (int r = r_begin; r < r_end; ++r) {
-    const int a0 = min(max(__ldg(a.off + r), 0), a.E);
-    const int a1 = min(max(__ldg(a.off + r + 1), 0), a.E);
+    const int a0 = max(min(max(__ldg(a.off + r), 0), a.E), e_begin);
+    const int a1 = min(min(max(__ldg(a.off + r + 1), 0), a.E), e_end);
     const int deg = min(max(a1 - a0, 0), total - (int)n);
     float out[16];
 #pragma unroll
@@ -475,8 +505,10 @@ __global__ void __launch_bounds__(So2Cfg<C, XT, RADIAL>::NTHREADS, So2Cfg<C, XT,
     for (int k = 0; k < 16; ++k) rb[(g * 16 + k) * C + c] = out[k];
     named_barrier(1, K::NCONS);
     constexpr int KPER = 16 / K::EG > 0 ? 16 / K::EG : 1;
+    const bool head = cr.head_cut && r == r_begin;    // piece handed to the CTA before
+    const bool tail = cr.tail_cut && r == r_end - 1;  // the CTA after holds the rest
+    float o[16];
     if (g * KPER < 16) {
-      float o[16];
 #pragma unroll
       for (int i = 0; i < KPER; ++i) {
         float sum = 0.0f;
@@ -484,6 +516,25 @@ __global__ void __launch_bounds__(So2Cfg<C, XT, RADIAL>::NTHREADS, So2Cfg<C, XT,
         for (int gg = 0; gg < K::EG; ++gg) sum += rb[(gg * 16 + g * KPER + i) * C + c];
         o[i] = sum;
       }
+    }
+    if (tail) {
+      // own piece first, then the next CTA's (which already holds the pieces after it)
+      if (!failed && !mbar_wait_cluster(xfull, 0, a.watchdog, 8)) failed = true;
+      if (!failed && g * KPER < 16) {
+        const uint32_t rex = map_rank(smem_u32(ex + (g * KPER) * C + c), rank + 1);
+#pragma unroll
+        for (int i = 0; i < KPER; ++i) o[i] += ld_cluster_f32(rex + 4u * (uint32_t)(i * C));
+      }
+    }
+    if (head) {
+      if (g * KPER < 16) {
+#pragma unroll
+        for (int i = 0; i < KPER; ++i) ex[(g * KPER + i) * C + c] = o[i];
+      }
+      fence_cluster();
+      named_barrier(3, K::NCONS);  // the whole piece is in ex
+      if (tid == 0) mbar_arrive_remote(map_rank(xfull, rank - 1));
+    } else if (g * KPER < 16) {
       if constexpr (sizeof(XT) == 4) {
         float* op = reinterpret_cast<float*>(a.out) + ((size_t)r * C + c) * 16 + g * KPER;
 #pragma unroll
@@ -496,6 +547,8 @@ __global__ void __launch_bounds__(So2Cfg<C, XT, RADIAL>::NTHREADS, So2Cfg<C, XT,
     }
     buf ^= 1;
   }
+  cluster_arrive();
+  cluster_wait();
 }
 
 }  // namespace eqmp

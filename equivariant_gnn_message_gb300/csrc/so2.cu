@@ -10,22 +10,33 @@ static eqmp_status launch_so2_t(const LayerArgs& a, const CUtensorMap& map, cuda
   using K = So2Cfg<C, XT, RADIAL>;
   auto kern = k_so2<C, XT, RADIAL>;
   static unsigned long long attr_done = 0;
-  static int occ_cache[64] = {0};
+  static int clusters_cache[64] = {0};
   if (ensure_smem_attr(kern, K::SMEM_BYTES, &attr_done) != cudaSuccess) return EQMP_ERR_CUDA;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = K::Q;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(K::NTHREADS);
+  cfg.dynamicSmemBytes = K::SMEM_BYTES;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   int d = 0;
   cudaGetDevice(&d);
-  int occ = __atomic_load_n(&occ_cache[d & 63], __ATOMIC_RELAXED);
-  if (occ == 0) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, K::NTHREADS, K::SMEM_BYTES) != cudaSuccess ||
-        occ < 1)
-      return EQMP_ERR_CUDA;
-    __atomic_store_n(&occ_cache[d & 63], occ, __ATOMIC_RELAXED);
+  // Clusters resident at once on the whole device: the persistent grid.
+  int nc = __atomic_load_n(&clusters_cache[d & 63], __ATOMIC_RELAXED);
+  if (nc == 0) {
+    cfg.gridDim = dim3(K::Q * dev.sms);
+    if (cudaOccupancyMaxActiveClusters(&nc, kern, &cfg) != cudaSuccess || nc < 1) return EQMP_ERR_CUDA;
+    __atomic_store_n(&clusters_cache[d & 63], nc, __ATOMIC_RELAXED);
   }
-  const long long slots = (long long)dev.sms * occ;
-  const int grid = (int)(a.N < slots ? a.N : slots);
-  if (grid <= 0) return EQMP_OK;
-  kern<<<grid, K::NTHREADS, K::SMEM_BYTES, st>>>(map, a);
-  return cuda_status(cudaGetLastError());
+  const long long need = ((long long)a.N + K::Q - 1) / K::Q;  // at least one receiver per cluster
+  const int clusters = (int)(need < nc ? need : nc);
+  if (clusters <= 0) return EQMP_OK;
+  cfg.gridDim = dim3(clusters * K::Q);
+  return cuda_status(cudaLaunchKernelEx(&cfg, kern, map, a));
 }
 
 template <typename XT, bool RADIAL>

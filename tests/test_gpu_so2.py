@@ -73,3 +73,30 @@ def test_so2_deterministic(eq):
     a = eq.eqmp_fused_so2(d["vec"], d["x"], d["off"], d["src"], **weights_kw(d)).clone()
     b = eq.eqmp_fused_so2(d["vec"], d["x"], d["off"], d["src"], **weights_kw(d))
     assert a.equal(b)
+
+
+@pytest.mark.parametrize("mode", ["shared", "radial"])
+def test_so2_receivers_cut_inside_clusters(eq, mode):
+    """Receivers cut between the CTAs of a cluster: a hub of degree 3000 (cut
+    across every CTA of one cluster, the middle CTAs holding only part of it),
+    three of degree about 200, isolated receivers and a plain ragged graph
+    around them.  Compared receiver by receiver."""
+    from tests.test_gpu_parity import _custom
+
+    rng = np.random.default_rng(5)
+    n = 3600
+    pos = rng.uniform(0, 40, (n, 3))
+    pairs = [(0, j) for j in range(1, 3001)]
+    for h in (3100, 3200, 3300):
+        pairs += [(h, int(j)) for j in rng.choice(n, 200, replace=False) if j != h]
+    for r in range(3400, 3600):
+        pairs += [(r, int(j)) for j in rng.choice(n, int(rng.integers(0, 30)), replace=False) if j != r]
+    wl = _custom(pos, pairs, mode=mode)
+    got = _check(eq, wl).astype(np.float64)
+    want = layer.message_pass(wl.vec, wl.x, wl.off, wl.src, **oracle_kw(wl))
+    deg = np.diff(wl.off)
+    assert np.all(got[deg == 0] == 0.0)
+    num = np.linalg.norm((got - want).reshape(n, -1), axis=1)
+    den = np.linalg.norm(want.reshape(n, -1), axis=1)
+    has = deg > 0
+    assert np.max(num[has] / den[has]) <= 1e-4

@@ -261,7 +261,9 @@ eqmp_status eqmp_fused_backward_noalloc(const float* vec, const float* x, int64_
  * takes one input order (Eq. 13, 111 terms instead of 611), then rotated
  * back and summed into the receiver.  Exact up to rounding; about 2.5x fewer
  * FMAs per edge and channel, so it is the faster choice for per-edge
- * (radial) weights.  Arguments and results as eqmp_fused.
+ * (radial) weights.  Arguments and results as eqmp_fused.  Launched in
+ * clusters of two CTAs that may sum one receiver in two pieces (added in
+ * a fixed order, so results stay bitwise reproducible on one device).
  */
 eqmp_status eqmp_fused_so2(const float* vec, const void* x, int64_t N_src, eqmp_dtype x_dtype,
                            const int32_t* row_offsets, const int32_t* src, int64_t N, int64_t E,
@@ -386,7 +388,9 @@ eqmp_status eqmp_validate_graph(const int32_t* row_offsets, const int32_t* src, 
  * call; otherwise a nonzero code naming the wait: 1 a consumer waiting for
  * a gathered row, 2 a producer waiting for a free slot, 3 a producer
  * draining its last slots, 4 a grid barrier of eqmp_radius_graph, 5 the
- * self-test below, 7 the look-back of eqmp_radius_graph's prefix sums.
+ * self-test below, 7 the look-back of eqmp_radius_graph's prefix sums,
+ * 8 a CTA of the aligned-frame layer waiting for the piece of a receiver
+ * that the next CTA of its cluster summed.
  * A nonzero code means the outputs of the kernels since the last call are
  * unspecified.  Returns
  * EQMP_ERR_DEVICE_TIMEOUT when *code != 0.

@@ -9,16 +9,15 @@
 // kappa_p[m3, m1] = C_p[m3, m1, 0] sqrt((2 l2 + 1) / 4 pi) (tables generated
 // at build time from this library's real CG coefficients).
 //
-// Organisation: 128 threads per CTA in groups of C threads (thread =
-// channel); a CTA owns one receiver at a time.  For each batch of its edges,
-// one thread per edge builds the real Wigner-D blocks D_1..D_L of the edge
-// frame in shared memory (frame by Duff et al. 2017; levels 2..L by the
-// Ivanic-Ruedenberg recursion with compile-time coefficients, so the threads
-// never diverge).  The groups then take the batch's edges: the sender row is
-// staged in shared memory with coalesced loads, every thread rotates its
-// channel in, applies the aligned terms with its path weights, and rotates
-// back into its partial accumulators; the partials are added in group order
-// at the end.  Deterministic (fixed order everywhere), no atomics.
+// Organisation (k_hl below): a producer warp builds the real Wigner-D
+// blocks D_1..D_L of each edge's frame (frame by Duff et al. 2017; levels
+// 2..L by the Ivanic-Ruedenberg recursion with compile-time coefficients, one
+// edge per lane, so the lanes never diverge) into an edge ring and
+// bulk-copies each sender row into a row ring; 128 consumer threads in
+// groups of C (thread = channel) rotate their channel in, apply the aligned
+// terms with their path weights, and rotate back into partial accumulators,
+// added in group order at each receiver's end.  Deterministic (fixed order
+// everywhere), no atomics.
 // Zero-length edges (r^2 < 1e-30) take Y = (Y00, 0, ...): only the paths
 // (l, 0, l) contribute, as W_p Y00 x_l.
 #include <stdint.h>
@@ -35,8 +34,7 @@ namespace {
 
 using tables_hl::Hl;
 
-constexpr int kHlThreads = 128;
-constexpr int kBatch = 16;  // edges whose Wigner blocks are built at once
+constexpr int kHlThreads = 128;  // consumer threads per CTA (plus one producer warp)
 
 struct HlArgs {
   const float* vec;
@@ -47,6 +45,7 @@ struct HlArgs {
   const float* R;
   const float* M;
   float* out;
+  int* watchdog;
   int N, E, N_src, C;
 };
 
@@ -62,30 +61,11 @@ struct HlCfg {
     return o;
   }
   // Floats per edge slot (D_1..D_L): a multiple of 4 (rows are read as
-  // float4s) that is 4 more than a multiple of 32, so the builders of a batch
-  // (thread j writes slot j) spread over the banks (2-way, not 16-way).
+  // float4s) that is 4 more than a multiple of 32, so the producer's lanes
+  // (lane j writes slot j) spread their stores over the banks.
   static constexpr int DS = (off(L + 1) + 31) / 32 * 32 + 4;
-  static constexpr int XV = (NC + 3) / 4;                  // float4s of a staged row per thread
-  // floats: a batch of kBatch edge slots (+ zero-length flags), the
-  // accumulators of every thread [NC][128], the staged sender rows
-  // [G][C][NC] (= [128][NC]), then the weights: shared [P][C], or the
-  // current edge's radial weights of every thread [P][128]
-  static constexpr int off_flag() { return kBatch * DS; }
-  static constexpr int off_acc() { return off_flag() + kBatch; }
-  static constexpr int off_x() { return off_acc() + NC * kHlThreads; }
-  static constexpr int off_w() { return off_x() + NC * kHlThreads; }
-  static constexpr int smem(int C, bool radial) { return (off_w() + (radial ? P * kHlThreads : P * C)) * 4; }
 };
 
-__device__ __forceinline__ void group_sync(int C, int g) {
-  if (C <= 32) {
-    const unsigned lane_base = (threadIdx.x & 31u) / (unsigned)C * (unsigned)C;
-    const unsigned mask = C == 32 ? 0xffffffffu : (((1u << C) - 1u) << lane_base);
-    __syncwarp(mask);
-  } else {
-    asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "r"(C) : "memory");
-  }
-}
 
 // ---- Wigner-D of one edge, computed by one thread -----------------------
 // Ivanic-Ruedenberg basis (real SH without the Condon-Shortley sign, l = 1
@@ -299,110 +279,200 @@ __device__ __forceinline__ void zero_len_terms(const HlArgs& a, const float* ws,
   (zero_len_path<L, RADIAL, Ps>(a, ws, c, rad, xrow, acc), ...);
 }
 
+// Shared-memory plan of k_hl for one (L, C, weights): a producer batch of
+// PB edges (their Wigner blocks built lane-parallel), an S-slot ring of
+// gathered sender rows (S a multiple of the group count 128 / C), and an
+// edge ring of YR = PB + S entries (the
+// producer writes a batch's entries only after the rows S edges back have
+// been released, so PB + S entries never collide).  Offsets in floats.
+struct HlPlan {
+  int PB, S, YR;
+  int o_slot, o_flag, o_rad, o_acc, o_x, o_w, o_bar, bytes;
+};
+
+template <int L>
+inline HlPlan hl_plan(int C, bool radial, int pb, int S) {
+  using K = HlCfg<L>;
+  HlPlan q{};
+  q.PB = pb;
+  q.S = S;
+  q.YR = pb + S;
+  auto up4 = [](int v) { return (v + 3) / 4 * 4; };
+  q.o_slot = 0;
+  q.o_flag = up4(q.o_slot + q.YR * K::DS);
+  q.o_rad = up4(q.o_flag + q.YR);
+  q.o_acc = up4(q.o_rad + (radial ? 8 * q.YR : 0));
+  q.o_x = up4(q.o_acc + K::NC * kHlThreads);
+  q.o_w = up4(q.o_x + S * C * K::NC);
+  q.o_bar = up4(q.o_w + (radial ? K::P * kHlThreads : K::P * C));  // barriers, then the range (int4)
+  q.bytes = q.o_bar * 4 + 2 * S * 8 + 16;
+  return q;
+}
+
+// CTA: NCONS = 128 consumer threads in groups of C (thread = channel) and one
+// producer warp.  The CTA owns a contiguous receiver range, balanced on edges
+// (balanced_range_publish), and walks its edges in order across receivers.
+// Producer, per batch of PB edges lane-parallel: the edge's unit vector, its
+// frame and D_1..D_L into the edge ring (lane j builds edge j, no
+// divergence), the zero-length flag and (radial) the 8 features; then one
+// bulk copy of the sender row x[src] (C (L+1)^2 floats, contiguous) per edge
+// into the row ring, completing on the slot's full barrier.  Group g takes
+// the edges whose CTA ordinal is g mod G: it rotates its channel in, applies
+// the aligned terms with its path weights, rotates back into its partial
+// accumulators (shared memory), and releases the slot.  At each receiver's
+// end the groups' partials are added in group order.
 template <int L, bool RADIAL>
-__global__ void __launch_bounds__(kHlThreads) k_hl(const HlArgs a) {
+__global__ void __launch_bounds__(kHlThreads + 32, 2) k_hl(const HlArgs a, const HlPlan q) {
   using K = HlCfg<L>;
   constexpr int NC = K::NC;
-  extern __shared__ float hsm[];
+  extern __shared__ __align__(16) float hsm[];
   const int C = a.C, G = kHlThreads / C;
-  const int t = threadIdx.x, g = t / C, c = t % C;
-  float* slots = hsm;                      // [kBatch][DS]
-  float* flags = hsm + K::off_flag();      // [kBatch]: 1 for a zero-length edge
-  float* accs = hsm + K::off_acc();        // partial accumulators [G][NC][C]
-  float* acc = accs + (size_t)g * NC * C + c;
-  float* xs = hsm + K::off_x() + (size_t)g * C * NC;  // the group's staged sender row [C][NC]
-  float* ws = hsm + K::off_w();
-  if constexpr (!RADIAL) {
-    for (int i = t; i < K::P * C; i += kHlThreads) ws[i] = __ldg(a.w + i);
-    __syncthreads();
+  const int t = threadIdx.x;
+  const int S = q.S, YR = q.YR;
+  float* slots = hsm + q.o_slot;  // [YR][DS]
+  float* flags = hsm + q.o_flag;  // [YR]: 1 for a zero-length edge
+  float* rads = hsm + q.o_rad;    // [YR][8] radial features
+  float* accs = hsm + q.o_acc;    // partial accumulators [G][NC][C]
+  float* xring = hsm + q.o_x;     // [S][C][NC]
+  float* ws = hsm + q.o_w;
+  const uint32_t full0 = smem_u32(hsm + q.o_bar);
+  const uint32_t empty0 = full0 + 8 * S;
+  int4* range_s = reinterpret_cast<int4*>(hsm + q.o_bar + 4 * S);
+  balanced_range_publish(range_s, a.off, a.N, gridDim.x, blockIdx.x, 1);
+  if (t < S) {
+    mbar_init(full0 + 8 * t, 1);
+    mbar_init(empty0 + 8 * t, C);  // the C threads of the owning group
+    fence_mbar_init();
   }
-  // One receiver per CTA at a time.  Its edges go in batches of kBatch:
-  // thread j builds the Wigner blocks of edge j of the batch (one edge per
-  // thread, no divergence), then the G groups take the batch's edges
-  // g, g + G, ... and add them into their partial sums, which are summed in
-  // group order at the end: deterministic.
-  for (long long r = blockIdx.x; r < a.N; r += gridDim.x) {
-    const int e0 = min(max(__ldg(a.off + r), 0), a.E);
-    const int e1 = max(e0, min(max(__ldg(a.off + r + 1), 0), a.E));
-#pragma unroll
-    for (int k = 0; k < NC; ++k) acc[k * C] = 0.0f;
-    for (int b0 = e0; b0 < e1; b0 += kBatch) {
-      const int nb = min(kBatch, e1 - b0);
-      __syncthreads();  // the previous batch's slots are no longer read
-      if (t < nb) {
-        const int e = b0 + t;
+  if constexpr (!RADIAL) {
+    if (t < kHlThreads)
+      for (int i = t; i < K::P * C; i += kHlThreads) ws[i] = __ldg(a.w + i);
+  }
+  __syncthreads();
+  const int4 rr = *range_s;
+  const int r_begin = rr.x, r_end = rr.y;
+  const int e_begin = min(max(rr.z, 0), a.E);
+  const int e_end = max(e_begin, min(max(rr.w, 0), a.E));
+  const int total = e_end - e_begin;
+  const uint32_t row_bytes = (uint32_t)(C * NC * 4);
+
+  if (t >= kHlThreads) {
+    // ------------------------------------------------------------ producer
+    const int lane = t & 31;
+    bool ok = true;
+    for (int base = 0; base < total && ok; base += q.PB) {
+      const uint32_t n = (uint32_t)(base + lane);
+      int node = 0;
+      if (lane < q.PB && n < (uint32_t)total) {
+        const int e = e_begin + (int)n;
+        node = __ldg(a.src + e);
         const float vx = __ldg(a.vec + 3 * (size_t)e), vy = __ldg(a.vec + 3 * (size_t)e + 1),
                     vz = __ldg(a.vec + 3 * (size_t)e + 2);
+        const int y = (int)(n % (uint32_t)YR);
         const float r2 = fmaf(vx, vx, fmaf(vy, vy, vz * vz));
         if (r2 >= 1e-30f) {
           const float inv = rsqrtf(r2);
-          hl_wigner<L>(vx * inv, vy * inv, vz * inv, slots + (size_t)t * K::DS);
-          flags[t] = 0.0f;
+          hl_wigner<L>(vx * inv, vy * inv, vz * inv, slots + (size_t)y * K::DS);
+          flags[y] = 0.0f;
         } else {
-          flags[t] = 1.0f;  // zero length: Y = (Y00, 0, ...)
+          flags[y] = 1.0f;  // zero length: Y = (Y00, 0, ...)
         }
-      }
-      __syncthreads();
-      for (int j = g; j < nb; j += G) {
-        const int e = b0 + j;
-        const float* D = slots + (size_t)j * K::DS;
-        const bool zero = flags[j] != 0.0f;
-        float rad[8];
         if constexpr (RADIAL) {
           const float4* rp = reinterpret_cast<const float4*>(a.R) + 2 * (size_t)e;
-          const float4 r0 = __ldg(rp), r1 = __ldg(rp + 1);
-          rad[0] = r0.x; rad[1] = r0.y; rad[2] = r0.z; rad[3] = r0.w;
-          rad[4] = r1.x; rad[5] = r1.y; rad[6] = r1.z; rad[7] = r1.w;
-          // W[p] = sum_k R[e,k] M[k, p C + c] for every path, into this
-          // thread's column (read only by this thread); eight paths at a time
-          const float* mc = a.M + c;
-          const size_t pc = (size_t)K::P * C;
-#pragma unroll 1
-          for (int p0 = 0; p0 < K::P; p0 += 8) {
-            float m[8][8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-#pragma unroll
-              for (int k = 0; k < 8; ++k)
-                m[q][k] = p0 + q < K::P ? __ldg(mc + k * pc + (size_t)(p0 + q) * C) : 0.0f;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              float w = 0.0f;
-#pragma unroll
-              for (int k = 0; k < 8; ++k) w = fmaf(rad[k], m[q][k], w);
-              if (p0 + q < K::P) ws[(p0 + q) * kHlThreads + t] = w;
-            }
-          }
+          reinterpret_cast<float4*>(rads + 8 * y)[0] = __ldg(rp);
+          reinterpret_cast<float4*>(rads + 8 * y)[1] = __ldg(rp + 1);
         }
-        const int s = __ldg(a.src + e);
-        const bool in_range = (unsigned)s < (unsigned)a.N_src;  // an out-of-range sender adds nothing
-        // stage the sender's row (C * NC floats, contiguous) with coalesced float4s
-        {
-          const float4* src4 = reinterpret_cast<const float4*>(a.x + (size_t)(in_range ? s : 0) * C * NC);
-          float4* xs4 = reinterpret_cast<float4*>(xs);
-          const int n4 = C * NC / 4;
-#pragma unroll
-          for (int v = 0; v < K::XV; ++v) {
-            const int i = c + v * C;
-            if (i < n4) xs4[i] = __ldg(src4 + i);
-          }
-        }
-        group_sync(C, g);
-        if (in_range) {
-          const float* xrs = xs + c * NC;
-          if (!zero) {
-            float xr[NC];
-            xr[0] = xrs[0];
-            rotate_in_all<L>(D, xrs, xr, std::make_integer_sequence<int, L>{});
-            all_blocks<L, RADIAL>(a, ws, c, rad, D, xr, acc, std::make_integer_sequence<int, L + 1>{});
+      }
+      const int cnt = min(q.PB, total - base);
+      for (int j = 0; j < cnt; ++j) {
+        int good = 1;
+        if (lane == j) {
+          const uint32_t s = n % (uint32_t)S, par = ((n / (uint32_t)S) & 1u) ^ 1u;
+          if (mbar_try_wait(empty0 + 8 * s, par) || mbar_wait(empty0 + 8 * s, par, a.watchdog, 2)) {
+            // an out-of-range sender copies row 0; its edge adds nothing
+            const size_t row = (unsigned)node < (unsigned)a.N_src ? (size_t)node : 0;
+            mbar_arrive_expect_tx(full0 + 8 * s, row_bytes);
+            bulk_load(smem_u32(xring + (size_t)s * C * NC), a.x + row * C * NC, row_bytes, full0 + 8 * s);
           } else {
-            zero_len_terms<L, RADIAL>(a, ws, c, rad, xrs, acc, std::make_integer_sequence<int, K::P>{});
+            good = 0;
           }
         }
-        group_sync(C, g);  // the staged row (and radial weights) are rewritten next
+        if (!__all_sync(0xffffffffu, good)) { ok = false; break; }
       }
     }
-    __syncthreads();
+    // Drain: the last min(S, total) copies have landed before this warp leaves.
+    if (lane == 0 && ok) {
+      const uint32_t last = (uint32_t)total;
+      const uint32_t first = last > (uint32_t)S ? last - S : 0;
+      for (uint32_t i = first; i < last; ++i)
+        if (!mbar_wait(full0 + 8 * (i % S), (i / S) & 1u, a.watchdog, 3)) break;
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int g = t / C, c = t % C;
+  float* acc = accs + (size_t)g * NC * C + c;
+  bool failed = false;
+  uint32_t n = 0;
+  for (int r = r_begin; r < r_end; ++r) {
+    const int a0 = min(max(__ldg(a.off + r), 0), a.E);
+    const int a1 = min(max(__ldg(a.off + r + 1), 0), a.E);
+    const int deg = min(max(a1 - a0, 0), total - (int)n);
+#pragma unroll
+    for (int k = 0; k < NC; ++k) acc[k * C] = 0.0f;
+    for (int j = 0; j < deg; ++j) {
+      const uint32_t m = n + j;
+      if ((int)(m % (uint32_t)G) != g) continue;
+      const uint32_t s = m % (uint32_t)S, par = (m / (uint32_t)S) & 1u;
+      if (!mbar_try_wait(full0 + 8 * s, par))
+        if (!mbar_wait_slow(full0 + 8 * s, par, a.watchdog, 1, failed)) failed = true;
+      const int y = (int)(m % (uint32_t)YR);
+      const float* D = slots + (size_t)y * K::DS;
+      const bool zero = flags[y] != 0.0f;
+      const int e = e_begin + (int)m;
+      const int snd = __ldg(a.src + e);
+      float rad[8];
+      if constexpr (RADIAL) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) rad[k] = rads[8 * y + k];
+        // W[p] = sum_k R[e,k] M[k, p C + c] for every path, into this
+        // thread's column (read only by this thread); eight paths at a time
+        const float* mc = a.M + c;
+        const size_t pc = (size_t)K::P * C;
+#pragma unroll 1
+        for (int p0 = 0; p0 < K::P; p0 += 8) {
+          float mm[8][8];
+#pragma unroll
+          for (int qq = 0; qq < 8; ++qq)
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              mm[qq][k] = p0 + qq < K::P ? __ldg(mc + k * pc + (size_t)(p0 + qq) * C) : 0.0f;
+#pragma unroll
+          for (int qq = 0; qq < 8; ++qq) {
+            float w = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) w = fmaf(rad[k], mm[qq][k], w);
+            if (p0 + qq < K::P) ws[(p0 + qq) * kHlThreads + t] = w;
+          }
+        }
+      }
+      if ((unsigned)snd < (unsigned)a.N_src) {  // an out-of-range sender adds nothing
+        const float* xrs = xring + (size_t)s * C * NC + c * NC;
+        if (!zero) {
+          float xr[NC];
+          xr[0] = xrs[0];
+          rotate_in_all<L>(D, xrs, xr, std::make_integer_sequence<int, L>{});
+          all_blocks<L, RADIAL>(a, ws, c, rad, D, xr, acc, std::make_integer_sequence<int, L + 1>{});
+        } else {
+          zero_len_terms<L, RADIAL>(a, ws, c, rad, xrs, acc, std::make_integer_sequence<int, K::P>{});
+        }
+      }
+      // all reads of row slot s and of edge entry y are done
+      mbar_arrive(empty0 + 8 * s);
+    }
+    n += deg;
+    named_barrier(1, kHlThreads);
     // out[r][c][k] = sum over groups in order; thread (g, c) takes k = g, g + G, ...
     float* orow = a.out + ((size_t)r * C + c) * NC;
     for (int k = g; k < NC; k += G) {
@@ -410,24 +480,40 @@ __global__ void __launch_bounds__(kHlThreads) k_hl(const HlArgs a) {
       for (int h = 0; h < G; ++h) v += accs[((size_t)h * NC + k) * C + c];
       orow[k] = v;
     }
-    __syncthreads();  // the partials are zeroed for the next receiver
+    named_barrier(1, kHlThreads);  // the partials are zeroed for the next receiver
   }
 }
 
 template <int L, bool RADIAL>
 eqmp_status launch_hl(const HlArgs& a, cudaStream_t st, const DeviceInfo& dev) {
   auto kern = k_hl<L, RADIAL>;
-  const int smem = HlCfg<L>::smem(a.C, RADIAL);
+  // The ring's slot count is a multiple of the group count, so every slot is
+  // always used by the same group, which takes its edges in order: a
+  // group never waits on a slot more than one phase ahead of it (the parity
+  // wait could not tell that phase from an older one).
+  // A plan that fits two CTAs per SM comes first (a smaller producer batch
+  // if need be), else one CTA per SM.
+  const int G = kHlThreads / a.C;
+  HlPlan q{};
+  bool fit = false;
+  for (int cap : {113 * 1024 - 1024, 227 * 1024 - 1024})
+    for (int pb : {32, 24, 16, 12, 8})
+      for (int S : {8, 16, 4, 2}) {
+        if (fit || S % G != 0) continue;
+        q = hl_plan<L>(a.C, RADIAL, pb, S);
+        fit = q.bytes <= cap;
+      }
+  if (!fit) return EQMP_ERR_UNSUPPORTED;
   static unsigned long long attr_done = 0;
   if (ensure_smem_attr(kern, 227 * 1024, &attr_done) != cudaSuccess) return EQMP_ERR_CUDA;
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kHlThreads, smem) != cudaSuccess || occ < 1)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kHlThreads + 32, q.bytes) != cudaSuccess ||
+      occ < 1)
     return EQMP_ERR_CUDA;
-  const long long want = a.N;  // one receiver per CTA at a time
   const long long cap = (long long)dev.sms * occ;
-  const int grid = (int)(want < cap ? want : cap);
+  const int grid = (int)(a.N < cap ? a.N : cap);
   if (grid <= 0) return EQMP_OK;
-  kern<<<grid, kHlThreads, smem, st>>>(a);
+  kern<<<grid, kHlThreads + 32, q.bytes, st>>>(a, q);
   return cuda_status(cudaGetLastError());
 }
 
@@ -467,12 +553,13 @@ eqmp_status eqmp_fused_lmax(int32_t l_max, const float* vec, const float* x, int
   if (N == 0) return EQMP_OK;
   if (!row_offsets || !out) return EQMP_ERR_INVALID_ARG;
   if (E > 0 && (!vec || !src || !x || N_src < 1)) return EQMP_ERR_INVALID_ARG;
+  if (E > 0 && (reinterpret_cast<uintptr_t>(x) & 15)) return EQMP_ERR_INVALID_ARG;  // rows are bulk-copied
   DeviceInfo dev;
   eqmp_status s = device_info(&dev);
   if (s != EQMP_OK) return s;
   HlArgs a{};
   a.vec = vec; a.x = x; a.off = row_offsets; a.src = src;
-  a.w = weights.w; a.R = weights.R; a.M = weights.M; a.out = out;
+  a.w = weights.w; a.R = weights.R; a.M = weights.M; a.out = out; a.watchdog = dev.watchdog;
   a.N = (int)N; a.E = (int)E; a.N_src = (int)N_src; a.C = C;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   switch (l_max) {

@@ -279,7 +279,8 @@ eqmp_status eqmp_fused_so2(const float* vec, const void* x, int64_t N_src, eqmp_
  * Computed in the aligned frame of E2Former-V2 section 2.1 (Lemma 4.1,
  * Eq. 13: O(l^3) terms per edge instead of the dense O(l^6)); exact up to
  * rounding.
- *   x    [N_src][C][(l_max+1)^2] fp32;  out [N][C][(l_max+1)^2] fp32, written
+ *   x    [N_src][C][(l_max+1)^2] fp32, 16-byte aligned (rows are bulk-copied);
+ *        out [N][C][(l_max+1)^2] fp32, written
  *   weights  shared w[P][C], or radial R[E][8] (16-byte aligned), M[8][P*C]
  *   other arguments as eqmp_fused; C in {8, 16, 32, 64, 128}.
  * EQMP_ERR_UNSUPPORTED for other l_max (l_max = 3 is eqmp_fused).

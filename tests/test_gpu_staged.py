@@ -100,13 +100,15 @@ def test_prepared_staged_call_on_two_streams(eq):
     assert eq.eqmp_device_error() == 0
 
 
-def test_plan_replays_the_staged_step(eq):
+@pytest.mark.parametrize("name", ["pages_1k_c32", "radial_1k_c32"])
+def test_plan_replays_the_staged_step(eq, name):
     """eqmp_plan_staged records the step once; launches on two streams (two
     plans over two buffer sets) give the one-off call's bits, and the plan
-    follows new input contents."""
+    follows new input contents.  Radial weights record the aligned-frame
+    kernel's cluster launch."""
     import torch
 
-    wl = make_workload("pages_1k_c32")
+    wl = make_workload(name)
     sets = []
     for _ in range(2):
         h, d, v = _pack(torch, wl)
@@ -114,10 +116,13 @@ def test_plan_replays_the_staged_step(eq):
         h_out = torch.full(out.shape, float("nan"), dtype=out.dtype).pin_memory()
         sets.append((h, d, v, out, h_out))
     h, d, v, out, h_out = sets[0]
-    eq.eqmp_fused_staged(h, d, v["vec"], v["x"], v["off"], v["src"], out, h_out, w=v["w"])
+    def kw(vv):
+        return dict(w=vv.get("w"), R=vv.get("R"), M=vv.get("M"))
+
+    eq.eqmp_fused_staged(h, d, v["vec"], v["x"], v["off"], v["src"], out, h_out, **kw(v))
     torch.cuda.synchronize()
     ref = h_out.clone()
-    plans = [eq.eqmp_plan_staged(hh, dd, vv["vec"], vv["x"], vv["off"], vv["src"], oo, ho, w=vv["w"])
+    plans = [eq.eqmp_plan_staged(hh, dd, vv["vec"], vv["x"], vv["off"], vv["src"], oo, ho, **kw(vv))
              for hh, dd, vv, oo, ho in sets]
     streams = [torch.cuda.Stream() for _ in range(2)]
     for b in range(2):

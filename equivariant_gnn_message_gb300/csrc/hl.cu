@@ -216,13 +216,36 @@ __device__ __forceinline__ float path_weight(const HlArgs& a, const float* ws, i
 }
 
 // Terms of one path into the output block of its l3 (mp indexed from l3^2).
+// Terms of a path whose |kappa| is equal (the orders m and -m) share one
+// product w |kappa| (about half as many multiplies as terms); the sign goes
+// into the FMA.
+template <int L>
+constexpr float hl_akappa(int i) {
+  return Hl<L>::kTerms[i].kappa < 0.0f ? -Hl<L>::kTerms[i].kappa : Hl<L>::kTerms[i].kappa;
+}
+template <int L, int First, int I>
+constexpr int hl_kappa_slot() {
+  for (int j = 0; j < I; ++j)
+    if (hl_akappa<L>(First + j) == hl_akappa<L>(First + I)) return j;
+  return I;
+}
+template <int L, int First, int O, int I, int NT>
+__device__ __forceinline__ void path_term(float wp, float (&wk)[NT], const float (&xr)[HlCfg<L>::NC],
+                                          float (&mp)[2 * L + 1]) {
+  constexpr tables_hl::HlTerm t = Hl<L>::kTerms[First + I];
+  constexpr int sl = hl_kappa_slot<L, First, I>();
+  if constexpr (sl == I) wk[I] = wp * hl_akappa<L>(First + I);
+  if constexpr (t.kappa < 0.0f) {
+    mp[t.k3 - O] = fmaf(-wk[sl], xr[t.k1], mp[t.k3 - O]);
+  } else {
+    mp[t.k3 - O] = fmaf(wk[sl], xr[t.k1], mp[t.k3 - O]);
+  }
+}
 template <int L, int First, int O, int... Is>
 __device__ __forceinline__ void path_terms(float wp, const float (&xr)[HlCfg<L>::NC], float (&mp)[2 * L + 1],
                                            std::integer_sequence<int, Is...>) {
-  ((mp[Hl<L>::kTerms[First + Is].k3 - O] = fmaf(wp * Hl<L>::kTerms[First + Is].kappa,
-                                                xr[Hl<L>::kTerms[First + Is].k1],
-                                                mp[Hl<L>::kTerms[First + Is].k3 - O])),
-   ...);
+  float wk[sizeof...(Is) > 0 ? sizeof...(Is) : 1];
+  (path_term<L, First, O, Is>(wp, wk, xr, mp), ...);
 }
 
 // Output block l3: the aligned terms of every path ending in l3, each with

@@ -399,6 +399,35 @@ class Timer:
         return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
+def copy_floor_ms(torch, h_in, d_in, h_out, d_out, pairs=20, reps=10):
+    """Device time of one step's copies alone (h_in -> d_in on one stream,
+    d_out -> h_out on another, recorded as a CUDA graph of `pairs` steps):
+    the host link's floor for the pipelined end-to-end step."""
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s1):
+        ev = torch.cuda.Event()
+        ev.record(s1)
+        s2.wait_event(ev)
+        for _ in range(pairs):
+            d_in.copy_(h_in, non_blocking=True)
+            with torch.cuda.stream(s2):
+                h_out.copy_(d_out, non_blocking=True)
+        ev2 = torch.cuda.Event()
+        ev2.record(s2)
+        s1.wait_event(ev2)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / (reps * pairs)
+
+
 def device_inputs(torch, wl, dev):
     t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     d = dict(vec=t(wl.vec), off=t(wl.off), src=t(wl.src), w=t(wl.w), R=t(wl.R), M=t(wl.M))
@@ -571,7 +600,7 @@ def main():
     # inputs sit in one pinned host block (each array 256-byte aligned) and
     # go over in one host->device copy; the result comes back in one copy.
     e2e_ms, h2d, d2h = None, 0, 0
-    pipe_sets, e2e_serial_ms, e2e_mode = None, None, None
+    pipe_sets, e2e_serial_ms, e2e_mode, e2e_copy_floor = None, None, None, None
     if args.which == "forward":
         parts = {"vec": wl.vec, "off": wl.off, "src": wl.src,
                  "x": wl.x_bf16_bits.view(np.int16) if wl.storage == "bf16" else wl.x}
@@ -700,6 +729,7 @@ def main():
             e2e_api = "eqmp_plan_staged + eqmp_plan_launch"
             for p_ in plans:
                 p_.destroy()
+            e2e_copy_floor = copy_floor_ms(torch, h_pack, pipe_sets[0][0], pipe_sets[0][3], pipe_sets[0][2])
 
     # ---- the other full-size workloads, same timing, one entry each
     extra = []
@@ -910,7 +940,8 @@ def main():
         "e2e": None if e2e_ms is None else {
             "value": n_edges * world / (e2e_ms * 1e-3), "unit": "edges/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "api": e2e_api,
-            "mode": e2e_mode, "serial_ms_per_step": e2e_serial_ms},
+            "mode": e2e_mode, "serial_ms_per_step": e2e_serial_ms,
+            "copy_floor_ms_per_step": e2e_copy_floor},
         "pass": args.which,
         "l_max": args.lmax,
         "graph_edges": None if args.which != "graph" else E_graph,

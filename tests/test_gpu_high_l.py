@@ -126,3 +126,53 @@ def test_deterministic_and_argument_errors(eq):
     s = lib.eqmp_fused_lmax(4, d["vec"].data_ptr(), d["x"].data_ptr(), 80, d["off"].data_ptr(),
                             d["src"].data_ptr(), 80, wl.n_edges, 24, W, a.data_ptr(), st)
     assert s == eq.EQMP_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("l_max,C,mode", [(4, 8, "shared"), (4, 32, "radial"), (6, 32, "shared")])
+def test_hub_wraps_the_rings(eq, l_max, C, mode):
+    """A receiver of degree 600 (one CTA's producer batches and row ring wrap
+    many times inside it) beside isolated receivers and a ragged graph,
+    compared receiver by receiver."""
+    from equivariant_gnn_message_gb300.inputs import Workload, csr_offsets
+
+    rng = np.random.default_rng(46)
+    n = 700
+    pos = rng.uniform(0, 30, (n, 3))
+    pairs = [(0, j) for j in range(1, 601)]
+    for r in range(600, 700):
+        pairs += [(r, int(j)) for j in rng.choice(n, int(rng.integers(0, 25)), replace=False) if j != r]
+    pairs = np.asarray(sorted(pairs), dtype=np.int64)
+    dst, src = pairs[:, 0], pairs[:, 1]
+    nc = (l_max + 1) ** 2
+    P = eq.eqmp_num_paths_lmax(l_max)
+    x = rng.standard_normal((n, C, nc)).astype(np.float32)
+    w = (rng.standard_normal((P, C)) / np.sqrt(P)).astype(np.float32) if mode == "shared" else None
+    M = (rng.standard_normal((8, P * C)) / np.sqrt(8)).astype(np.float32) if mode != "shared" else None
+    R = rng.random((len(src), 8)).astype(np.float32) if mode != "shared" else None
+    wl = Workload(name="hub", n_atoms=n, channels=C, storage="f32", vec=(pos[src] - pos[dst]).astype(np.float32),
+                  src=src.astype(np.int32), dst=dst.astype(np.int32), off=csr_offsets(dst, n), x=x,
+                  x_bf16_bits=None, w=w, R=R, M=M)
+    got = _run(eq, l_max, _dev(wl)).astype(np.float64)
+    want = layer.message_pass(wl.vec, wl.x, wl.off, wl.src, **oracle_kw(wl))
+    deg = np.diff(wl.off)
+    assert np.all(got[deg == 0] == 0.0)
+    num = np.linalg.norm((got - want).reshape(n, -1), axis=1)
+    den = np.linalg.norm(want.reshape(n, -1), axis=1)
+    assert np.max(num[deg > 0] / den[deg > 0]) <= TOL
+    assert eq.eqmp_device_error() == 0
+
+
+def test_misaligned_features_are_rejected(eq):
+    """Sender rows are bulk-copied, so x must start on a 16-byte boundary."""
+    import torch
+
+    wl = make_workload(n_atoms=40, cutoff=5.0, channels=8, weights="shared", storage="f32", seed=47, l_max=4)
+    d = _dev(wl)
+    lib = eq.load_library()
+    buf = torch.zeros(d["x"].numel() + 4, dtype=torch.float32, device="cuda")
+    out = torch.empty((40, 8, 25), dtype=torch.float32, device="cuda")
+    W = eq.Weights(d["w"].data_ptr(), None, None, 0)
+    st = torch.cuda.current_stream().cuda_stream
+    s = lib.eqmp_fused_lmax(4, d["vec"].data_ptr(), buf.data_ptr() + 4, 40, d["off"].data_ptr(),
+                            d["src"].data_ptr(), 40, wl.n_edges, 8, W, out.data_ptr(), st)
+    assert s == eq.EQMP_ERR_INVALID_ARG

@@ -203,12 +203,20 @@ __device__ __forceinline__ void rotate_in_all(const float* D, const float* xrow,
                                               std::integer_sequence<int, ls...>) {
   (rotate_in<L, ls + 1>(D, xrow, xr), ...);
 }
-// Weight of path p for this thread's channel: shared weights staged in
-// shared memory (ws[p * C + c]); radial weights of the current edge, formed
-// per thread at the start of the edge (ws[p * 128 + thread]).
-template <int L, bool RADIAL>
+// Weight of path p for this thread's channel.  RADIAL = 0: shared weights
+// staged in shared memory (ws[p * C + c]).  RADIAL = 1: radial weights of
+// the current edge, formed per thread at the start of the edge from M in
+// global memory (ws[p * 128 + thread]).  RADIAL = 2: M staged in shared
+// memory (ws[(k * P + p) * C + c]) and the weight formed here, 8 FMAs.
+template <int L, int RADIAL>
 __device__ __forceinline__ float path_weight(const HlArgs& a, const float* ws, int p, int c, const float (&rad)[8]) {
-  if constexpr (RADIAL) {
+  if constexpr (RADIAL == 2) {
+    constexpr int P = HlCfg<L>::P;
+    float w = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) w = fmaf(rad[k], ws[(k * P + p) * a.C + c], w);
+    return w;
+  } else if constexpr (RADIAL == 1) {
     return ws[p * kHlThreads + threadIdx.x];
   } else {
     return ws[p * a.C + c];
@@ -251,7 +259,7 @@ __device__ __forceinline__ void path_terms(float wp, const float (&xr)[HlCfg<L>:
 // Output block l3: the aligned terms of every path ending in l3, each with
 // its weight, then the rotation back into the accumulators.  Working one
 // output block at a time keeps only 2 l3 + 1 partial outputs live.
-template <int L, bool RADIAL, int L3, int p>
+template <int L, int RADIAL, int L3, int p>
 __device__ __forceinline__ void block_path(const HlArgs& a, const float* ws, int c, const float (&rad)[8],
                                            const float (&xr)[HlCfg<L>::NC], float (&mp)[2 * L + 1]) {
   constexpr tables_hl::HlPath path = Hl<L>::kPaths[p];
@@ -260,7 +268,7 @@ __device__ __forceinline__ void block_path(const HlArgs& a, const float* ws, int
                                        std::make_integer_sequence<int, path.count>{});
 }
 
-template <int L, bool RADIAL, int L3, int... Ps>
+template <int L, int RADIAL, int L3, int... Ps>
 __device__ __forceinline__ void out_block(const HlArgs& a, const float* ws, int c, const float (&rad)[8],
                                           const float* D, const float (&xr)[HlCfg<L>::NC], float* acc,
                                           std::integer_sequence<int, Ps...>) {
@@ -275,7 +283,7 @@ __device__ __forceinline__ void out_block(const HlArgs& a, const float* ws, int 
   }
 }
 
-template <int L, bool RADIAL, int... L3s>
+template <int L, int RADIAL, int... L3s>
 __device__ __forceinline__ void all_blocks(const HlArgs& a, const float* ws, int c, const float (&rad)[8],
                                            const float* D, const float (&xr)[HlCfg<L>::NC], float* acc,
                                            std::integer_sequence<int, L3s...>) {
@@ -283,7 +291,7 @@ __device__ __forceinline__ void all_blocks(const HlArgs& a, const float* ws, int
 }
 
 // Zero-length edge: out_l += W_(l,0,l) Y00 x_l.
-template <int L, bool RADIAL, int p>
+template <int L, int RADIAL, int p>
 __device__ __forceinline__ void zero_len_path(const HlArgs& a, const float* ws, int c, const float (&rad)[8],
                                               const float* xrow, float* acc) {
   constexpr float y00 = 0.28209479177387814f;
@@ -296,7 +304,7 @@ __device__ __forceinline__ void zero_len_path(const HlArgs& a, const float* ws, 
   }
 }
 
-template <int L, bool RADIAL, int... Ps>
+template <int L, int RADIAL, int... Ps>
 __device__ __forceinline__ void zero_len_terms(const HlArgs& a, const float* ws, int c, const float (&rad)[8],
                                                const float* xrow, float* acc, std::integer_sequence<int, Ps...>) {
   (zero_len_path<L, RADIAL, Ps>(a, ws, c, rad, xrow, acc), ...);
@@ -314,7 +322,7 @@ struct HlPlan {
 };
 
 template <int L>
-inline HlPlan hl_plan(int C, bool radial, int pb, int S) {
+inline HlPlan hl_plan(int C, int radial, int pb, int S) {
   using K = HlCfg<L>;
   HlPlan q{};
   q.PB = pb;
@@ -327,7 +335,8 @@ inline HlPlan hl_plan(int C, bool radial, int pb, int S) {
   q.o_acc = up4(q.o_rad + (radial ? 8 * q.YR : 0));
   q.o_x = up4(q.o_acc + K::NC * kHlThreads);
   q.o_w = up4(q.o_x + S * C * K::NC);
-  q.o_bar = up4(q.o_w + (radial ? K::P * kHlThreads : K::P * C));  // barriers, then the range (int4)
+  const int wfloats = radial == 2 ? 8 * K::P * C : radial ? K::P * kHlThreads : K::P * C;
+  q.o_bar = up4(q.o_w + wfloats);  // barriers, then the range (int4)
   q.bytes = q.o_bar * 4 + 2 * S * 8 + 16;
   return q;
 }
@@ -344,7 +353,7 @@ inline HlPlan hl_plan(int C, bool radial, int pb, int S) {
 // the aligned terms with its path weights, rotates back into its partial
 // accumulators (shared memory), and releases the slot.  At each receiver's
 // end the groups' partials are added in group order.
-template <int L, bool RADIAL>
+template <int L, int RADIAL>
 __global__ void __launch_bounds__(kHlThreads + 32, 2) k_hl(const HlArgs a, const HlPlan q) {
   using K = HlCfg<L>;
   constexpr int NC = K::NC;
@@ -367,9 +376,12 @@ __global__ void __launch_bounds__(kHlThreads + 32, 2) k_hl(const HlArgs a, const
     mbar_init(empty0 + 8 * t, C);  // the C threads of the owning group
     fence_mbar_init();
   }
-  if constexpr (!RADIAL) {
+  if constexpr (RADIAL == 0) {
     if (t < kHlThreads)
       for (int i = t; i < K::P * C; i += kHlThreads) ws[i] = __ldg(a.w + i);
+  } else if constexpr (RADIAL == 2) {
+    if (t < kHlThreads)  // M[k][p C + c], the same layout
+      for (int i = t; i < 8 * K::P * C; i += kHlThreads) ws[i] = __ldg(a.M + i);
   }
   __syncthreads();
   const int4 rr = *range_s;
@@ -459,6 +471,8 @@ __global__ void __launch_bounds__(kHlThreads + 32, 2) k_hl(const HlArgs a, const
       if constexpr (RADIAL) {
 #pragma unroll
         for (int k = 0; k < 8; ++k) rad[k] = rads[8 * y + k];
+      }
+      if constexpr (RADIAL == 1) {
         // W[p] = sum_k R[e,k] M[k, p C + c] for every path, into this
         // thread's column (read only by this thread); eight paths at a time
         const float* mc = a.M + c;
@@ -507,26 +521,28 @@ __global__ void __launch_bounds__(kHlThreads + 32, 2) k_hl(const HlArgs a, const
   }
 }
 
-template <int L, bool RADIAL>
-eqmp_status launch_hl(const HlArgs& a, cudaStream_t st, const DeviceInfo& dev) {
-  auto kern = k_hl<L, RADIAL>;
-  // The ring's slot count is a multiple of the group count, so every slot is
-  // always used by the same group, which takes its edges in order: a
-  // group never waits on a slot more than one phase ahead of it (the parity
-  // wait could not tell that phase from an older one).
-  // A plan that fits two CTAs per SM comes first (a smaller producer batch
-  // if need be), else one CTA per SM.
-  const int G = kHlThreads / a.C;
-  HlPlan q{};
-  bool fit = false;
+// The plan for one weight mode: the ring's slot count is a multiple of the
+// group count, so every slot is always used by the same group, which takes
+// its edges in order (a group never waits on a slot more than one phase
+// ahead of it; the parity wait could not tell that phase from an older
+// one).  Plans that fit two CTAs per SM come first (a smaller producer batch
+// if need be), then one CTA per SM.
+template <int L, int RADIAL>
+static bool hl_pick(int C, HlPlan& q) {
+  const int G = kHlThreads / C;
   for (int cap : {113 * 1024 - 1024, 227 * 1024 - 1024})
     for (int pb : {32, 24, 16, 12, 8})
       for (int S : {8, 16, 4, 2}) {
-        if (fit || S % G != 0) continue;
-        q = hl_plan<L>(a.C, RADIAL, pb, S);
-        fit = q.bytes <= cap;
+        if (S % G != 0) continue;
+        q = hl_plan<L>(C, RADIAL, pb, S);
+        if (q.bytes <= cap) return true;
       }
-  if (!fit) return EQMP_ERR_UNSUPPORTED;
+  return false;
+}
+
+template <int L, int RADIAL>
+static eqmp_status launch_hl_plan(const HlArgs& a, const HlPlan& q, cudaStream_t st, const DeviceInfo& dev) {
+  auto kern = k_hl<L, RADIAL>;
   static unsigned long long attr_done = 0;
   if (ensure_smem_attr(kern, 227 * 1024, &attr_done) != cudaSuccess) return EQMP_ERR_CUDA;
   int occ = 0;
@@ -538,6 +554,16 @@ eqmp_status launch_hl(const HlArgs& a, cudaStream_t st, const DeviceInfo& dev) {
   if (grid <= 0) return EQMP_OK;
   kern<<<grid, kHlThreads + 32, q.bytes, st>>>(a, q);
   return cuda_status(cudaGetLastError());
+}
+
+// Radial weights keep M (8 P C floats) in shared memory when it fits beside
+// the rings; otherwise every edge forms its weights from M in global memory.
+template <int L>
+eqmp_status launch_hl(const HlArgs& a, bool radial, cudaStream_t st, const DeviceInfo& dev) {
+  HlPlan q{};
+  if (!radial) return hl_pick<L, 0>(a.C, q) ? launch_hl_plan<L, 0>(a, q, st, dev) : EQMP_ERR_UNSUPPORTED;
+  if (hl_pick<L, 2>(a.C, q)) return launch_hl_plan<L, 2>(a, q, st, dev);
+  return hl_pick<L, 1>(a.C, q) ? launch_hl_plan<L, 1>(a, q, st, dev) : EQMP_ERR_UNSUPPORTED;
 }
 
 int num_paths(int l_max) {
@@ -586,9 +612,9 @@ eqmp_status eqmp_fused_lmax(int32_t l_max, const float* vec, const float* x, int
   a.N = (int)N; a.E = (int)E; a.N_src = (int)N_src; a.C = C;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   switch (l_max) {
-    case 4: return radial ? launch_hl<4, true>(a, st, dev) : launch_hl<4, false>(a, st, dev);
-    case 5: return radial ? launch_hl<5, true>(a, st, dev) : launch_hl<5, false>(a, st, dev);
-    default: return radial ? launch_hl<6, true>(a, st, dev) : launch_hl<6, false>(a, st, dev);
+    case 4: return launch_hl<4>(a, radial, st, dev);
+    case 5: return launch_hl<5>(a, radial, st, dev);
+    default: return launch_hl<6>(a, radial, st, dev);
   }
 }
 

@@ -161,8 +161,8 @@ __device__ __forceinline__ long long block_exclusive(long long v, long long* war
 // Single-pass exclusive scan (decoupled look-back): each block takes the
 // next tile in launch order from a ticket counter, scans it, publishes its
 // aggregate, and adds up its predecessors' published values until it meets
-// an inclusive prefix (tile 0 publishes one at once); then it publishes its
-// own inclusive prefix and writes its tile.  A block waits only for tiles
+// an inclusive prefix (tile 0 publishes one at once), 32 predecessors per
+// read; then it publishes its own inclusive prefix and writes its tile.  A block waits only for tiles
 // that earlier blocks hold, so the scan completes whatever the residency;
 // every wait is bounded (watchdog code 7).  Status words: bits 63..62 flag
 // (1 aggregate, 2 inclusive), 61..0 the value (saturated; a sum that large is
@@ -198,36 +198,52 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_1p(int32_t* __restrict__ 
     s += v[k];
   }
   long long run = block_exclusive(s, warp_tot, &total);
-  if (threadIdx.x == 0) {
+  if (threadIdx.x < 32) {
+    // Look-back by warp 0, 32 predecessors per round: lane i reads tile
+    // j - i.  If one of them holds an inclusive prefix, the values from
+    // lane 0 up to the nearest such lane make up the prefix; otherwise all
+    // 32 are aggregates and the window moves 32 tiles back.  A round whose
+    // needed words are not all published yet is read again.
+    const int lane = threadIdx.x;
     const unsigned long long agg = (unsigned long long)min(total, (long long)kScanVal);
     long long prefix = 0;
     if (t == 0) {
-      st_release_u64(status, kScanIncl | agg);
+      if (lane == 0) st_release_u64(status, kScanIncl | agg);
     } else {
-      st_release_u64(status + t, kScanAgg | agg);
+      if (lane == 0) st_release_u64(status + t, kScanAgg | agg);
       long long j = t - 1;
       const unsigned long long t0 = global_ns();
       while (j >= 0) {
-        const unsigned long long w = ld_acquire_u64g(status + j);
-        if (w == 0ull) {
-          if (global_ns() - t0 > kWaitLimitNs) {
-            watchdog_trip(watchdog, 7);
+        const long long idx = j - lane;
+        const unsigned long long w = idx >= 0 ? ld_acquire_u64g(status + idx) : 0ull;
+        const unsigned incl = __ballot_sync(0xffffffffu, idx >= 0 && (w & kScanIncl) != 0ull);
+        const unsigned zero = __ballot_sync(0xffffffffu, idx >= 0 && w == 0ull);
+        const unsigned need = incl ? (2u << (__ffs(incl) - 1)) - 1u : 0xffffffffu;  // lanes 0 .. nearest inclusive
+        if (zero & need) {
+          // the give-up decision is the warp's, so every lane leaves together
+          if (__any_sync(0xffffffffu, global_ns() - t0 > kWaitLimitNs)) {
+            if (lane == 0) watchdog_trip(watchdog, 7);
             break;
           }
           continue;
         }
-        prefix += (long long)(w & kScanVal);
-        if (w & kScanIncl) break;
-        --j;
+        long long v = ((need >> lane) & 1u) && idx >= 0 ? (long long)(w & kScanVal) : 0ll;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
+        prefix += __shfl_sync(0xffffffffu, v, 0);
+        if (incl) break;
+        j -= 32;
       }
-      st_release_u64(status + t, kScanIncl | (unsigned long long)min(prefix + total, (long long)kScanVal));
+      if (lane == 0) st_release_u64(status + t, kScanIncl | (unsigned long long)min(prefix + total, (long long)kScanVal));
     }
-    prefix_s = prefix;
-    if (e_total && t == (long long)gridDim.x - 1) {  // the last tile knows the grand total
-      long long e = prefix + total;
-      if (e > INT32_MAX) e = -2;
-      if (*bad) e = -1;
-      *e_total = e;
+    if (lane == 0) {
+      prefix_s = prefix;
+      if (e_total && t == (long long)gridDim.x - 1) {  // the last tile knows the grand total
+        long long e = prefix + total;
+        if (e > INT32_MAX) e = -2;
+        if (*bad) e = -1;
+        *e_total = e;
+      }
     }
   }
   __syncthreads();

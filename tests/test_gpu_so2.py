@@ -75,8 +75,9 @@ def test_so2_deterministic(eq):
     assert a.equal(b)
 
 
-@pytest.mark.parametrize("mode", ["shared", "radial"])
-def test_so2_receivers_cut_inside_clusters(eq, mode):
+@pytest.mark.parametrize("mode,C,storage", [("shared", 32, "f32"), ("radial", 32, "f32"),
+                                            ("radial", 8, "bf16"), ("radial", 128, "f32")])
+def test_so2_receivers_cut_inside_clusters(eq, mode, C, storage):
     """Receivers cut between the CTAs of a cluster: a hub of degree 3000 (cut
     across every CTA of one cluster, the middle CTAs holding only part of it),
     three of degree about 200, isolated receivers and a plain ragged graph
@@ -91,7 +92,7 @@ def test_so2_receivers_cut_inside_clusters(eq, mode):
         pairs += [(h, int(j)) for j in rng.choice(n, 200, replace=False) if j != h]
     for r in range(3400, 3600):
         pairs += [(r, int(j)) for j in rng.choice(n, int(rng.integers(0, 30)), replace=False) if j != r]
-    wl = _custom(pos, pairs, mode=mode)
+    wl = _custom(pos, pairs, C=C, storage=storage, mode=mode)
     got = _check(eq, wl).astype(np.float64)
     want = layer.message_pass(wl.vec, wl.x, wl.off, wl.src, **oracle_kw(wl))
     deg = np.diff(wl.off)
@@ -99,4 +100,4 @@ def test_so2_receivers_cut_inside_clusters(eq, mode):
     num = np.linalg.norm((got - want).reshape(n, -1), axis=1)
     den = np.linalg.norm(want.reshape(n, -1), axis=1)
     has = deg > 0
-    assert np.max(num[has] / den[has]) <= 1e-4
+    assert np.max(num[has] / den[has]) <= (1e-4 if storage == "f32" else 2e-2)

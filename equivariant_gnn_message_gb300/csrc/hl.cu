@@ -456,9 +456,10 @@ __global__ void __launch_bounds__(kHlThreads + 32, 2) k_hl(const HlArgs a, const
     const int deg = min(max(a1 - a0, 0), total - (int)n);
 #pragma unroll
     for (int k = 0; k < NC; ++k) acc[k * C] = 0.0f;
-    for (int j = 0; j < deg; ++j) {
+    // the group's edges of this receiver: ordinals n + j with j = j0, j0 + G, ...
+    const int j0 = (int)(((uint32_t)g + (uint32_t)G - n % (uint32_t)G) % (uint32_t)G);
+    for (int j = j0; j < deg; j += G) {
       const uint32_t m = n + j;
-      if ((int)(m % (uint32_t)G) != g) continue;
       const uint32_t s = m % (uint32_t)S, par = (m / (uint32_t)S) & 1u;
       if (!mbar_try_wait(full0 + 8 * s, par))
         if (!mbar_wait_slow(full0 + 8 * s, par, a.watchdog, 1, failed)) failed = true;

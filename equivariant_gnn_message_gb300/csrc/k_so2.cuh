@@ -423,9 +423,10 @@ __global__ void __launch_bounds__(So2Cfg<C, XT, RADIAL>::NTHREADS, So2Cfg<C, XT,
     float out[16];
 #pragma unroll
     for (int k = 0; k < 16; ++k) out[k] = 0.0f;
-    for (int j = 0; j < deg; ++j) {
+    // the group's edges of this receiver: ordinals n + j with j = j0, j0 + EG, ...
+    const int j0 = (int)(((uint32_t)g + (uint32_t)K::EG - n % (uint32_t)K::EG) % (uint32_t)K::EG);
+    for (int j = j0; j < deg; j += K::EG) {
       const uint32_t m = n + j;
-      if ((int)(m % K::EG) != g) continue;
       const uint32_t s = m % S, par = (m / S) & 1u;
       if (!mbar_try_wait(full0 + 8 * s, par))
         if (!mbar_wait_slow(full0 + 8 * s, par, a.watchdog, 1, failed)) failed = true;

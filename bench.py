@@ -69,7 +69,7 @@ PIPE = 6  # streams (and buffer sets) of the pipelined end-to-end measurement
 # profiles/ (None until captured for the current kernel version).
 # Keyed by (workload, kernel version); a changed kernel gets a new version
 # tag, which makes its entry missing (traffic null) until re-captured.
-KERNEL_VERSION = {"shared": "k_shared-pairs-v5", "radial": "k_so2-pairs-v6"}
+KERNEL_VERSION = {"shared": "k_shared-pairs-v5", "radial": "k_so2-pairs-v7"}
 NCU_TRAFFIC = {
     ("pages_1k_c32", "k_shared-pairs-v5"): 2357504 + 0,
     ("scale_100k_c64", "k_shared-pairs-v5"): 6207318016 + 407371008,
@@ -77,6 +77,7 @@ NCU_TRAFFIC = {
     ("radial_1k_c32", "k_so2-v4"): 2888704 + 0,
     ("radial_1k_c32", "k_so2-v5"): 2899456 + 0,
     ("radial_1k_c32", "k_so2-pairs-v6"): 2906368 + 0,
+    ("radial_1k_c32", "k_so2-pairs-v7"): 2906624 + 0,
     ("scale_100k_c64_morton", "k_shared-pairs-v5"): 1679304960 + 394390272,
 }
 

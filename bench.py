@@ -458,7 +458,7 @@ def kernel_version(wl, which, l_max, entry):
     if which == "backward":
         return "k_bwd-v1"
     if l_max != 3:
-        return f"k_hl<{l_max}>-producer-v4"
+        return f"k_hl<{l_max}>-producer-v5"
     if entry == "tp_scatter":
         return "k_sh+" + ("k_shared-tp" if wl.w is not None else "k_radial")
     if entry == "so2":

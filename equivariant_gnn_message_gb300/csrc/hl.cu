@@ -475,10 +475,12 @@ __global__ void __launch_bounds__(kHlThreads + 32, 2) k_hl(const HlArgs a, const
       }
       if constexpr (RADIAL == 1) {
         // W[p] = sum_k R[e,k] M[k, p C + c] for every path, into this
-        // thread's column (read only by this thread); eight paths at a time
+        // thread's column (read only by this thread); eight paths at a time,
+        // two batches unrolled so one batch's loads are in flight while the
+        // other's are summed
         const float* mc = a.M + c;
         const size_t pc = (size_t)K::P * C;
-#pragma unroll 1
+#pragma unroll 2
         for (int p0 = 0; p0 < K::P; p0 += 8) {
           float mm[8][8];
 #pragma unroll
